@@ -1,0 +1,319 @@
+/*
+ * echo.h -- C ABI of the ECHO per-layer decode hot path on one GB300 (sm_103a).
+ *
+ * Sources, cited by page and section:
+ *   [REV]   "ECHO: Efficient KV Cache Offloading with Lossless Prefetching for Serving
+ *           Native Sparse Attention LLMs (OSDI 2026)", review page (awesome-system-papers).
+ *   [NOTES] "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs", podcast show notes.
+ *   [DSA]   DeepSeek-V3.2-Exp report (listed in the show notes' sources): lightning indexer.
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller allocates every buffer (device memory, and pinned host
+ *     memory made device-visible with echo_host_device_pointer).  The library
+ *     allocates nothing, keeps no global state and never synchronises the stream,
+ *     except echo_cache_status / echo_cache_read_counters, which do.
+ *   - Every data-dependent count (misses, prefetched rows, the step number, context
+ *     lengths, the EMA threshold) lives in device memory, so a sequence of calls can
+ *     be captured into one CUDA Graph and replayed step after step [REV] "In-graph
+ *     per-layer cache management"; [NOTES] fixed-size integer tensors on the GPU.
+ *   - Errors: a call returns ECHO_ERR_INVALID_ARG for a null pointer or a bad size,
+ *     ECHO_ERR_UNSUPPORTED for a dtype/shape the kernels do not handle, ECHO_ERR_CUDA
+ *     when a launch fails.  Conditions found on the device set a sticky status word
+ *     (counters[ECHO_CTR_STATUS], first error wins) and the kernels skip the bad
+ *     access instead of trapping; read it with echo_cache_status.
+ *   - Host index of token t of request b is host_base[b] + t: each request owns a
+ *     contiguous range of the model-wide host pool ([REV] "In-graph per-layer cache
+ *     management": the host pool is managed for the whole model).
+ *   - Latent rows are 576 wide (ECHO_KV_WIDTH); attention values are the first 512.
+ */
+#ifndef ECHO_H
+#define ECHO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *echo_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef int32_t echo_status_t;
+enum {
+  ECHO_OK = 0,
+  ECHO_ERR_INVALID_ARG = 1,
+  ECHO_ERR_UNSUPPORTED = 2,
+  ECHO_ERR_CUDA = 3,
+  ECHO_ERR_TIMEOUT = 4,        /* device: a bounded wait gave up                        */
+  ECHO_ERR_POOL_EXHAUSTED = 5, /* device: not enough evictable slots for the tokens    */
+  ECHO_ERR_HOST_INDEX = 6,     /* device: a host index fell outside [0, n_host)        */
+  ECHO_ERR_STAGING = 7         /* device: a request's prefetch cap exceeds its staging  */
+};
+
+enum { ECHO_F32 = 0, ECHO_BF16 = 1, ECHO_E4M3 = 2 };
+
+enum { ECHO_KV_WIDTH = 576, ECHO_V_WIDTH = 512 };
+
+/* Indices into the per-layer counters block (int32[ECHO_NUM_COUNTERS], device). */
+enum {
+  ECHO_CTR_STEP = 0,        /* current decode step s (a write-back begins a step)       */
+  ECHO_CTR_N_FREE = 1,      /* number of free GPU slots                                 */
+  ECHO_CTR_STATUS = 2,      /* sticky device status (ECHO_OK or an ECHO_ERR_*)           */
+  ECHO_CTR_NEED = 3,        /* tokens the current recall must bind to slots             */
+  ECHO_CTR_CURSOR = 4,      /* allocation cursor (scratch)                              */
+  ECHO_CTR_EVICT_M = 5,     /* victims requested by the last eviction                   */
+  ECHO_CTR_HITS = 8,        /* stats, cleared by echo_cache_writeback as a step begins:  */
+  ECHO_CTR_STAGED_HITS = 9, /*   selected & resident / selected & prefetched this step  */
+  ECHO_CTR_MISSES = 10,     /*   selected & copied from the host after the top-k        */
+  ECHO_CTR_EVICTED = 11,    /*   tokens evicted by the recall                           */
+  ECHO_CTR_STAGED = 12,     /*   rows prefetched (staged) during scoring                */
+  ECHO_CTR_WB_EVICTED = 13, /*   tokens evicted by the write-back                       */
+  ECHO_CTR_BOUND = 14,      /*   tokens bound to slots by the recall                    */
+  ECHO_CTR_QUALIFIED = 15,  /*   tokens that met the prefetch rule (before the cap)     */
+  ECHO_NUM_COUNTERS = 32
+};
+
+/*
+ * One layer's GPU cache ([REV] "In-graph per-layer cache management": a
+ * preallocated free bitmap, eviction priorities, index buffers and a bidirectional
+ * host<->GPU map).  Every pointer is caller-owned device memory, except host_kv,
+ * which is the device-visible pointer of a pinned host buffer.
+ *   host2gpu[n_host] : slot of each host token; -1 = not resident; <= -2 = staged in
+ *                      this step at staging row (-2 - value), until the recall binds it
+ *   gpu2host[n_gpu]  : host token in each slot; -1 = free
+ *   priority[n_gpu]  : step of the slot's last touch (LRU key with the host index)
+ *   index_buf[n_gpu] : scratch index buffer used by allocation
+ *   free_map[n_gpu]  : one byte per slot, 1 = free
+ * Metadata = 4*n_host + 13*n_gpu bytes (echo_cache_metadata_bytes) plus the fixed
+ * 128-byte counters block.
+ */
+typedef struct {
+  int32_t n_gpu;
+  int32_t n_host;
+  int32_t *host2gpu;
+  int32_t *gpu2host;
+  int32_t *priority;
+  int32_t *index_buf;
+  uint8_t *free_map;
+  int32_t *counters;   /* [ECHO_NUM_COUNTERS] */
+  void *gpu_kv;        /* [n_gpu, 576], kv_dtype                                  */
+  void *host_kv;       /* [n_host, 576], kv_dtype, pinned host memory (device view) */
+  int32_t kv_dtype;    /* ECHO_F32 or ECHO_BF16                                    */
+} echo_cache_layer_t;
+
+/* Closed form of the per-layer metadata, 4*N_H + 13*N_G bytes
+ * ([REV] "In-graph per-layer cache management": 2M host / 200K GPU slots give
+ * about 10 MB per layer).  Pure host function. */
+size_t echo_cache_metadata_bytes(int64_t n_host, int64_t n_gpu);
+
+/* Device-visible address of pinned host memory (cudaHostGetDevicePointer).
+ * host_ptr must come from cudaHostAlloc / pinned torch memory. */
+echo_status_t echo_host_device_pointer(void *host_ptr, void **dev_ptr);
+
+/* Number of SMs of the current device (for callers sizing persistent work). */
+int32_t echo_device_sm_count(void);
+
+/* Empty cache: every slot free, both maps -1, priorities 0, step 0, counters 0,
+ * n_free = n_gpu.  The cache starts cold. */
+echo_status_t echo_cache_reset(const echo_cache_layer_t *layer, echo_stream_t stream);
+
+/*
+ * A1 -- write-back of each request's new token ([REV] "In-graph per-layer cache
+ * management": KV is backed up to the host when generated, so eviction needs no
+ * copy back; "Trade-offs": every new token is written back).
+ * Begins step s = counters[STEP] + 1.  For b = 0..B-1: h = host_base[b] + seq_len[b];
+ * new_kv[b] (576 values, kv_dtype) is stored to host_kv[h] and to a GPU slot (a free
+ * one, else the resident token with the smallest (priority, host index) among those
+ * with priority < s is evicted); the slot's priority becomes s; new_ik[b] (D values,
+ * ik_dtype) is appended to idx_k[b, seq_len[b]]; seq_len[b] += 1.
+ *   new_kv [B,576] device; new_ik [B,D] device; idx_k [B,Lmax,D] device (in/out);
+ *   host_base [B], seq_len [B] device int32 (seq_len in/out).
+ * Device errors: HOST_INDEX if h >= n_host; POOL_EXHAUSTED if no slot can be freed;
+ * a token whose seq_len has reached Lmax is not appended (INVALID_ARG status).
+ */
+echo_status_t echo_cache_writeback(const echo_cache_layer_t *layer, const void *new_kv,
+                                   const void *new_ik, void *idx_k, int32_t D, int32_t Lmax,
+                                   int32_t ik_dtype, const int32_t *host_base, int32_t *seq_len,
+                                   int32_t B, echo_stream_t stream);
+
+/*
+ * A2 -- reserve the prefetch budget of this step before scoring ([REV] "Decode:
+ * predict the transfer, then recall exactly": a global counter caps the prefetch
+ * volume, and the cap grows with the context).  For each request:
+ * cap[b] = min(cap_max, ceil(seq_len[b] / cap_div)) (cap_div > 0) or cap_max
+ * (cap_div == 0); pf_count[b] = 0.  The per-request staging area holds cap_max rows,
+ * so cap[b] rows of it are reserved.
+ *   seq_len [B], cap [B] (out), pf_count [B] (out) device int32.
+ */
+echo_status_t echo_cache_reserve(const echo_cache_layer_t *layer, const int32_t *seq_len,
+                                 int32_t B, int32_t cap_max, int32_t cap_div, int32_t *cap,
+                                 int32_t *pf_count, echo_stream_t stream);
+
+/*
+ * A3 + A4 -- lightning-indexer scoring with fused threshold prefetch
+ * ([REV] "Problem and motivation": the DSA indexer scores every past token;
+ *  [DSA] score_b(t) = sum_h w[b,h] * ReLU(q[b,h,:] . idx_k[b,t,:]);
+ *  [REV] "Decode: predict the transfer, then recall exactly" and "Fusing prefetch
+ *  into the indexer pipeline": as soon as a block of scores exists, tokens above the
+ *  EMA threshold that are not cached are fetched, without waiting for the top-k).
+ *   q      [B,H,D]  dtype (ECHO_E4M3 with H=64, D=128, or ECHO_F32 with D % 4 == 0)
+ *   w      [B,H]    float32 head weights
+ *   idx_k  [B,Lmax,D] dtype: GPU-resident indexer keys (never offloaded)
+ *   seq_len[B]      device int32, tokens 0..seq_len[b]-1 are scored
+ *   scores [B,Lmax] float32 out (entries >= seq_len[b] untouched)
+ *   theta  [B]      float32 EMA threshold; +inf marks nothing
+ *   cap    [B]      device int32 from echo_cache_reserve, or NULL for no prefetch
+ *   pf_list[B,cap_max] int32 out: prefetched token indices of request b in rows
+ *                   0..pf_count[b]-1 (any order); staging row of pf_list[b,i] is b*cap_max+i
+ *   pf_count[B]     int32 in/out (zeroed by echo_cache_reserve): rows staged
+ *   stage_kv[B*cap_max, 576] kv_dtype out: staged latent rows (host -> GPU copies)
+ * Prefetch rule: t is staged iff score > theta[b] (strict), host2gpu[h] == -1, and t is
+ * among the first cap[b] such tokens by ascending t.  Staged tokens get
+ * host2gpu[h] = -2 - staging_row until echo_cache_recall binds them.
+ * Device errors: STAGING if cap[b] > cap_max; TIMEOUT if a bounded wait gave up.
+ */
+echo_status_t echo_index_prefetch(const void *q, const float *w, const void *idx_k,
+                                  const int32_t *seq_len, int32_t B, int32_t H, int32_t D,
+                                  int32_t Lmax, int32_t dtype, const float *theta,
+                                  const int32_t *cap, int32_t cap_max, const int32_t *host_base,
+                                  const echo_cache_layer_t *layer, float *scores, int32_t *pf_list,
+                                  int32_t *pf_count, void *stage_kv, echo_stream_t stream);
+
+/*
+ * A5 -- exact top-k with the EMA threshold update ([REV] "Problem and motivation":
+ * the 2048 highest-scoring tokens; "Decode: ...": exact top-k after the indexer;
+ * "Key observations" Obs. 2: EMA of the k-th score with smoothing 0.5).
+ * For each b: out_idx[b, 0..k) = the k tokens of largest score (equal scores: lower
+ * token index first), any order; if seq_len[b] < k all tokens are selected and the
+ * rest of the row is -1.  kth[b] = the smallest selected score (-inf if none);
+ * theta[b] <- kth[b] if theta[b] == +inf, else alpha*kth[b] + (1-alpha)*theta[b]
+ * (float32, each operation rounded, no fused multiply-add).
+ *   scores [B,Lmax] float32; seq_len [B]; out_idx [B,k] int32; kth [B]; theta [B] in/out.
+ */
+echo_status_t echo_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax,
+                        int32_t k, int32_t *out_idx, float *kth, float *theta, float alpha,
+                        echo_stream_t stream);
+
+/*
+ * A7 -- eviction with protection ([REV] "In-graph per-layer cache management":
+ * release protects the current selection, then frees low-priority slots and
+ * updates the maps; no data is written back).  Frees
+ * m = max(0, *n_needed - n_free) slots: the resident tokens with the smallest
+ * (priority, host index) among those with priority < current step (everything
+ * touched in this step -- write-back, selection, prefetch bind -- is protected).
+ *   n_needed: device int32 scalar.  Device errors: POOL_EXHAUSTED if fewer than m
+ *   tokens are evictable (all of those are evicted).
+ */
+echo_status_t echo_cache_evict(const echo_cache_layer_t *layer, const int32_t *n_needed,
+                               echo_stream_t stream);
+
+/*
+ * A8 -- allocation by a parallel scan of the free bitmap with one atomic count per
+ * warp ([REV] "In-graph per-layer cache management").  Binds host_idx[0..*n) to
+ * free slots (any slots): maps set, priority = current step, out_slot[i] = slot
+ * (-1 if none was free).  host_idx [n_max], n device scalar (<= n_max), out_slot [n_max].
+ * Device errors: POOL_EXHAUSTED if fewer than *n slots are free; HOST_INDEX.
+ */
+echo_status_t echo_cache_alloc(const echo_cache_layer_t *layer, const int32_t *host_idx,
+                               const int32_t *n, int32_t n_max, int32_t *out_slot,
+                               echo_stream_t stream);
+
+/*
+ * A6 + A7 + A8 + A9 + A10 -- recall after the exact top-k ([REV] "In-graph per-layer
+ * cache management": find the missing entries from the map, allocate slots, and a GPU
+ * kernel reads host memory directly to copy the KV; "Decode: ... recall exactly":
+ * every selected token that is not resident is fetched before attention).
+ * In order: (1) every selected resident token gets priority = step (protection);
+ * (2) misses = selected tokens neither resident nor staged, listed in
+ * miss_list[b, 0..n_miss[b]) (any order); (3) evict so that every staged row and
+ * every miss has a slot (echo_cache_evict rule); (4) bind staged rows (pf_list) and
+ * misses to free slots (echo_cache_alloc rule); (5) copy staged rows from stage_kv
+ * and missed rows from host_kv (zero-copy 16-byte reads of pinned host memory);
+ * (6) slot_idx[b,j] = slot of sel[b,j] (-1 where sel is -1).
+ *   sel [B,k], host_base [B]; pf_list/pf_count/stage_kv as produced by
+ *   echo_index_prefetch (pf_count may be NULL: nothing staged); miss_list [B,k],
+ *   n_miss [B], slot_idx [B,k] out.
+ */
+echo_status_t echo_cache_recall(const echo_cache_layer_t *layer, const int32_t *sel,
+                                const int32_t *host_base, int32_t B, int32_t k,
+                                const int32_t *pf_list, const int32_t *pf_count, int32_t cap_max,
+                                const void *stage_kv, int32_t *miss_list, int32_t *n_miss,
+                                int32_t *slot_idx, echo_stream_t stream);
+
+/*
+ * A11 -- sparse MLA decode attention over the selected rows ([REV] "Problem and
+ * motivation": MLA over the top-2048 tokens; latents are 576 wide, values are the
+ * first 512 dims).  For each b and head h:
+ *   logit_j = scale * q[b,h,:] . kv[slot_idx[b,j], :]   (all 576 dims; -1 skipped)
+ *   out[b,h,:] = softmax_j(logit) . kv[slot_idx[b,j], 0:512];  lse[b,h] = log sum_j exp(logit_j)
+ *   q [B,Hq,576] dtype; kv [kv_rows,576] dtype (a layer's gpu_kv, or any dense
+ *   buffer); out [B,Hq,512] dtype; lse [B,Hq] float32.
+ *   dtype ECHO_BF16 (Hq = 128, tensor cores) or ECHO_F32 (any Hq <= 128).
+ *   workspace: echo_sparse_mla_workspace_bytes(B, Hq, k) bytes of device memory.
+ * A row with no valid entry gives out = 0 and lse = -inf.  The result depends only on
+ * the rows and their order in slot_idx, so attention over the cache equals attention
+ * over any other buffer holding the same rows in the same order (lossless check).
+ */
+size_t echo_sparse_mla_workspace_bytes(int32_t B, int32_t Hq, int32_t k);
+echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, int32_t kv_rows, int32_t dtype,
+                                     const int32_t *slot_idx, int32_t B, int32_t Hq, int32_t k,
+                                     float scale, void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, echo_stream_t stream);
+
+/*
+ * One layer's whole decode step, A1..A11, enqueued on one stream in the pages'
+ * order ([REV] "Decode: predict the transfer, then recall exactly"): write-back,
+ * reserve, score + prefetch, top-k + EMA, recall, sparse MLA.  With prefetch = 0 the
+ * indexer runs without the fused prefetch (the unfused index -> top-k -> recall
+ * sequence).  Every argument keeps the meaning it has in the single calls.
+ */
+typedef struct {
+  int32_t B;
+  const int32_t *host_base; /* [B]                                  */
+  int32_t *seq_len;         /* [B] in/out                           */
+  /* indexer */
+  int32_t H, D, Lmax, idx_dtype;
+  const void *q_idx;        /* [B,H,D]                              */
+  const float *w_idx;       /* [B,H]                                */
+  void *idx_k;              /* [B,Lmax,D]                           */
+  const void *new_ik;       /* [B,D]                                */
+  const void *new_kv;       /* [B,576]                              */
+  float *theta;             /* [B] in/out                           */
+  float alpha;
+  int32_t k;
+  int32_t prefetch;         /* 1 = fused prefetch, 0 = none         */
+  int32_t cap_max, cap_div;
+  int32_t *cap;             /* [B]                                  */
+  float *scores;            /* [B,Lmax]                             */
+  int32_t *pf_list;         /* [B,cap_max]                          */
+  int32_t *pf_count;        /* [B]                                  */
+  void *stage_kv;           /* [B*cap_max,576]                      */
+  int32_t *sel;             /* [B,k]                                */
+  float *kth;               /* [B]                                  */
+  int32_t *miss_list;       /* [B,k]                                */
+  int32_t *n_miss;          /* [B]                                  */
+  int32_t *slot_idx;        /* [B,k]                                */
+  /* attention */
+  int32_t Hq;
+  const void *q_mla;        /* [B,Hq,576]                           */
+  float scale;
+  void *out;                /* [B,Hq,512]                           */
+  float *lse;               /* [B,Hq]                               */
+  void *mla_workspace;
+  size_t mla_workspace_bytes;
+} echo_step_args_t;
+
+echo_status_t echo_decode_layer_step(const echo_cache_layer_t *layer, const echo_step_args_t *a,
+                                     echo_stream_t stream);
+
+/* Synchronises the stream's device and copies counters[ECHO_CTR_STATUS] to
+ * *host_status.  Returns ECHO_ERR_CUDA if the device reported an error. */
+echo_status_t echo_cache_status(const echo_cache_layer_t *layer, int32_t *host_status);
+
+/* Synchronising copy of the whole counters block to host_counters[ECHO_NUM_COUNTERS]. */
+echo_status_t echo_cache_read_counters(const echo_cache_layer_t *layer, int32_t *host_counters);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ECHO_H */

@@ -1,0 +1,235 @@
+// Exact top-k with the EMA threshold update (sm_103a).
+//
+// "ECHO: Efficient KV Cache Offloading with Lossless Prefetching ..." review page:
+//   "Problem and motivation" -- DSA keeps the 2048 highest-scoring tokens;
+//   "Decode: predict the transfer, then recall exactly" -- the final selection is the
+//   exact top-k, computed after the indexer;
+//   "Key observations", Obs. 2 (Fig 7-8) -- the k-th score is tracked by an EMA with
+//   smoothing 0.5, which is the next step's prefetch threshold.
+//
+// One thread-block cluster (8 CTAs x 1024 threads) per request.  Each CTA holds the
+// order-preserving uint32 keys of a contiguous slice of the request's scores in
+// shared memory.  An MSB-first radix select (11 + 11 + 10 bit digits) finds the
+// k-th largest key K*; each CTA histograms its slice and reads the other CTAs'
+// histograms through distributed shared memory, so every CTA derives the same
+// digit with no broadcast step.  Output: every key > K*, then the tokens equal to
+// K* with the lowest indices (ranks ordered across warps and CTAs), so ties go to
+// the lower token index.  The selection order is ascending t within each class.
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace echo {
+
+constexpr int TK_CL = 8;
+constexpr int TK_THREADS = 1024;
+constexpr int TK_BINS = 2048;
+constexpr int TK_KEYCAP = 40 * 1024;   // keys cached per CTA (160 KB)
+
+struct TkShared {
+  uint32_t hist[2][TK_BINS];
+  uint32_t warp_sums[32];
+  uint32_t res[4];
+  uint32_t cta_cnt[2];                  // [0] keys > K*, [1] keys == K* in this CTA
+  uint32_t warp_gt[32], warp_eq[32];
+  uint32_t minkey;
+};
+
+__device__ __forceinline__ uint32_t tk_block_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
+  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= (uint32_t)o) v += n;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= (uint32_t)o) w += n;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  if (wid > 0) v += warp_sums[wid - 1];
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return v;
+}
+
+__device__ __forceinline__ float ema(float theta, float kth, float alpha) {
+  if (isinf(kth) && kth < 0.f) return theta;                 // nothing selected
+  if (isinf(theta) && theta > 0.f) return kth;               // first observation
+  const float a = alpha, b = __fsub_rn(1.0f, alpha);
+  return __fadd_rn(__fmul_rn(a, kth), __fmul_rn(b, theta));  // each op rounded, no FMA
+}
+
+__global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
+    topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
+                float *theta, float alpha) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  TkShared &S = *reinterpret_cast<TkShared *>(dsm);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(dsm + ((sizeof(TkShared) + 15) & ~size_t(15)));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_rank();
+  const int b = blockIdx.x / TK_CL;
+  const int L = min(max(seq_len[b], 0), Lmax);
+  const float *sc = scores + (int64_t)b * Lmax;
+  int32_t *out = out_idx + (int64_t)b * k;
+  const int per = (L + TK_CL - 1) / TK_CL;
+  const int t0 = min(L, (int)rank * per), t1 = min(L, t0 + per);
+  const int n = t1 - t0;
+  const bool cached = per <= TK_KEYCAP;
+
+  if (L <= k) {
+    // every token is selected; kth = smallest score
+    uint32_t mn = 0xffffffffu;
+    for (int i = tid; i < n; i += TK_THREADS) {
+      out[t0 + i] = t0 + i;
+      mn = min(mn, f32_key(sc[t0 + i]));
+    }
+    for (int i = L + (int)rank * TK_THREADS + tid; i < k; i += TK_CL * TK_THREADS) out[i] = -1;
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    if (tid == 0) S.minkey = 0xffffffffu;
+    __syncthreads();
+    if (lane == 0) atomicMin(&S.minkey, mn);
+    __syncthreads();
+    cluster_sync();
+    if (rank == 0 && tid == 0) {
+      uint32_t m = 0xffffffffu;
+      for (uint32_t r = 0; r < TK_CL; ++r) m = min(m, ld_dsmem_u32(map_dsmem(&S.minkey, r)));
+      const float kv = L > 0 ? key_f32(m) : -INFINITY;
+      kth_out[b] = kv;
+      theta[b] = ema(theta[b], kv, alpha);
+    }
+    cluster_sync();
+    return;
+  }
+
+  if (cached)
+    for (int i = tid; i < n; i += TK_THREADS) keys[i] = f32_key(sc[t0 + i]);
+  __syncthreads();
+
+  // ---- radix select of the k-th largest key -----------------------------
+  uint32_t prefix = 0, above = 0;
+  int left = 32, buf = 0;
+  uint32_t eq_total = 0;
+  while (left > 0) {
+    const int w = min(11, left), shift = left - w;
+    uint32_t *h = S.hist[buf];
+    for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
+    __syncthreads();
+    const uint32_t hi_mask = (shift + w >= 32) ? 0u : (0xffffffffu << (shift + w));
+    for (int i = tid; i < n; i += TK_THREADS) {
+      const uint32_t kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+      if ((kk & hi_mask) == (prefix & hi_mask)) atomicAdd(&h[(kk >> shift) & ((1u << w) - 1)], 1u);
+    }
+    __syncthreads();
+    cluster_sync();
+    const int d1 = 2 * tid + 1, d0 = 2 * tid;
+    uint32_t c1 = 0, c0 = 0;
+    for (uint32_t r = 0; r < TK_CL; ++r) {
+      c1 += ld_dsmem_u32(map_dsmem(&h[d1], r));
+      c0 += ld_dsmem_u32(map_dsmem(&h[d0], r));
+    }
+    uint32_t tot;
+    const uint32_t incl = tk_block_scan(c0 + c1, S.warp_sums, &tot);
+    const uint32_t sfx = tot - incl;
+    const uint32_t need = (uint32_t)k - above;
+    if (sfx < need && need <= sfx + c1) { S.res[0] = d1; S.res[1] = sfx; S.res[2] = c1; }
+    else if (sfx + c1 < need && need <= sfx + c1 + c0) { S.res[0] = d0; S.res[1] = sfx + c1; S.res[2] = c0; }
+    __syncthreads();
+    prefix |= S.res[0] << shift;
+    above += S.res[1];
+    eq_total = S.res[2];
+    left = shift;
+    buf ^= 1;
+    __syncthreads();
+  }
+  const uint32_t kstar = prefix;
+  const uint32_t need_eq = (uint32_t)k - above;   // 1 <= need_eq <= eq_total
+  (void)eq_total;
+
+  // ---- ordered output ---------------------------------------------------
+  // warp w of this CTA owns the contiguous sub-range [s0, s1) of the slice
+  const int wspan = (n + 31) / 32;
+  const int s0 = min(n, warp * wspan), s1 = min(n, s0 + wspan);
+  uint32_t gt = 0, eq = 0;
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t kk = 0;
+    if (i < s1) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+    gt += __popc(__ballot_sync(0xffffffffu, i < s1 && kk > kstar));
+    eq += __popc(__ballot_sync(0xffffffffu, i < s1 && kk == kstar));
+  }
+  if (lane == 0) { S.warp_gt[warp] = gt; S.warp_eq[warp] = eq; }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0, e = 0;
+    for (int w = 0; w < 32; ++w) {
+      const uint32_t g = S.warp_gt[w], q = S.warp_eq[w];
+      S.warp_gt[w] = a;
+      S.warp_eq[w] = e;
+      a += g;
+      e += q;
+    }
+    S.cta_cnt[0] = a;
+    S.cta_cnt[1] = e;
+  }
+  __syncthreads();
+  cluster_sync();
+  uint32_t gt_base = 0, eq_base = 0;
+  for (uint32_t r = 0; r < rank; ++r) {
+    gt_base += ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r));
+    eq_base += ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r));
+  }
+  uint32_t gpos = gt_base + S.warp_gt[warp];
+  uint32_t epos = eq_base + S.warp_eq[warp];
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + lane;
+    uint32_t kk = 0;
+    if (i < s1) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+    const bool isg = i < s1 && kk > kstar, ise = i < s1 && kk == kstar;
+    const uint32_t bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
+    if (isg) out[gpos + __popc(bg & lanemask_lt())] = t0 + i;
+    if (ise) {
+      const uint32_t er = epos + __popc(be & lanemask_lt());
+      if (er < need_eq) out[above + er] = t0 + i;
+    }
+    gpos += __popc(bg);
+    epos += __popc(be);
+  }
+  if (rank == 0 && tid == 0) {
+    const float kv = key_f32(kstar);
+    kth_out[b] = kv;
+    theta[b] = ema(theta[b], kv, alpha);
+  }
+  cluster_sync();
+}
+
+static size_t topk_smem(int Lmax) {
+  const int per = (Lmax + TK_CL - 1) / TK_CL;
+  size_t s = (sizeof(TkShared) + 15) & ~size_t(15);
+  if (per <= TK_KEYCAP) s += (size_t)per * 4;
+  return s;
+}
+
+}  // namespace echo
+
+using namespace echo;
+
+extern "C" echo_status_t echo_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t k,
+                                   int32_t *out_idx, float *kth, float *theta, float alpha, echo_stream_t stream) {
+  if (!scores || !seq_len || !out_idx || !kth || !theta || B <= 0 || Lmax <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
+  if (!(alpha >= 0.f && alpha <= 1.f)) return ECHO_ERR_INVALID_ARG;
+  const size_t smem = topk_smem(Lmax);
+  ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  topk_kernel<<<B * TK_CL, TK_THREADS, smem, (cudaStream_t)stream>>>(scores, seq_len, Lmax, k, out_idx, kth, theta,
+                                                                     alpha);
+  ECHO_LAUNCH_OK();
+  return ECHO_OK;
+}

@@ -130,11 +130,13 @@ def workloads() -> dict:
     return out
 
 
-def small_workload(name="small-b3", *, batch=3, ctx=(700, 1500, 333), h_idx=64, d_idx=128, grid=8,
+def small_workload(name="small-b3", *, batch=None, ctx=(700, 1500, 333), h_idx=64, d_idx=128, grid=8,
                    topk=256, h_q=128, kv_fp32=False, n_gpu=2048, steps=4, rho=0.9, cap_max=64,
                    cap_div=0, w_values=None) -> Workload:
     """A small workload that the oracle finishes in seconds but that still spans
     several tiles and a ragged tail."""
+    batch = len(ctx) if batch is None else batch
+    assert batch == len(ctx)
     n_host = sum(c + steps + 8 for c in ctx) + 64
     return Workload(name=name, cfg_id=100, layers=1, batch=batch, ctx=list(ctx), h_idx=h_idx,
                     d_idx=d_idx, grid=grid, w_values=w_values or [i / 16.0 for i in range(1, 17)],
