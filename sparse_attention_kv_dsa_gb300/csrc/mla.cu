@@ -14,6 +14,7 @@
 // attention over any buffer holding the same rows in the same order.
 
 #include <algorithm>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 
@@ -153,6 +154,319 @@ __global__ void mla_combine_kernel(MlaPart part, int S, int Hq, T *out, float *l
 
 static int mla_splits(int k) { return (k + MS_SPLIT - 1) / MS_SPLIT; }
 
+// ===================================================== bf16 tensor-core path ==
+// CTA = (request b, split s of 256 selected entries), all 128 heads.
+//   phase 1  S[128 x 256] = Q . C^T over nine 64-dim chunks: Q chunk by TMA,
+//            gathered C chunk by cp.async into the 128-byte-swizzled K-major
+//            layout; tcgen05.mma kind::f16 M=128 N=256 K=16, f32 in TMEM.
+//   softmax  one thread per head row reads its 256 logits from TMEM, writes bf16
+//            probabilities P[128 x 256] to shared memory (K-major, swizzled).
+//   phase 2  for each half of the 512 value dims: O[128 x 256] = P . V with V
+//            chunks of 32 rows x 256 dims as MN-major operands; the epilogue
+//            writes O / l as bf16 partials, plus (m, l) per head.
+// Warps 0-3 load (cp.async), run the softmax and the epilogues; warp 4 issues the
+// MMAs from one thread.  256 TMEM columns and ~100 KB shared memory per CTA: two
+// CTAs per SM overlap each other's phases.
+constexpr int TC_T = 256;                 // selected entries per CTA
+constexpr int TC_THREADS = 160;
+constexpr int TC_QCH = 128 * 128;         // Q chunk bytes (128 heads x 64 dims)
+constexpr int TC_KCH = TC_T * 128;        // C chunk bytes (256 rows x 64 dims)
+constexpr int TC_STAGE = TC_QCH + TC_KCH; // 48 KB
+constexpr int TC_VCH = 32 * 512;          // V chunk bytes (32 rows x 256 dims)
+constexpr int TC_P = 128 * TC_T * 2;      // 64 KB
+constexpr int TC_REGION = 2 * TC_STAGE;   // 96 KB, phase 1 ring / (P + V ring)
+
+struct TcShared {
+  uint64_t full[2], empty[2], qfull[2];
+  uint64_t s_full, p_full, o_full, o_empty;
+  uint64_t vfull[2], vempty[2];
+  uint32_t tmem_base;
+  int32_t slots[TC_T];
+};
+constexpr size_t TC_SMEM = 1024 + TC_REGION + sizeof(TcShared);
+
+struct TcPart {
+  __nv_bfloat16 *o;   // [B, S, 128, 512] normalised partial outputs
+  float *ml;          // [B, S, 128, 2]
+};
+
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
+  // byte offset of 16-byte chunk `chunk16` of row `row` in a 128B-swizzled
+  // K-major tile whose rows are 128 bytes apart
+  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 2)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __nv_bfloat16 *kv, int kv_rows,
+                  const int32_t *slot_idx, int k, float scale, TcPart part) {
+  extern __shared__ unsigned char tc_raw[];
+  unsigned char *R = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  TcShared &S = *reinterpret_cast<TcShared *>(R + TC_REGION);
+  unsigned char *P = R;                       // phase 2: probabilities
+  unsigned char *V = R + TC_P;                // phase 2: V ring (2 x 16 KB)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s = blockIdx.x, b = blockIdx.y, nsplit = gridDim.x;
+  const int j0 = s * TC_T;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.full[i], 128);
+      mbar_init(&S.empty[i], 1);
+      mbar_init(&S.qfull[i], 1);
+      mbar_init(&S.vfull[i], 128);
+      mbar_init(&S.vempty[i], 1);
+    }
+    mbar_init(&S.s_full, 1);
+    mbar_init(&S.p_full, 128);
+    mbar_init(&S.o_full, 1);
+    mbar_init(&S.o_empty, 128);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < TC_T; i += TC_THREADS) {
+    const int j = j0 + i;
+    int32_t g = j < k ? slot_idx[(int64_t)b * k + j] : -1;
+    S.slots[i] = (g >= 0 && g < kv_rows) ? g : -1;
+  }
+  if (warp == 4) {
+    tmem_alloc(&S.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool ok = true;
+
+  if (warp < 4) {
+    // ------------------------------------------------ phase 1 loads --
+    const int row_base = tid;                          // 128 threads
+    for (int dc = 0; dc < 9; ++dc) {
+      const int st = dc & 1;
+      if (!mbar_wait(&S.empty[st], ((dc >> 1) & 1) ^ 1)) { ok = false; break; }
+      unsigned char *qb = R + st * TC_STAGE, *kb = qb + TC_QCH;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&S.qfull[st], TC_QCH);
+        tma_load_2d(qb, &qmap, &S.qfull[st], dc * 64, b * 128);
+      }
+      // 256 rows x 8 chunks: thread handles chunk (tid & 7) of rows (tid >> 3) + 16 i
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int r = (row_base >> 3) + 16 * i, c = row_base & 7;
+        const int32_t g = S.slots[r];
+        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + dc * 64 + c * 8;
+        cp_async_16(kb + sw128(r, c), src, g >= 0 ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (dc > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&S.full[(dc - 1) & 1]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    mbar_arrive(&S.full[8 & 1]);
+
+    // ------------------------------------------------------ softmax --
+    if (!mbar_wait(&S.s_full, 0)) ok = false;
+    tc_fence_after();
+    // V loads of the first two chunks can start: phase 1 no longer reads smem
+    auto load_v = [&](int vc) {                        // vc = 0..15: half vc/8, rows (vc%8)*32
+      const int st = vc & 1, hf = vc >> 3, r0 = (vc & 7) * 32;
+      unsigned char *vb = V + st * TC_VCH;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = tid + 128 * i;                 // 0..1023 = 32 rows x 32 chunks
+        const int r = idx >> 5, cc = idx & 31;         // chunk cc: dims hf*256 + cc*8
+        const int ac = cc >> 3, c = cc & 7;
+        const int32_t g = S.slots[r0 + r];
+        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + hf * 256 + cc * 8;
+        cp_async_16(vb + ac * 4096 + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
+      }
+      cp_async_commit();
+    };
+    load_v(0);
+    load_v(1);
+    const int h = tid;                                  // head row = TMEM lane
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    float m = -INFINITY;
+    for (int c0 = 0; c0 < TC_T; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(trow + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (S.slots[c0 + j] >= 0) m = fmaxf(m, __uint_as_float(r[j]));
+    }
+    const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
+    float l = 0.f;
+    for (int c0 = 0; c0 < TC_T; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(trow + c0, r);
+      tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float p0 = S.slots[c0 + j] >= 0 ? exp2f((__uint_as_float(r[j]) - m) * c2) : 0.f;
+        float p1 = S.slots[c0 + j + 1] >= 0 ? exp2f((__uint_as_float(r[j + 1]) - m) * c2) : 0.f;
+        l += p0 + p1;
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+        pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+      }
+      // 32 tokens = half an atom column: chunks (c0 % 64)/8 .. +3
+      unsigned char *pa = P + (c0 >> 6) * (128 * 128);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ch = ((c0 & 63) >> 3) + q;
+        *reinterpret_cast<uint4 *>(pa + sw128(h, ch)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                                   pk[4 * q + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&S.p_full);
+
+    // ------------------------------------------- phase 2 loads + epilogue --
+    for (int vc = 0; vc < 16; ++vc) {
+      // chunk vc was issued earlier; make it visible and signal
+      if (vc + 1 < 16) cp_async_wait<1>(); else cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(&S.vfull[vc & 1]);
+      if (vc + 2 < 16) {
+        if (!mbar_wait(&S.vempty[vc & 1], ((vc >> 1) & 1))) { ok = false; }
+        load_v(vc + 2);
+      }
+      if ((vc & 7) == 7) {
+        // epilogue of half vc/8
+        const int hf = vc >> 3;
+        if (!mbar_wait(&S.o_full, hf & 1)) ok = false;
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16 *dst = part.o + ((((int64_t)b * nsplit + s) * 128 + h) * 512 + hf * 256);
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + c0, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+            pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            reinterpret_cast<uint4 *>(dst + c0)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        tc_fence_before();
+        mbar_arrive(&S.o_empty);
+      }
+    }
+    part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
+    part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1] = l;
+  } else if (lane == 0) {
+    // ------------------------------------------------------------- MMA --
+    constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, TC_T);
+    constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 256);
+    for (int dc = 0; dc < 9 && ok; ++dc) {
+      const int st = dc & 1;
+      if (!mbar_wait(&S.qfull[st], (dc >> 1) & 1) || !mbar_wait(&S.full[st], (dc >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t ad = smem_desc(smem_u32(R + st * TC_STAGE), 16, 1024, LAYOUT_SW128);
+      const uint64_t bd = smem_desc(smem_u32(R + st * TC_STAGE + TC_QCH), 16, 1024, LAYOUT_SW128);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, id1, (dc | kk) ? 1u : 0u);
+      mma_commit(&S.empty[st]);
+    }
+    mma_commit(&S.s_full);
+    if (ok && !mbar_wait(&S.p_full, 0)) ok = false;
+    tc_fence_after();
+    for (int vc = 0; vc < 16 && ok; ++vc) {
+      const int st = vc & 1, hf = vc >> 3, tc = vc & 7;
+      if (tc == 0 && hf == 1) {                          // O columns reused: wait for the first epilogue
+        if (!mbar_wait(&S.o_empty, 0)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (!mbar_wait(&S.vfull[st], (vc >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int t0 = tc * 32 + kk * 16;                // token offset in P
+        const uint64_t ad = smem_desc(smem_u32(P + (t0 >> 6) * (128 * 128) + (t0 & 63) * 2), 16, 1024, LAYOUT_SW128);
+        const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH + kk * 2048), 4096, 1024, LAYOUT_SW128);
+        mma_f16(tmem, ad, bd, id2, (tc | kk) ? 1u : 0u);
+      }
+      mma_commit(&S.vempty[st]);
+      if (tc == 7) mma_commit(&S.o_full);
+    }
+  }
+  if (!ok && tid == 0) {
+    // a bounded wait gave up: poison this split so the combine skips it
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, 256);
+}
+
+// Merge the bf16 partials of one (request, head) in split order.
+__global__ void mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out, float *lse) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  __shared__ float wgt[64];
+  __shared__ float Ls, Ms;
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2]);
+    float Lsum = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float m = part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2];
+      const float l = part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1];
+      const float w = (m == -INFINITY || l <= 0.f) ? 0.f : expf(m - M) * l;
+      wgt[s] = w;
+      Lsum += w;
+    }
+    Ls = Lsum;
+    Ms = M;
+  }
+  __syncthreads();
+  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+  for (int d = threadIdx.x * 2; d < V_W; d += blockDim.x * 2) {
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float w = wgt[s];
+      if (w == 0.f) continue;
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(
+          part.o + (((int64_t)b * nsplit + s) * 128 + h) * 512 + d);
+      a0 = fmaf(w, __bfloat162float(v.x), a0);
+      a1 = fmaf(w, __bfloat162float(v.y), a1);
+    }
+    *reinterpret_cast<__nv_bfloat162 *>(out + ((int64_t)b * 128 + h) * V_W + d) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+  }
+  if (threadIdx.x == 0) {
+    // the per-split logits are scaled, so M and lse are in logit units
+    lse[(int64_t)b * 128 + h] = Ls > 0.f ? Ms + logf(Ls) : -INFINITY;
+  }
+}
+
+// Q as a 2-D bf16 tensor [rows, 576] with a [128 rows x 64 dims] box, 128-byte swizzle.
+static bool make_q_map(CUtensorMap *m, const void *base, uint64_t rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  const cuuint64_t dims[2] = {KV_W, rows};
+  const cuuint64_t strides[1] = {KV_W * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace echo
 
 using namespace echo;
@@ -186,12 +500,20 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
     ECHO_LAUNCH_OK();
     mla_combine_kernel<float><<<dim3(Hq, B), 128, 0, st>>>(part, S, Hq, (float *)out, lse);
   } else if (dtype == ECHO_BF16) {
-    ECHO_CUDA_OK(cudaFuncSetAttribute(mla_split_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
-    mla_split_kernel<__nv_bfloat16><<<grid, MS_THREADS, smem, st>>>(
-        (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, Hq, k, scale, part);
+    if (Hq != 128) return ECHO_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(q) & 15) return ECHO_ERR_INVALID_ARG;
+    const int ns = (k + TC_T - 1) / TC_T;
+    if (ns > 64) return ECHO_ERR_UNSUPPORTED;
+    TcPart tp;
+    tp.o = reinterpret_cast<__nv_bfloat16 *>(workspace);
+    tp.ml = reinterpret_cast<float *>(tp.o + (size_t)B * ns * 128 * 512);
+    CUtensorMap qmap;
+    if (!make_q_map(&qmap, q, (uint64_t)B * 128)) return ECHO_ERR_CUDA;
+    ECHO_CUDA_OK(cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM));
+    mla_tc_kernel<<<dim3(ns, B), TC_THREADS, TC_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
+                                                            scale, tp);
     ECHO_LAUNCH_OK();
-    mla_combine_kernel<__nv_bfloat16><<<dim3(Hq, B), 128, 0, st>>>(part, S, Hq, (__nv_bfloat16 *)out, lse);
+    mla_tc_combine_kernel<<<dim3(128, B), 128, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
   } else {
     return ECHO_ERR_UNSUPPORTED;
   }
