@@ -255,6 +255,8 @@ def run_echo(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = S.workloads()[args.workload]
+    if args.layers:
+        wl.layers = int(args.layers)
     layers = wl.layers
     total_steps = args.warmup + args.steps + args.steps + 2
     prefetch = not args.no_prefetch
@@ -510,6 +512,7 @@ def main(argv=None):
     ap.add_argument("--no-prefetch", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-stages", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()

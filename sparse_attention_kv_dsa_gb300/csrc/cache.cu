@@ -231,10 +231,12 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
         for (int i = tid; i < NBINS; i += MG_THREADS) h[i] = 0;
         __syncthreads();
         const uint64_t hi_mask = (shift + w >= 64) ? 0ull : (~0ull << (shift + w));
-        for (int i = tid; i < nloc; i += MG_THREADS) {
-          const uint64_t kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
-          if (kk != 0 && (kk & hi_mask) == (prefix & hi_mask))
-            atomicAdd(&h[(kk >> shift) & ((1u << w) - 1)], 1u);
+        for (int base = 0; base < nloc; base += MG_THREADS) {   // uniform trip count per warp
+          const int i = base + tid;
+          uint64_t kk = 0;
+          if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
+          hist_add_warp(h, kk != 0 && (kk & hi_mask) == (prefix & hi_mask),
+                        (uint32_t)((kk >> shift) & ((1u << w) - 1)));
         }
         __syncthreads();
         cluster_sync();

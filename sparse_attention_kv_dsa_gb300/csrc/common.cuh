@@ -270,3 +270,13 @@ __device__ __forceinline__ void warp_copy_rows4(const uint4 *const (&src)[4], ui
   }
 }
 }  // namespace echo
+
+namespace echo {
+// Histogram increment aggregated over the warp: lanes with the same bin add once
+// (keys of scores and of LRU ages cluster in few bins).  All 32 lanes must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t *h, bool in, uint32_t bin) {
+  const uint32_t key = in ? bin : 0xFFFFFFFFu;
+  const uint32_t m = __match_any_sync(0xFFFFFFFFu, key);
+  if (in && (int)(threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&h[bin], (uint32_t)__popc(m));
+}
+}  // namespace echo

@@ -124,9 +124,11 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
     for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
     __syncthreads();
     const uint32_t hi_mask = (shift + w >= 32) ? 0u : (0xffffffffu << (shift + w));
-    for (int i = tid; i < n; i += TK_THREADS) {
-      const uint32_t kk = cached ? keys[i] : f32_key(sc[t0 + i]);
-      if ((kk & hi_mask) == (prefix & hi_mask)) atomicAdd(&h[(kk >> shift) & ((1u << w) - 1)], 1u);
+    for (int base = 0; base < n; base += TK_THREADS) {     // uniform trip count per warp
+      const int i = base + tid;
+      uint32_t kk = 0;
+      if (i < n) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+      hist_add_warp(h, i < n && (kk & hi_mask) == (prefix & hi_mask), (kk >> shift) & ((1u << w) - 1));
     }
     __syncthreads();
     cluster_sync();
