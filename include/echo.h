@@ -47,7 +47,9 @@ enum {
   ECHO_ERR_TIMEOUT = 4,        /* device: a bounded wait gave up                        */
   ECHO_ERR_POOL_EXHAUSTED = 5, /* device: not enough evictable slots for the tokens    */
   ECHO_ERR_HOST_INDEX = 6,     /* device: a host index fell outside [0, n_host)        */
-  ECHO_ERR_STAGING = 7         /* device: a request's prefetch cap exceeds its staging  */
+  ECHO_ERR_STAGING = 7,        /* device: a request's prefetch cap exceeds its staging  */
+  ECHO_ERR_SCRATCH_LIMIT = 8   /* host: the call needs more than the library's built-in
+                                  scratch (echo_sparse_mla_decode_noalloc only)         */
 };
 
 enum { ECHO_F32 = 0, ECHO_BF16 = 1, ECHO_E4M3 = 2 };
@@ -259,6 +261,33 @@ echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, int32_t kv_r
                                      const int32_t *slot_idx, int32_t B, int32_t Hq, int32_t k,
                                      float scale, void *out, float *lse, void *workspace,
                                      size_t workspace_bytes, echo_stream_t stream);
+
+/*
+ * Sparse MLA decode for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a packaging variant of echo_sparse_mla_decode for code
+ * that may not call cudaMalloc (or any allocating runtime or framework routine) at
+ * run time -- for example a plug-in running inside another engine's memory pool, a
+ * process whose allocator is owned by someone else, or a step being recorded where
+ * allocation is not allowed.  It computes exactly what echo_sparse_mla_decode
+ * computes, with the same arguments minus the workspace: the split partials live in
+ * a scratch array built into the library (ECHO_MLA_NOALLOC_SCRATCH_BYTES, 32 MiB,
+ * held on every GPU that loads the library until the process exits).
+ *   - Sizes: the call needs echo_sparse_mla_workspace_bytes(B, Hq, k) <= 32 MiB
+ *     (for Hq = 128 and k = 2048 that is up to 15 requests); larger calls return
+ *     ECHO_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Set-up: the first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  A failed look-up returns ECHO_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same scratch array, which keeps the
+ *     last call's contents.  Nothing in it has to start at zero (each call writes
+ *     every partial before reading it), but two calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and corrupt each other's
+ *     results: serialise them.
+ */
+#define ECHO_MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+echo_status_t echo_sparse_mla_decode_noalloc(const void *q, const void *kv, int32_t kv_rows, int32_t dtype,
+                                             const int32_t *slot_idx, int32_t B, int32_t Hq, int32_t k,
+                                             float scale, void *out, float *lse, echo_stream_t stream);
 
 /*
  * One layer's whole decode step, A1..A11, enqueued on one stream in the pages'

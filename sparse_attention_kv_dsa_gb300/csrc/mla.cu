@@ -520,3 +520,36 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
   ECHO_LAUNCH_OK();
   return ECHO_OK;
 }
+
+// ----------------------------------------------- variant without allocation --
+// For callers that may not allocate device memory: the split partials go to a
+// scratch array compiled into the library instead of a caller workspace.  Every
+// GPU that loads the library holds the array until the process exits.
+namespace {
+static __device__ __align__(256) unsigned char g_mla_noalloc_scratch[ECHO_MLA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+}  // namespace
+
+extern "C" echo_status_t echo_sparse_mla_decode_noalloc(const void *q, const void *kv, int32_t kv_rows,
+                                                        int32_t dtype, const int32_t *slot_idx, int32_t B,
+                                                        int32_t Hq, int32_t k, float scale, void *out, float *lse,
+                                                        echo_stream_t stream) {
+  if (!q || !kv || !slot_idx || !out || !lse || B <= 0 || Hq <= 0 || k <= 0 || kv_rows <= 0)
+    return ECHO_ERR_INVALID_ARG;
+  const size_t need = echo_sparse_mla_workspace_bytes(B, Hq, k);
+  if (need == 0) return ECHO_ERR_INVALID_ARG;
+  if (need > (size_t)ECHO_MLA_NOALLOC_SCRATCH_BYTES) return ECHO_ERR_SCRATCH_LIMIT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ECHO_ERR_CUDA;
+  if (!g_scratch_addr[dev]) {
+    // host code cannot use the array's name as a device address: look it up once
+    // per device, with that device current
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mla_noalloc_scratch) != cudaSuccess || !p) return ECHO_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  return echo_sparse_mla_decode(q, kv, kv_rows, dtype, slot_idx, B, Hq, k, scale, out, lse, g_scratch_addr[dev],
+                                (size_t)ECHO_MLA_NOALLOC_SCRATCH_BYTES, stream);
+}

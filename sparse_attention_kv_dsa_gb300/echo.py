@@ -16,6 +16,8 @@ from . import build as _build
 
 # ---------------------------------------------------------------- constants --
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_POOL_EXHAUSTED, ERR_HOST_INDEX, ERR_STAGING = range(8)
+ERR_SCRATCH_LIMIT = 8
+MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 F32, BF16, E4M3 = 0, 1, 2
 KV_WIDTH, V_WIDTH = 576, 512
 CTR_STEP, CTR_N_FREE, CTR_STATUS, CTR_NEED, CTR_CURSOR, CTR_EVICT_M = 0, 1, 2, 3, 4, 5
@@ -24,7 +26,7 @@ NUM_COUNTERS = 32
 
 STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                 ERR_TIMEOUT: "TIMEOUT", ERR_POOL_EXHAUSTED: "POOL_EXHAUSTED", ERR_HOST_INDEX: "HOST_INDEX",
-                ERR_STAGING: "STAGING"}
+                ERR_STAGING: "STAGING", ERR_SCRATCH_LIMIT: "SCRATCH_LIMIT"}
 
 
 class EchoError(RuntimeError):
@@ -71,6 +73,7 @@ SIGNATURES = {
     "echo_cache_recall": (_I, [_P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "echo_sparse_mla_workspace_bytes": (_S, [_I, _I, _I]),
     "echo_sparse_mla_decode": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
+    "echo_sparse_mla_decode_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P]),
     "echo_decode_layer_step": (_I, [_P, _P, _P]),
     "echo_cache_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "echo_cache_read_counters": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
@@ -240,3 +243,13 @@ def sparse_mla_decode(q, kv, slot_idx, scale: float, out, lse, workspace, stream
 
 def decode_layer_step(layer: LayerCache, args: StepArgsT, stream=None):
     check(lib().echo_decode_layer_step(layer.ref, ctypes.byref(args), stream_handle(stream)), "decode_layer_step")
+
+
+def sparse_mla_decode_noalloc(q, kv, slot_idx, scale: float, out, lse, stream=None):
+    """echo_sparse_mla_decode without a workspace argument: for callers that may not
+    allocate device memory, the library's built-in scratch holds the partials."""
+    B, Hq, _ = q.shape
+    k = slot_idx.shape[1]
+    check(lib().echo_sparse_mla_decode_noalloc(ptr(q), ptr(kv), kv.shape[0], dtype_code(q.dtype), ptr(slot_idx), B,
+                                               Hq, k, scale, ptr(out), ptr(lse), stream_handle(stream)),
+          "sparse_mla_decode_noalloc")
