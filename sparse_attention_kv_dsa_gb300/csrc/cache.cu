@@ -157,29 +157,17 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
   // B = misses; alloc: A = host_idx[0..n).
   int nA = 0, nB = 0;
   if (P.mode == MODE_WRITEBACK) {
-    if (tid == 0) {
-      int acc = 0;
-      for (int b = 0; b < P.B; ++b) {
-        S.pre_a[b] = acc;
-        const int32_t l = P.seq_len[b];
-        const int64_t h = (int64_t)P.host_base[b] + l;
-        const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
-        acc += (ok && L.host2gpu[h] < 0) ? 1 : 0;
-      }
-      S.pre_a[P.B] = acc;
-    }
+    block_prefix(P.B, [&](int b) {
+      const int32_t l = P.seq_len[b];
+      const int64_t h = (int64_t)P.host_base[b] + l;
+      const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
+      return (ok && L.host2gpu[h] < 0) ? 1 : 0;
+    }, S.pre_a);
   } else if (P.mode == MODE_RECALL) {
-    if (tid == 0) {
-      int a = 0, c = 0;
-      for (int b = 0; b < P.B; ++b) {
-        S.pre_a[b] = a;
-        S.pre_b[b] = c;
-        a += P.pf_count ? min(max(P.pf_count[b], 0), P.cap_max) : 0;
-        c += P.n_miss[b];
-      }
-      S.pre_a[P.B] = a;
-      S.pre_b[P.B] = c;
-    }
+    const int32_t *pfc = P.pf_count;
+    const int cm = P.cap_max;
+    block_prefix(P.B, [&](int b) { return pfc ? min(max(pfc[b], 0), cm) : 0; }, S.pre_a);
+    block_prefix(P.B, [&](int b) { return (int)P.n_miss[b]; }, S.pre_b);
   }
   if (tid == 0) { S.cursor = 0; S.cnt = 0; }
   __syncthreads();
@@ -440,18 +428,8 @@ __global__ void __launch_bounds__(CT_THREADS) copy_translate_kernel(
     const int32_t *pf_count, int cap_max, const void *stage_kv, const int32_t *miss_list, const int32_t *n_miss,
     int32_t *slot_idx) {
   __shared__ int32_t pre_a[MAXB + 1], pre_b[MAXB + 1];
-  if (threadIdx.x == 0) {
-    int a = 0, c = 0;
-    for (int b = 0; b < B; ++b) {
-      pre_a[b] = a;
-      pre_b[b] = c;
-      a += pf_count ? min(max(pf_count[b], 0), cap_max) : 0;
-      c += n_miss[b];
-    }
-    pre_a[B] = a;
-    pre_b[B] = c;
-  }
-  __syncthreads();
+  block_prefix(B, [&](int b) { return pf_count ? min(max(pf_count[b], 0), cap_max) : 0; }, pre_a);
+  block_prefix(B, [&](int b) { return (int)n_miss[b]; }, pre_b);
   const int nA = pre_a[B], n = nA + pre_b[B];
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
   const int chunks = KV_W * esz / 16;                 // 72 (bf16) or 144 (f32)

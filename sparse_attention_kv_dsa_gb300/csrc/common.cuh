@@ -280,3 +280,47 @@ __device__ __forceinline__ void hist_add_warp(uint32_t *h, bool in, uint32_t bin
   if (in && (int)(threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&h[bin], (uint32_t)__popc(m));
 }
 }  // namespace echo
+
+namespace echo {
+// Exclusive prefix of f(0..n-1) into pre[0..n] (pre[n] = total), computed by the
+// whole block in parallel (every thread loads its own value; no serial loop over
+// global loads).  Every thread of the block must call it; it ends with a barrier.
+template <typename F>
+__device__ __forceinline__ void block_prefix(int n, F f, int32_t *pre) {
+  __shared__ int32_t bp_warp[32];
+  __shared__ int32_t bp_carry;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if (threadIdx.x == 0) bp_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int v = i < n ? f(i) : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) bp_warp[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int w = lane < nw ? bp_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      bp_warp[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (wid > 0 ? bp_warp[wid - 1] : 0);
+    const int carry = bp_carry;
+    if (i < n) pre[i] = carry + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 0) bp_carry = carry + bp_warp[nw - 1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) pre[n] = bp_carry;
+  __syncthreads();
+}
+}  // namespace echo

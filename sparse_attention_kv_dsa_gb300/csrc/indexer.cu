@@ -26,6 +26,7 @@
 // outnumber its cap.
 
 #include <algorithm>
+#include <cstddef>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -41,6 +42,8 @@ constexpr int IX_MAXB = 1024;
 constexpr int IX_THREADS = 7 * 32;
 constexpr int IX_KTILE_BYTES = IX_TILE * IX_D;   // 16384
 constexpr int IX_Q_BYTES = IX_H * IX_D;          // 8192
+constexpr int IX_ACC = 4;                        // TMEM accumulator buffers (4 x 64 columns)
+constexpr int IX_WB = 128;                       // requests whose head weights are kept in smem
 
 struct IxParams {
   const float *w;
@@ -59,7 +62,7 @@ struct IxParams {
 
 struct IxSmemTail {
   uint64_t full[IX_STAGES], empty[IX_STAGES];
-  uint64_t qfull[2], qempty[2], tfull[2], tempty[2];
+  uint64_t qfull[2], qempty[2], tfull[IX_ACC], tempty[IX_ACC];
   uint32_t tmem_base;
   uint32_t ring_tail;
   uint32_t ring_head;
@@ -68,8 +71,13 @@ struct IxSmemTail {
   int32_t ring_b[IX_RING];
   int32_t ring_t[IX_RING];
   int32_t ring_seq[IX_RING];
+  alignas(16) float w_s[IX_WB * IX_H];            // head weights of the first IX_WB requests (float4 reads)
+  float theta_s[IX_MAXB];
+  int32_t len_s[IX_MAXB];
 };
 
+static_assert(offsetof(IxSmemTail, w_s) % 16 == 0, "float4 reads of the head weights need 16-byte alignment");
+static_assert((IX_STAGES * IX_KTILE_BYTES + 2 * IX_Q_BYTES) % 1024 == 0, "tail must start 1024-byte aligned");
 constexpr size_t IX_SMEM = 1024 /*align slack*/ + IX_STAGES * IX_KTILE_BYTES + 2 * IX_Q_BYTES + sizeof(IxSmemTail);
 
 __device__ __forceinline__ int find_req(const int32_t *pre, int B, int tile) {
@@ -150,24 +158,26 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.qfull[s], 1);
       mbar_init(&S.qempty[s], 1);
+    }
+    for (int s = 0; s < IX_ACC; ++s) {
       mbar_init(&S.tfull[s], 1);
       mbar_init(&S.tempty[s], 128);
     }
     S.ring_tail = 0;
     S.ring_head = 0;
     S.epi_done = 0;
-    int acc = 0;
-    for (int b = 0; b < P.B; ++b) {
-      S.tile_pre[b] = acc;
-      const int l = min(max(P.seq_len[b], 0), P.Lmax);
-      acc += (l + IX_TILE - 1) / IX_TILE;
-    }
-    S.tile_pre[P.B] = acc;
     fence_mbar_init();
   }
+  block_prefix(P.B, [&](int b) { return (min(max(P.seq_len[b], 0), P.Lmax) + IX_TILE - 1) / IX_TILE; },
+               S.tile_pre);
   for (int i = threadIdx.x; i < IX_RING; i += IX_THREADS) S.ring_seq[i] = 0;
+  for (int i = threadIdx.x; i < min(P.B, IX_WB) * IX_H; i += IX_THREADS) S.w_s[i] = P.w[i];
+  for (int i = threadIdx.x; i < P.B; i += IX_THREADS) {
+    S.theta_s[i] = P.theta[i];
+    S.len_s[i] = min(P.seq_len[i], P.Lmax);
+  }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, 128);
+    tmem_alloc(&S.tmem_base, IX_ACC * IX_H);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -217,8 +227,8 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
         }
         const int s = it % IX_STAGES;
         const uint32_t ph = (it / IX_STAGES) & 1;
-        const int acc = it & 1;
-        if (!mbar_wait(&S.tempty[acc], ((it >> 1) & 1) ^ 1)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
+        const int acc = it % IX_ACC;
+        if (!mbar_wait(&S.tempty[acc], ((it / IX_ACC) & 1) ^ 1)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
         if (!mbar_wait(&S.full[s], ph)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
         tc_fence_after();
         const uint64_t ad = smem_desc(smem_u32(kbuf + s * IX_KTILE_BYTES), 16, 1024, LAYOUT_SW128);
@@ -242,18 +252,18 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
       const int b = find_req(S.tile_pre, P.B, i);
       const int t0 = (i - S.tile_pre[b]) * IX_TILE;
       if (b != cur) {
-        const float4 *wp = reinterpret_cast<const float4 *>(P.w + (int64_t)b * IX_H);
+        const float4 *wp = reinterpret_cast<const float4 *>(b < IX_WB ? S.w_s + b * IX_H : P.w + (int64_t)b * IX_H);
 #pragma unroll
         for (int j = 0; j < IX_H / 4; ++j) {
-          const float4 v = __ldg(wp + j);
+          const float4 v = wp[j];
           wr[4 * j] = v.x; wr[4 * j + 1] = v.y; wr[4 * j + 2] = v.z; wr[4 * j + 3] = v.w;
         }
-        theta = P.theta[b];
-        Lb = min(P.seq_len[b], P.Lmax);
+        theta = S.theta_s[b];
+        Lb = S.len_s[b];
         cur = b;
       }
-      const int acc = it & 1;
-      if (!mbar_wait(&S.tfull[acc], (it >> 1) & 1)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
+      const int acc = it % IX_ACC;
+      if (!mbar_wait(&S.tfull[acc], (it / IX_ACC) & 1)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
       tc_fence_after();
       uint32_t r0[32], r1[32];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + acc * IX_H;
@@ -262,11 +272,16 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&S.tempty[acc]);
-      float sc = 0.f;
+      // four independent partial sums (every partial sum is exact on the grid)
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), sc);
-#pragma unroll
-      for (int h = 0; h < 32; ++h) sc = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), sc);
+      for (int h = 0; h < 32; h += 2) {
+        a0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), a0);
+        a1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), a1);
+        a2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), a2);
+        a3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), a3);
+      }
+      const float sc = (a0 + a1) + (a2 + a3);
       const int t = t0 + row;
       if (t < Lb) {
         P.scores[(int64_t)b * P.Lmax + t] = sc;
@@ -330,7 +345,7 @@ __global__ void __launch_bounds__(IX_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 128);
+  if (warp == 1) tmem_dealloc(tmem, IX_ACC * IX_H);
 }
 
 // ------------------------------------------------------- float32 SIMT path --

@@ -408,43 +408,38 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   if (warp == 4) tmem_dealloc(tmem, 256);
 }
 
-// Merge the bf16 partials of one (request, head) in split order.
-__global__ void mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out, float *lse) {
-  const int h = blockIdx.x, b = blockIdx.y;
-  __shared__ float wgt[64];
-  __shared__ float Ls, Ms;
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2]);
-    float Lsum = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float m = part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2];
-      const float l = part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1];
-      const float w = (m == -INFINITY || l <= 0.f) ? 0.f : expf(m - M) * l;
-      wgt[s] = w;
-      Lsum += w;
+// Merge the bf16 partials of one (request, head) in split order.  A block of 256
+// threads covers 4 heads; each thread produces 8 consecutive output dims.
+__global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out,
+                                                             float *lse) {
+  const int b = blockIdx.y;
+  const int h = blockIdx.x * 4 + (threadIdx.x >> 6);
+  const int d0 = (threadIdx.x & 63) * 8;
+  const float *ml = part.ml + ((int64_t)b * nsplit * 128 + h) * 2;   // split s at ml[s * 256]
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * 256));
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float Lsum = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float m = __ldg(ml + (int64_t)s * 256), l = __ldg(ml + (int64_t)s * 256 + 1);
+    const float w = (m == -INFINITY || l <= 0.f) ? 0.f : expf(m - M) * l;
+    Lsum += w;
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(part.o + (((int64_t)b * nsplit + s) * 128 + h) * 512 + d0));
+    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[2 * j] = fmaf(w, __bfloat162float(p2[j].x), acc[2 * j]);
+      acc[2 * j + 1] = fmaf(w, __bfloat162float(p2[j].y), acc[2 * j + 1]);
     }
-    Ls = Lsum;
-    Ms = M;
   }
-  __syncthreads();
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-  for (int d = threadIdx.x * 2; d < V_W; d += blockDim.x * 2) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = wgt[s];
-      if (w == 0.f) continue;
-      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(
-          part.o + (((int64_t)b * nsplit + s) * 128 + h) * 512 + d);
-      a0 = fmaf(w, __bfloat162float(v.x), a0);
-      a1 = fmaf(w, __bfloat162float(v.y), a1);
-    }
-    *reinterpret_cast<__nv_bfloat162 *>(out + ((int64_t)b * 128 + h) * V_W + d) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-  }
-  if (threadIdx.x == 0) {
-    // the per-split logits are scaled, so M and lse are in logit units
-    lse[(int64_t)b * 128 + h] = Ls > 0.f ? Ms + logf(Ls) : -INFINITY;
-  }
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+  uint4 o;
+  __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o2[j] = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+  *reinterpret_cast<uint4 *>(out + ((int64_t)b * 128 + h) * V_W + d0) = o;
+  // the per-split logits are scaled, so M and lse are in logit units
+  if (d0 == 0) lse[(int64_t)b * 128 + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
 }
 
 // Q as a 2-D bf16 tensor [rows, 576] with a [128 rows x 64 dims] box, 128-byte swizzle.
@@ -501,7 +496,7 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
     mla_combine_kernel<float><<<dim3(Hq, B), 128, 0, st>>>(part, S, Hq, (float *)out, lse);
   } else if (dtype == ECHO_BF16) {
     if (Hq != 128) return ECHO_ERR_UNSUPPORTED;
-    if (reinterpret_cast<uintptr_t>(q) & 15) return ECHO_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return ECHO_ERR_INVALID_ARG;
     const int ns = (k + TC_T - 1) / TC_T;
     if (ns > 64) return ECHO_ERR_UNSUPPORTED;
     TcPart tp;
@@ -513,7 +508,7 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
     mla_tc_kernel<<<dim3(ns, B), TC_THREADS, TC_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
                                                             scale, tp);
     ECHO_LAUNCH_OK();
-    mla_tc_combine_kernel<<<dim3(128, B), 128, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
+    mla_tc_combine_kernel<<<dim3(32, B), 256, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
   } else {
     return ECHO_ERR_UNSUPPORTED;
   }

@@ -7,7 +7,7 @@
 //   "Key observations", Obs. 2 (Fig 7-8) -- the k-th score is tracked by an EMA with
 //   smoothing 0.5, which is the next step's prefetch threshold.
 //
-// One thread-block cluster (8 CTAs x 1024 threads) per request.  Each CTA holds the
+// One thread-block cluster (8 CTAs x 512 threads, two CTAs per SM) per request.  Each CTA holds the
 // order-preserving uint32 keys of a contiguous slice of the request's scores in
 // shared memory.  An MSB-first radix select (11 + 11 + 10 bit digits) finds the
 // k-th largest key K*; each CTA histograms its slice and reads the other CTAs'
@@ -17,22 +17,25 @@
 // the lower token index.  The selection order is ascending t within each class.
 
 #include <algorithm>
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
 namespace echo {
 
 constexpr int TK_CL = 8;
-constexpr int TK_THREADS = 1024;
+constexpr int TK_THREADS = 512;         // two CTAs per SM: all clusters of a batch co-resident
+constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_BINS = 2048;
-constexpr int TK_KEYCAP = 40 * 1024;   // keys cached per CTA (160 KB)
+constexpr int TK_BPT = TK_BINS / TK_THREADS;   // bins per thread (4)
+constexpr int TK_KEYCAP = 23 * 1024;    // keys cached per CTA (92 KB)
 
 struct TkShared {
   uint32_t hist[2][TK_BINS];
   uint32_t warp_sums[32];
   uint32_t res[4];
   uint32_t cta_cnt[2];                  // [0] keys > K*, [1] keys == K* in this CTA
-  uint32_t warp_gt[32], warp_eq[32];
+  uint32_t warp_gt[TK_WARPS], warp_eq[TK_WARPS];
   uint32_t minkey;
 };
 
@@ -68,9 +71,11 @@ __device__ __forceinline__ float ema(float theta, float kth, float alpha) {
   return __fadd_rn(__fmul_rn(a, kth), __fmul_rn(b, theta));  // each op rounded, no FMA
 }
 
-__global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
+__global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
                 float *theta, float alpha) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char dsm[];
   TkShared &S = *reinterpret_cast<TkShared *>(dsm);
   uint32_t *keys = reinterpret_cast<uint32_t *>(dsm + ((sizeof(TkShared) + 15) & ~size_t(15)));
@@ -80,10 +85,11 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
   const int L = min(max(seq_len[b], 0), Lmax);
   const float *sc = scores + (int64_t)b * Lmax;
   int32_t *out = out_idx + (int64_t)b * k;
-  const int per = (L + TK_CL - 1) / TK_CL;
+  const int per = ((L + TK_CL - 1) / TK_CL + 3) & ~3;        // slice length, multiple of 4
   const int t0 = min(L, (int)rank * per), t1 = min(L, t0 + per);
   const int n = t1 - t0;
-  const bool cached = per <= TK_KEYCAP;
+  // keys live in shared memory when the slice for Lmax fits (that is what was allocated)
+  const bool cached = (((Lmax + TK_CL - 1) / TK_CL + 3) & ~3) <= TK_KEYCAP;
 
   if (L <= k) {
     // every token is selected; kth = smallest score
@@ -101,7 +107,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
     cluster_sync();
     if (rank == 0 && tid == 0) {
       uint32_t m = 0xffffffffu;
-      for (uint32_t r = 0; r < TK_CL; ++r) m = min(m, ld_dsmem_u32(map_dsmem(&S.minkey, r)));
+      for (uint32_t r = 0; r < TK_CL; ++r) m = min(m, *cluster.map_shared_rank(&S.minkey, r));
       const float kv = L > 0 ? key_f32(m) : -INFINITY;
       kth_out[b] = kv;
       theta[b] = ema(theta[b], kv, alpha);
@@ -110,14 +116,24 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
     return;
   }
 
-  if (cached)
-    for (int i = tid; i < n; i += TK_THREADS) keys[i] = f32_key(sc[t0 + i]);
+  if (cached) {
+    const float *src = sc + t0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      const int n4 = n >> 2;
+      for (int i = tid; i < n4; i += TK_THREADS) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+        reinterpret_cast<uint4 *>(keys)[i] = make_uint4(f32_key(v.x), f32_key(v.y), f32_key(v.z), f32_key(v.w));
+      }
+      for (int i = 4 * n4 + tid; i < n; i += TK_THREADS) keys[i] = f32_key(src[i]);
+    } else {
+      for (int i = tid; i < n; i += TK_THREADS) keys[i] = f32_key(src[i]);
+    }
+  }
   __syncthreads();
 
   // ---- radix select of the k-th largest key -----------------------------
   uint32_t prefix = 0, above = 0;
   int left = 32, buf = 0;
-  uint32_t eq_total = 0;
   while (left > 0) {
     const int w = min(11, left), shift = left - w;
     uint32_t *h = S.hist[buf];
@@ -132,33 +148,39 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
     }
     __syncthreads();
     cluster_sync();
-    const int d1 = 2 * tid + 1, d0 = 2 * tid;
-    uint32_t c1 = 0, c0 = 0;
+    // cluster-wide counts of this thread's TK_BPT consecutive bins (plain loads,
+    // issued together)
+    uint32_t c[TK_BPT];
+#pragma unroll
+    for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
+#pragma unroll
     for (uint32_t r = 0; r < TK_CL; ++r) {
-      c1 += ld_dsmem_u32(map_dsmem(&h[d1], r));
-      c0 += ld_dsmem_u32(map_dsmem(&h[d0], r));
+      const uint4 v = *reinterpret_cast<const uint4 *>(cluster.map_shared_rank(h + TK_BPT * tid, r));
+      c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
     }
     uint32_t tot;
-    const uint32_t incl = tk_block_scan(c0 + c1, S.warp_sums, &tot);
-    const uint32_t sfx = tot - incl;
+    const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+    const uint32_t incl = tk_block_scan(mine, S.warp_sums, &tot);
+    uint32_t sfx = tot - incl;                              // keys in bins above mine
     const uint32_t need = (uint32_t)k - above;
-    if (sfx < need && need <= sfx + c1) { S.res[0] = d1; S.res[1] = sfx; S.res[2] = c1; }
-    else if (sfx + c1 < need && need <= sfx + c1 + c0) { S.res[0] = d0; S.res[1] = sfx + c1; S.res[2] = c0; }
+#pragma unroll
+    for (int j = TK_BPT - 1; j >= 0; --j) {                 // my bins, from the top
+      if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
+      sfx += c[j];
+    }
     __syncthreads();
     prefix |= S.res[0] << shift;
     above += S.res[1];
-    eq_total = S.res[2];
     left = shift;
     buf ^= 1;
     __syncthreads();
   }
   const uint32_t kstar = prefix;
-  const uint32_t need_eq = (uint32_t)k - above;   // 1 <= need_eq <= eq_total
-  (void)eq_total;
+  const uint32_t need_eq = (uint32_t)k - above;   // 1 <= need_eq <= count of keys == K*
 
   // ---- ordered output ---------------------------------------------------
   // warp w of this CTA owns the contiguous sub-range [s0, s1) of the slice
-  const int wspan = (n + 31) / 32;
+  const int wspan = (n + TK_WARPS - 1) / TK_WARPS;
   const int s0 = min(n, warp * wspan), s1 = min(n, s0 + wspan);
   uint32_t gt = 0, eq = 0;
   for (int i0 = s0; i0 < s1; i0 += 32) {
@@ -172,7 +194,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
   __syncthreads();
   if (tid == 0) {
     uint32_t a = 0, e = 0;
-    for (int w = 0; w < 32; ++w) {
+    for (int w = 0; w < TK_WARPS; ++w) {
       const uint32_t g = S.warp_gt[w], q = S.warp_eq[w];
       S.warp_gt[w] = a;
       S.warp_eq[w] = e;
@@ -186,8 +208,9 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
   cluster_sync();
   uint32_t gt_base = 0, eq_base = 0;
   for (uint32_t r = 0; r < rank; ++r) {
-    gt_base += ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r));
-    eq_base += ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r));
+    const uint32_t *rc = cluster.map_shared_rank(S.cta_cnt, r);
+    gt_base += rc[0];
+    eq_base += rc[1];
   }
   uint32_t gpos = gt_base + S.warp_gt[warp];
   uint32_t epos = eq_base + S.warp_eq[warp];
@@ -214,7 +237,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 1)
 }
 
 static size_t topk_smem(int Lmax) {
-  const int per = (Lmax + TK_CL - 1) / TK_CL;
+  const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
   size_t s = (sizeof(TkShared) + 15) & ~size_t(15);
   if (per <= TK_KEYCAP) s += (size_t)per * 4;
   return s;
