@@ -21,6 +21,7 @@
 //   copy_translate_kernel zero-copy host reads + staged rows into slots, slot ids (A9, A10)
 
 #include <algorithm>
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
@@ -140,6 +141,8 @@ __device__ __forceinline__ uint64_t victim_key(const echo_cache_layer_t &L, int 
 
 template <int CL>
 __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char dsm[];
   MgShared &S = *reinterpret_cast<MgShared *>(dsm);
   uint64_t *keys = reinterpret_cast<uint64_t *>(dsm + ((sizeof(MgShared) + 15) & ~size_t(15)));
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
     __syncthreads();
     cluster_sync();
     uint32_t total = 0;
-    for (uint32_t r = 0; r < CL; ++r) total += ld_dsmem_u32(map_dsmem(&S.cnt, r));
+    for (uint32_t r = 0; r < CL; ++r) total += *cluster.map_shared_rank(&S.cnt, r);
     m_eff = min((uint32_t)m_req, total);
     if (rank == 0 && tid == 0 && m_eff < (uint32_t)m_req) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
 
@@ -231,9 +234,11 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
         // global counts of my two bins; find the digit (descending)
         const int d1 = 2 * tid + 1, d0 = 2 * tid;
         uint32_t c1 = 0, c0 = 0;
-        for (uint32_t r = 0; r < CL; ++r) {
-          c1 += ld_dsmem_u32(map_dsmem(&h[d1], r));
-          c0 += ld_dsmem_u32(map_dsmem(&h[d0], r));
+#pragma unroll
+        for (uint32_t r = 0; r < CL; ++r) {             // plain loads, issued together
+          const uint2 v = *reinterpret_cast<const uint2 *>(cluster.map_shared_rank(&h[d0], r));
+          c0 += v.x;
+          c1 += v.y;
         }
         uint32_t tot;
         const uint32_t incl = block_incl_scan(c0 + c1, S.warp_sums, &tot);
