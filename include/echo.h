@@ -87,7 +87,8 @@ enum {
  *   index_buf[n_gpu] : scratch index buffer used by allocation
  *   free_map[n_gpu]  : one byte per slot, 1 = free
  * Metadata = 4*n_host + 13*n_gpu bytes (echo_cache_metadata_bytes) plus the fixed
- * 128-byte counters block.
+ * 128-byte counters block.  gpu2host and priority must be 16-byte aligned (they are
+ * read as int4 vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t n_gpu;

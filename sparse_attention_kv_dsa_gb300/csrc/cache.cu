@@ -96,6 +96,7 @@ struct MgShared {
   uint32_t res[4];                   // [0] chosen digit, [1] count above it
   uint32_t cursor;                   // allocation cursor (CTA 0's copy is used)
   uint32_t cnt;                      // eligible count of this CTA
+  uint32_t vcnt, vcur;               // victims of this CTA, victim-rank cursor
   int32_t pre_a[MAXB + 1];           // prefixes of the token lists
   int32_t pre_b[MAXB + 1];
 };
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
     block_prefix(P.B, [&](int b) { return pfc ? min(max(pfc[b], 0), cm) : 0; }, S.pre_a);
     block_prefix(P.B, [&](int b) { return (int)P.n_miss[b]; }, S.pre_b);
   }
-  if (tid == 0) { S.cursor = 0; S.cnt = 0; }
+  if (tid == 0) { S.cursor = 0; S.cnt = 0; S.vcnt = 0; S.vcur = 0; }
   __syncthreads();
   if (P.mode == MODE_WRITEBACK) nA = S.pre_a[P.B];
   if (P.mode == MODE_RECALL) { nA = S.pre_a[P.B]; nB = S.pre_b[P.B]; }
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
   if (P.mode == MODE_EVICT) m_req = max(0, *P.n_needed - n_free0);
 
   // ---- this CTA's slot range ----------------------------------------------
-  const int per = (L.n_gpu + CL - 1) / CL;
+  const int per = ((L.n_gpu + CL - 1) / CL + 3) & ~3;     // slices start 16-byte aligned
   const int g0 = min(L.n_gpu, (int)rank * per), g1 = min(L.n_gpu, g0 + per);
   const int nloc = g1 - g0;
   const bool cached = per <= KEYCAP;
@@ -192,12 +193,73 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
   const uint64_t hmax = (1ull << hbits) - 1;
   const int nb = bitlen_u64((uint64_t)max(step, 1)) + hbits + 1;
 
+  // tokens of ranks [0, n_scan) go to slots that were already free (bitmap scan);
+  // tokens of ranks [n_scan, n_bind) go straight to this call's victims
+  const int n_scan = min(max((int)n_free0, 0), n_bind);
+  // host index of the token of rank r
+  auto token_of = [&](uint32_t r, int *req) -> int64_t {
+    if (P.mode == MODE_WRITEBACK) {
+      int b = 0;                                   // rank r -> request (B is small)
+      while (b + 1 < P.B && S.pre_a[b + 1] <= (int)r) ++b;
+      *req = b;
+      return (int64_t)P.host_base[b] + P.seq_len[b];
+    } else if (P.mode == MODE_RECALL) {
+      const int32_t *pre = (int)r < nA ? S.pre_a : S.pre_b;
+      const int rr = (int)r < nA ? (int)r : (int)r - nA;
+      int lo = 0, hi = P.B - 1;                    // last b with pre[b] <= rr
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= rr) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo, ii = rr - pre[b];
+      const int32_t t = (int)r < nA ? P.pf_list[(int64_t)b * P.cap_max + ii] : P.miss_list[(int64_t)b * P.k + ii];
+      *req = b;
+      return (int64_t)P.host_base[b] + t;
+    }
+    *req = 0;
+    return P.host_idx[r];
+  };
+  // bind the token of rank r to slot g (slot already removed from the free bitmap)
+  auto bind = [&](int g, uint32_t r) {
+    int b = 0;
+    const int64_t h = token_of(r, &b);
+    if (h >= 0 && h < L.n_host) {
+      L.free_map[g] = 0;
+      L.gpu2host[g] = (int32_t)h;
+      L.host2gpu[h] = g;
+      L.priority[g] = step;
+      if (P.mode == MODE_WRITEBACK) L.index_buf[b] = g;
+      if (P.mode == MODE_ALLOC && P.out_slot) P.out_slot[r] = g;
+    } else {
+      L.gpu2host[g] = -1;
+      L.free_map[g] = 1;
+      set_status(ctr, ECHO_ERR_HOST_INDEX);
+      if (P.mode == MODE_ALLOC && P.out_slot) P.out_slot[r] = -1;
+    }
+  };
+
   uint32_t m_eff = 0;
   uint64_t kstar = ~0ull;
   if (m_req > 0) {                                         // uniform across the cluster
-    // load keys, count evictable
+    // load keys (4 slots per thread and iteration, both arrays as int4), count evictable
     uint32_t c = 0;
-    for (int i = tid; i < nloc; i += MG_THREADS) {
+    const int n4 = nloc >> 2;
+    const int4 *g2h4 = reinterpret_cast<const int4 *>(L.gpu2host + g0);
+    const int4 *pr4 = reinterpret_cast<const int4 *>(L.priority + g0);
+    auto key_of = [&](int32_t hh, int32_t pp) -> uint64_t {
+      if (hh < 0 || pp >= step || pp < 0) return 0;
+      return (((uint64_t)(int64_t)(step - 1 - pp) << hbits) | (hmax - (uint64_t)hh)) + 1;
+    };
+    for (int j = tid; j < n4; j += MG_THREADS) {
+      const int4 hv = g2h4[j], pv = pr4[j];
+      const uint64_t k0 = key_of(hv.x, pv.x), k1 = key_of(hv.y, pv.y), k2 = key_of(hv.z, pv.z),
+                     k3 = key_of(hv.w, pv.w);
+      if (cached) {
+        keys[4 * j] = k0; keys[4 * j + 1] = k1; keys[4 * j + 2] = k2; keys[4 * j + 3] = k3;
+      }
+      c += (k0 != 0) + (k1 != 0) + (k2 != 0) + (k3 != 0);
+    }
+    for (int i = 4 * n4 + tid; i < nloc; i += MG_THREADS) {
       const uint64_t kk = victim_key(L, g0 + i, step, hbits, hmax);
       if (cached) keys[i] = kk;
       c += kk != 0;
@@ -254,33 +316,56 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
         __syncthreads();
       }
       kstar = prefix;
-      // evict every key >= kstar: exactly m_eff tokens
-      uint32_t ev = 0;
-      for (int i = tid; i < nloc; i += MG_THREADS) {
-        const uint64_t kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
-        if (kk != 0 && kk >= kstar) {
+      // evict every key >= kstar (exactly m_eff tokens).  Victims are ranked across
+      // the cluster (prefix of per-CTA counts; any order inside a CTA) and victim v
+      // is rebound at once to the token of rank n_scan + v, or freed if none is left.
+      uint32_t nv = 0;
+      for (int base = 0; base < nloc; base += MG_THREADS) {
+        const int i = base + tid;
+        uint64_t kk = 0;
+        if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
+        nv += __popc(__ballot_sync(0xffffffffu, kk != 0 && kk >= kstar));
+      }
+      if ((tid & 31) == 0) atomicAdd(&S.vcnt, nv);
+      __syncthreads();
+      cluster_sync();
+      uint32_t vbase = 0;
+      for (uint32_t r = 0; r < rank; ++r) vbase += *cluster.map_shared_rank(&S.vcnt, r);
+      for (int base = 0; base < nloc; base += MG_THREADS) {
+        const int i = base + tid;
+        uint64_t kk = 0;
+        if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
+        const bool isv = kk != 0 && kk >= kstar;
+        const uint32_t bal = __ballot_sync(0xffffffffu, isv);
+        uint32_t wb = 0;
+        if ((tid & 31) == 0 && bal) wb = atomicAdd(&S.vcur, (uint32_t)__popc(bal));
+        wb = __shfl_sync(0xffffffffu, wb, 0);
+        if (isv) {
           const int g = g0 + i;
-          const int32_t hh = L.gpu2host[g];
-          L.host2gpu[hh] = -1;
-          L.gpu2host[g] = -1;
-          L.free_map[g] = 1;
-          ++ev;
+          L.host2gpu[L.gpu2host[g]] = -1;
+          const uint32_t r = (uint32_t)n_scan + vbase + wb + __popc(bal & lanemask_lt());
+          if (r < (uint32_t)n_bind) {
+            bind(g, r);
+          } else {
+            L.gpu2host[g] = -1;
+            L.free_map[g] = 1;
+          }
         }
       }
-      (void)ev;
     }
   }
   cluster_sync();                                      // evictions visible cluster-wide
 
-  // ---- allocation: warp-ballot scan of the free bitmap -------------------
+  // ---- allocation of already-free slots: warp-ballot scan of the free bitmap
+  // with one atomic count per warp (ranks [0, n_scan)) ----------------------
   const uint32_t cursor_addr = map_dsmem(&S.cursor, 0);
-  if (n_bind > 0) {
+  if (n_scan > 0) {
     const int lane = tid & 31;
     for (int base = 0; base < nloc; base += MG_THREADS) {
       // stop early once every token has a slot (one read per warp, uniform)
       uint32_t cur = 0;
       if (lane == 0) cur = ld_dsmem_u32(cursor_addr);
-      if (__shfl_sync(0xffffffffu, cur, 0) >= (uint32_t)n_bind) break;
+      if (__shfl_sync(0xffffffffu, cur, 0) >= (uint32_t)n_scan) break;
       const int i = base + tid;
       const bool fr = i < nloc && L.free_map[g0 + i] != 0;
       const uint32_t bal = __ballot_sync(0xffffffffu, fr);
@@ -293,40 +378,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
       wbase = __shfl_sync(0xffffffffu, wbase, 0);
       if (fr) {
         const uint32_t r = wbase + __popc(bal & lanemask_lt());
-        if (r < (uint32_t)n_bind) {
-          const int g = g0 + i;
-          int64_t h = -1;
-          if (P.mode == MODE_WRITEBACK) {
-            int b = 0;                               // rank r -> request (B is small)
-            while (b + 1 < P.B && S.pre_a[b + 1] <= (int)r) ++b;
-            h = (int64_t)P.host_base[b] + P.seq_len[b];
-            L.index_buf[b] = g;
-          } else if (P.mode == MODE_RECALL) {
-            const int32_t *pre = (int)r < nA ? S.pre_a : S.pre_b;
-            const int rr = (int)r < nA ? (int)r : (int)r - nA;
-            int lo = 0, hi = P.B - 1;                  // last b with pre[b] <= rr
-            while (lo < hi) {
-              const int mid = (lo + hi + 1) >> 1;
-              if (pre[mid] <= rr) lo = mid; else hi = mid - 1;
-            }
-            const int b = lo, ii = rr - pre[b];
-            const int32_t t = (int)r < nA ? P.pf_list[(int64_t)b * P.cap_max + ii]
-                                          : P.miss_list[(int64_t)b * P.k + ii];
-            h = (int64_t)P.host_base[b] + t;
-          } else {
-            h = P.host_idx[r];
-          }
-          if (h >= 0 && h < L.n_host) {
-            L.free_map[g] = 0;
-            L.gpu2host[g] = (int32_t)h;
-            L.host2gpu[h] = g;
-            L.priority[g] = step;
-            if (P.mode == MODE_ALLOC && P.out_slot) P.out_slot[r] = g;
-          } else {
-            set_status(ctr, ECHO_ERR_HOST_INDEX);
-            if (P.mode == MODE_ALLOC && P.out_slot) P.out_slot[r] = -1;
-          }
-        }
+        if (r < (uint32_t)n_scan) bind(g0 + i, r);
       }
     }
   }
@@ -366,7 +418,9 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
   // ---- counters (CTA 0, after everything) ---------------------------------
   cluster_sync();
   if (rank == 0 && tid == 0) {
-    const uint32_t bound = min(S.cursor, (uint32_t)n_bind);
+    const uint32_t bound_scan = min(S.cursor, (uint32_t)n_scan);
+    const uint32_t bound_victims = min(m_eff, (uint32_t)(n_bind - n_scan));
+    const uint32_t bound = bound_scan + bound_victims;
     if (n_bind > 0 && bound < (uint32_t)n_bind) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
     ctr[ECHO_CTR_N_FREE] = n_free0 + (int32_t)m_eff - (int32_t)bound;
     ctr[ECHO_CTR_EVICT_M] = (int32_t)m_eff;
@@ -442,16 +496,13 @@ __global__ void __launch_bounds__(CT_THREADS) copy_translate_kernel(
   const int64_t gw = (blockIdx.x * (int64_t)CT_THREADS + threadIdx.x) >> 5;
   const int64_t nw = (gridDim.x * (int64_t)CT_THREADS) >> 5;
 
-  // rows: r < nA from staging, else from the host pool
+  // rows: r < nA from staging, else from the host pool.  Lane j < CT_ROWS resolves
+  // row r0 + j (list entry, host index, slot) so the 4 lookups run in parallel.
   for (int64_t r0 = gw * CT_ROWS; r0 < n; r0 += nw * CT_ROWS) {
-    const uint4 *src[CT_ROWS];
-    uint4 *dst[CT_ROWS];
-#pragma unroll
-    for (int j = 0; j < CT_ROWS; ++j) {
-      src[j] = nullptr;
-      dst[j] = nullptr;
-      const int64_t r = r0 + j;
-      if (r >= n) continue;
+    const uint4 *my_src = nullptr;
+    uint4 *my_dst = nullptr;
+    const int64_t r = r0 + lane;
+    if (lane < CT_ROWS && r < n) {
       const bool staged = r < nA;
       const int32_t *pre = staged ? pre_a : pre_b;
       const int rr = staged ? (int)r : (int)(r - nA);
@@ -463,31 +514,24 @@ __global__ void __launch_bounds__(CT_THREADS) copy_translate_kernel(
       const int b = lo, ii = rr - pre[b];
       const int32_t t = staged ? pf_list[(int64_t)b * cap_max + ii] : miss_list[(int64_t)b * k + ii];
       const int64_t h = (int64_t)host_base[b] + t;
-      if (h < 0 || h >= L.n_host) continue;
-      const int32_t g = L.host2gpu[h];
-      if (g < 0) continue;                                  // pool exhausted: not bound
-      src[j] = staged ? reinterpret_cast<const uint4 *>((const char *)stage_kv +
-                                                        ((int64_t)b * cap_max + ii) * KV_W * esz)
-                      : reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * KV_W * esz);
-      dst[j] = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz);
-    }
-    for (int c0 = 0; c0 < chunks; c0 += 96) {
-      uint4 v[CT_ROWS][3];
-#pragma unroll
-      for (int j = 0; j < CT_ROWS; ++j)
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int c = c0 + lane + 32 * u;
-          if (src[j] && c < chunks && c < c0 + 96) v[j][u] = __ldg(src[j] + c);
+      if (h >= 0 && h < L.n_host) {
+        const int32_t g = L.host2gpu[h];
+        if (g >= 0) {                                       // not bound: pool exhausted
+          my_src = staged ? reinterpret_cast<const uint4 *>((const char *)stage_kv +
+                                                            ((int64_t)b * cap_max + ii) * KV_W * esz)
+                          : reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * KV_W * esz);
+          my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz);
         }
-#pragma unroll
-      for (int j = 0; j < CT_ROWS; ++j)
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int c = c0 + lane + 32 * u;
-          if (src[j] && c < chunks && c < c0 + 96) dst[j][c] = v[j][u];
-        }
+      }
     }
+    const uint4 *src[CT_ROWS];
+    uint4 *dst[CT_ROWS];
+#pragma unroll
+    for (int j = 0; j < CT_ROWS; ++j) {
+      src[j] = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), j));
+      dst[j] = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), j));
+    }
+    warp_copy_rows4(src, dst, chunks);
   }
 
   // slot translation for every selected entry (A10)
@@ -509,7 +553,7 @@ __global__ void __launch_bounds__(CT_THREADS) copy_translate_kernel(
 static int g_cluster = 0;  // chosen cluster size for manage_kernel (16 if allowed, else 8)
 
 static size_t manage_smem(int CL, int n_gpu) {
-  const int per = (n_gpu + CL - 1) / CL;
+  const int per = ((n_gpu + CL - 1) / CL + 3) & ~3;
   size_t s = (sizeof(MgShared) + 15) & ~size_t(15);
   if (per <= KEYCAP) s += (size_t)per * 8;
   return s;
@@ -572,7 +616,8 @@ static cudaError_t run_manage(const ManageParams &P, cudaStream_t st) {
 static bool layer_ok(const echo_cache_layer_t *L) {
   return L && L->n_gpu > 0 && L->n_host > 0 && L->host2gpu && L->gpu2host && L->priority && L->index_buf &&
          L->free_map && L->counters && L->gpu_kv && L->host_kv &&
-         (L->kv_dtype == ECHO_F32 || L->kv_dtype == ECHO_BF16);
+         (L->kv_dtype == ECHO_F32 || L->kv_dtype == ECHO_BF16) &&
+         ((reinterpret_cast<uintptr_t>(L->gpu2host) | reinterpret_cast<uintptr_t>(L->priority)) & 15) == 0;
 }
 
 int sm_count() {

@@ -172,16 +172,21 @@ constexpr int TC_THREADS = 160;
 constexpr int TC_QCH = 128 * 128;         // Q chunk bytes (128 heads x 64 dims)
 constexpr int TC_KCH = TC_T * 128;        // C chunk bytes (256 rows x 64 dims)
 constexpr int TC_STAGE = TC_QCH + TC_KCH; // 48 KB
-constexpr int TC_VCH = 32 * 512;          // V chunk bytes (32 rows x 256 dims)
+constexpr int TC_VROWS = 16;              // rows per V chunk (one K-step)
+constexpr int TC_VCH = TC_VROWS * 512;    // V chunk bytes (16 rows x 256 dims)
+constexpr int TC_VST = 4;                 // V ring stages
+constexpr int TC_NV = 2 * TC_T / TC_VROWS; // V chunks per CTA (two halves)
 constexpr int TC_P = 128 * TC_T * 2;      // 64 KB
 constexpr int TC_REGION = 2 * TC_STAGE;   // 96 KB, phase 1 ring / (P + V ring)
+static_assert(TC_P + TC_VST * TC_VCH <= TC_REGION, "P and the V ring share the phase-1 region");
 
 struct TcShared {
   uint64_t full[2], empty[2], qfull[2];
   uint64_t s_full, p_full, o_full, o_empty;
-  uint64_t vfull[2], vempty[2];
+  uint64_t vfull[TC_VST], vempty[TC_VST];
   uint32_t tmem_base;
   int32_t slots[TC_T];
+  uint32_t vmask[TC_T / 32];
 };
 constexpr size_t TC_SMEM = 1024 + TC_REGION + sizeof(TcShared);
 
@@ -213,6 +218,8 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       mbar_init(&S.full[i], 128);
       mbar_init(&S.empty[i], 1);
       mbar_init(&S.qfull[i], 1);
+    }
+    for (int i = 0; i < TC_VST; ++i) {
       mbar_init(&S.vfull[i], 128);
       mbar_init(&S.vempty[i], 1);
     }
@@ -225,7 +232,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   for (int i = tid; i < TC_T; i += TC_THREADS) {
     const int j = j0 + i;
     int32_t g = j < k ? slot_idx[(int64_t)b * k + j] : -1;
-    S.slots[i] = (g >= 0 && g < kv_rows) ? g : -1;
+    g = (g >= 0 && g < kv_rows) ? g : -1;
+    S.slots[i] = g;
+    const uint32_t bal = __ballot_sync(0xffffffffu, g >= 0);   // whole warps: 160 and 256 are multiples of 32
+    if (lane == 0) S.vmask[i >> 5] = bal;
   }
   if (warp == 4) {
     tmem_alloc(&S.tmem_base, 256);
@@ -270,50 +280,54 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     // ------------------------------------------------------ softmax --
     if (!mbar_wait(&S.s_full, 0)) ok = false;
     tc_fence_after();
-    // V loads of the first two chunks can start: phase 1 no longer reads smem
-    auto load_v = [&](int vc) {                        // vc = 0..15: half vc/8, rows (vc%8)*32
-      const int st = vc & 1, hf = vc >> 3, r0 = (vc & 7) * 32;
+    // V loads of the first chunks can start: phase 1 no longer reads smem
+    constexpr int NV2 = TC_NV / 2;                     // chunks per half
+    auto load_v = [&](int vc) {                        // half vc / NV2, rows (vc % NV2) * 16
+      const int st = vc % TC_VST, hf = vc / NV2, r0 = (vc % NV2) * TC_VROWS;
       unsigned char *vb = V + st * TC_VCH;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = tid + 128 * i;                 // 0..1023 = 32 rows x 32 chunks
+      for (int i = 0; i < TC_VROWS * 32 / 128; ++i) {
+        const int idx = tid + 128 * i;                 // rows x 32 chunks of 16 B
         const int r = idx >> 5, cc = idx & 31;         // chunk cc: dims hf*256 + cc*8
         const int ac = cc >> 3, c = cc & 7;
         const int32_t g = S.slots[r0 + r];
         const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + hf * 256 + cc * 8;
-        cp_async_16(vb + ac * 4096 + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
+        cp_async_16(vb + ac * (TC_VROWS * 128) + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
       }
       cp_async_commit();
     };
-    load_v(0);
-    load_v(1);
+    for (int vc = 0; vc < TC_VST; ++vc) load_v(vc);
+    // validity of the 256 entries as a bit mask (written before the first barrier)
+    const uint32_t *vmask = S.vmask;
     const int h = tid;                                  // head row = TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     float m = -INFINITY;
-    for (int c0 = 0; c0 < TC_T; c0 += 32) {
-      uint32_t r[32];
+    for (int c0 = 0; c0 < TC_T; c0 += 64) {                // two TMEM loads per wait
+      uint32_t r[32], r2[32];
       tmem_ld32(trow + c0, r);
+      tmem_ld32(trow + c0 + 32, r2);
       tmem_wait_ld();
+      const uint32_t vm = vmask[c0 >> 5], vm2 = vmask[(c0 >> 5) + 1];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (S.slots[c0 + j] >= 0) m = fmaxf(m, __uint_as_float(r[j]));
+      for (int j = 0; j < 32; ++j) {
+        if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]));
+        if ((vm2 >> j) & 1u) m = fmaxf(m, __uint_as_float(r2[j]));
+      }
     }
     const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
+    const float mc = m * c2;
     float l = 0.f;
-    for (int c0 = 0; c0 < TC_T; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(trow + c0, r);
-      tmem_wait_ld();
+    // 32 probabilities -> bf16 -> four 16-byte chunks of P (half an atom column)
+    auto write_p = [&](int c0, const uint32_t (&r)[32], uint32_t vm) {
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        float p0 = S.slots[c0 + j] >= 0 ? exp2f((__uint_as_float(r[j]) - m) * c2) : 0.f;
-        float p1 = S.slots[c0 + j + 1] >= 0 ? exp2f((__uint_as_float(r[j + 1]) - m) * c2) : 0.f;
+        const float p0 = ((vm >> j) & 1u) ? exp2f(fmaf(__uint_as_float(r[j]), c2, -mc)) : 0.f;
+        const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[j + 1]), c2, -mc)) : 0.f;
         l += p0 + p1;
         __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
         pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
       }
-      // 32 tokens = half an atom column: chunks (c0 % 64)/8 .. +3
       unsigned char *pa = P + (c0 >> 6) * (128 * 128);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -321,32 +335,43 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         *reinterpret_cast<uint4 *>(pa + sw128(h, ch)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
                                                                    pk[4 * q + 3]);
       }
+    };
+    for (int c0 = 0; c0 < TC_T; c0 += 64) {                // two TMEM loads per wait
+      uint32_t r[32], r2[32];
+      tmem_ld32(trow + c0, r);
+      tmem_ld32(trow + c0 + 32, r2);
+      tmem_wait_ld();
+      write_p(c0, r, vmask[c0 >> 5]);
+      write_p(c0 + 32, r2, vmask[(c0 >> 5) + 1]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&S.p_full);
 
     // ------------------------------------------- phase 2 loads + epilogue --
-    for (int vc = 0; vc < 16; ++vc) {
-      // chunk vc was issued earlier; make it visible and signal
-      if (vc + 1 < 16) cp_async_wait<1>(); else cp_async_wait<0>();
+    for (int vc = 0; vc < TC_NV; ++vc) {
+      // chunk vc was issued earlier; wait for it (later groups may stay in flight)
+      // groups issued after chunk vc so far: chunks vc+1 .. vc+TC_VST-2 (refills lag one iteration)
+      const int later = max(0, min(TC_VST - 2, TC_NV - 1 - vc));
+      if (later >= 3) cp_async_wait<3>(); else if (later == 2) cp_async_wait<2>();
+      else if (later == 1) cp_async_wait<1>(); else cp_async_wait<0>();
       fence_proxy_async_smem();
-      mbar_arrive(&S.vfull[vc & 1]);
-      if (vc + 2 < 16) {
-        if (!mbar_wait(&S.vempty[vc & 1], ((vc >> 1) & 1))) { ok = false; }
-        load_v(vc + 2);
+      mbar_arrive(&S.vfull[vc % TC_VST]);
+      // refill the buffer of the chunk delivered one iteration ago (likely consumed
+      // by now), not the one just delivered: the other stages stay in flight
+      if (vc >= 1 && vc - 1 + TC_VST < TC_NV) {
+        const int pv = vc - 1;
+        if (!mbar_wait(&S.vempty[pv % TC_VST], (pv / TC_VST) & 1)) { ok = false; }
+        load_v(pv + TC_VST);
       }
-      if ((vc & 7) == 7) {
-        // epilogue of half vc/8
-        const int hf = vc >> 3;
+      if ((vc % NV2) == NV2 - 1) {
+        // epilogue of half vc / NV2
+        const int hf = vc / NV2;
         if (!mbar_wait(&S.o_full, hf & 1)) ok = false;
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16 *dst = part.o + ((((int64_t)b * nsplit + s) * 128 + h) * 512 + hf * 256);
-        for (int c0 = 0; c0 < 256; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(trow + c0, r);
-          tmem_wait_ld();
+        auto store_o = [&](int c0, const uint32_t (&r)[32]) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -356,6 +381,14 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             reinterpret_cast<uint4 *>(dst + c0)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        };
+        for (int c0 = 0; c0 < 256; c0 += 64) {             // two TMEM loads per wait
+          uint32_t r[32], r2[32];
+          tmem_ld32(trow + c0, r);
+          tmem_ld32(trow + c0 + 32, r2);
+          tmem_wait_ld();
+          store_o(c0, r);
+          store_o(c0 + 32, r2);
         }
         tc_fence_before();
         mbar_arrive(&S.o_empty);
@@ -380,23 +413,21 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     mma_commit(&S.s_full);
     if (ok && !mbar_wait(&S.p_full, 0)) ok = false;
     tc_fence_after();
-    for (int vc = 0; vc < 16 && ok; ++vc) {
-      const int st = vc & 1, hf = vc >> 3, tc = vc & 7;
+    constexpr int NV2 = TC_NV / 2;
+    for (int vc = 0; vc < TC_NV && ok; ++vc) {
+      const int st = vc % TC_VST, hf = vc / NV2, tc = vc % NV2;
       if (tc == 0 && hf == 1) {                          // O columns reused: wait for the first epilogue
         if (!mbar_wait(&S.o_empty, 0)) { ok = false; break; }
         tc_fence_after();
       }
-      if (!mbar_wait(&S.vfull[st], (vc >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait(&S.vfull[st], (vc / TC_VST) & 1)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int t0 = tc * 32 + kk * 16;                // token offset in P
-        const uint64_t ad = smem_desc(smem_u32(P + (t0 >> 6) * (128 * 128) + (t0 & 63) * 2), 16, 1024, LAYOUT_SW128);
-        const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH + kk * 2048), 4096, 1024, LAYOUT_SW128);
-        mma_f16(tmem, ad, bd, id2, (tc | kk) ? 1u : 0u);
-      }
+      const int t0 = tc * TC_VROWS;                      // token offset in P (one K-step)
+      const uint64_t ad = smem_desc(smem_u32(P + (t0 >> 6) * (128 * 128) + (t0 & 63) * 2), 16, 1024, LAYOUT_SW128);
+      const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH), TC_VROWS * 128, 1024, LAYOUT_SW128);
+      mma_f16(tmem, ad, bd, id2, tc ? 1u : 0u);
       mma_commit(&S.vempty[st]);
-      if (tc == 7) mma_commit(&S.o_full);
+      if (tc == NV2 - 1) mma_commit(&S.o_full);
     }
   }
   if (!ok && tid == 0) {
