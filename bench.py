@@ -418,10 +418,12 @@ def run_echo(args, ws, rank, local):
     staged_hits = sum(c[9] for c in ctrs)
     misses = sum(c[10] for c in ctrs)
     sel_total = hits + staged_hits + misses
-    recall_bytes = (misses + sum(c[12] for c in ctrs)) * 576 * 2
+    recall_bytes = misses * 576 * 2          # host-link bytes of the recall (staged rows come from HBM)
     clocks = clk.summary()
+    link = None if args.skip_host_link else host_link(dev)
     if rank != 0:
         return 0
+    recall_gbs = (recall_bytes / (stages["recall_us"] / 1e6) / 1e9) if stages.get("recall_us") else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_ms_max / args.steps, "higher_is_better": True,
@@ -445,7 +447,9 @@ def run_echo(args, ws, rank, local):
         "clocks": clocks,
         "stages_us": stages,
         "indexer_gbs": achieved,
-        "recall_gbs": (recall_bytes / (stages["recall_us"] / 1e6) / 1e9) if stages.get("recall_us") else None,
+        "recall_gbs": recall_gbs,
+        "host_link": link,
+        "recall_kernel_frac_of_host_link": (link["zero_copy_recall_gbs"] / link["memcpy_h2d_gbs"]) if link else None,
         "hit_rate": (hits / sel_total) if sel_total else None,
         "hit_rate_after_prefetch": ((hits + staged_hits) / sel_total) if sel_total else None,
         "device_status": statuses,
@@ -460,8 +464,9 @@ def launches_per_step(prefetch: bool) -> int:
     return (1 + 1 + 2 + 1 + 3 + 2) if prefetch else (1 + 1 + 1 + 3 + 2)
 
 
-def stage_timing(L, inp, s_idx, stream, layers) -> dict:
-    """Average per-layer time of each stage of one step, eager, events on the stream."""
+def stage_timing(L, inp, s_idx, stream, layers, loaded=False) -> dict:
+    """Average per-layer time of each stage of one step, eager, events on the stream.
+    With loaded=True the step inputs are already in the layers' input buffers."""
     import ctypes
     import torch
     import sparse_attention_kv_dsa_gb300.echo as E
@@ -471,7 +476,9 @@ def stage_timing(L, inp, s_idx, stream, layers) -> dict:
     for l in range(layers):
         dl = L[l]
         a = dl.args
-        dl.load_step_inputs(inp.q_ik[l][s_idx], inp.new_ik_ik[l][s_idx], inp.new_kv[l][s_idx], inp.q_mla[l][s_idx])
+        if not loaded:
+            dl.load_step_inputs(inp.q_ik[l][s_idx], inp.new_ik_ik[l][s_idx], inp.new_kv[l][s_idx],
+                                inp.q_mla[l][s_idx])
         torch.cuda.synchronize()
         h = stream.cuda_stream
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -502,6 +509,119 @@ def stage_timing(L, inp, s_idx, stream, layers) -> dict:
     return {n + "_us": round(v, 2) for n, v in acc.items()}
 
 
+def host_link(dev) -> dict:
+    """Host-to-GPU bandwidth on this machine: a large pinned cudaMemcpyAsync, and a large
+    all-miss zero-copy recall through the library's own recall kernels (16-byte
+    loads of pinned host memory).  The roof for recall is the larger of the two."""
+    import torch
+    import sparse_attention_kv_dsa_gb300.echo as E
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(3):
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, src.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del src, dst
+    B, k = 32, 2048
+    n = B * k
+    host = torch.zeros(n, 576, dtype=torch.bfloat16, pin_memory=True)
+    layer = E.LayerCache(n, n, torch.bfloat16, dev, host_kv=host)
+    sel = torch.arange(k, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    base = (torch.arange(B, dtype=torch.int32, device=dev) * k).contiguous()
+    miss = torch.empty(B, k, dtype=torch.int32, device=dev)
+    nmiss = torch.empty(B, dtype=torch.int32, device=dev)
+    slot = torch.empty(B, k, dtype=torch.int32, device=dev)
+    zc = 0.0
+    for _ in range(3):
+        layer.reset()
+        torch.cuda.synchronize()
+        e0.record()
+        E.cache_recall(layer, sel, base, miss, nmiss, slot)
+        e1.record()
+        torch.cuda.synchronize()
+        zc = max(zc, n * 1152 / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return {"memcpy_h2d_gbs": best, "zero_copy_recall_gbs": zc, "peak_gbs": max(best, zc),
+            "how": "1 GiB pinned cudaMemcpyAsync; echo_cache_recall of 65536 missed 1152-B rows (best of 3)"}
+
+
+def run_compare_prefetch(args, local) -> int:
+    """Index + top-k + recall latency per layer-step, fused prefetch against the
+    unfused index -> top-k -> recall sequence, on identical inputs."""
+    import torch
+    import sparse_attention_kv_dsa_gb300.echo as E
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = S.workloads()[args.workload]
+    wl.layers = 1
+    steps = args.warmup + args.steps
+    inp = StepInputs(wl, 1, steps, dev, gen_device=dev)
+    res = {}
+    for mode in ("fused", "unfused"):
+        sc = SharedScratch(wl, dev, wl.cap_max)
+        dl = DecodeLayer(wl, 0, dev, prefetch=(mode == "fused"), scratch=sc, gen_device=dev)
+        t_ir, hits, staged, misses, sel_n = [], 0, 0, 0, 0
+        per = {"index_prefetch_us": [], "topk_us": [], "recall_us": []}
+        for s in range(steps):
+            dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+            st = stage_timing([dl], None, None, torch.cuda.current_stream(), 1, loaded=True)
+            if s >= args.warmup:
+                t_ir.append(st["index_prefetch_us"] + st["topk_us"] + st["recall_us"])
+                for n in per:
+                    per[n].append(st[n])
+                c = dl.cache.read_counters()
+                hits += c[8]; staged += c[9]; misses += c[10]
+        sel_n = hits + staged + misses
+        res[mode] = {"index_topk_recall_us": statistics.median(t_ir),
+                     **{n: statistics.median(v) for n, v in per.items()}, "hit_rate": hits / sel_n,
+                     "hit_rate_after_prefetch": (hits + staged) / sel_n, "misses_per_step": misses / args.steps}
+        del dl, sc
+        torch.cuda.empty_cache()
+    line = {"mode": "compare-prefetch", "workload": wl.name, "steps": args.steps, "warmup": args.warmup, **res,
+            "speedup_fused": res["unfused"]["index_topk_recall_us"] / res["fused"]["index_topk_recall_us"]}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cap_sweep(args, local) -> int:
+    """Low-locality workload: miss-list size and recall time against the prefetch cap."""
+    import torch
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = S.workloads()[args.workload]
+    wl.layers = 1
+    steps = args.warmup + args.steps
+    inp = StepInputs(wl, 1, steps, dev, gen_device=dev)
+    rows = []
+    for cap in (wl.cap_sweep or [0, wl.cap_max]):
+        sc = SharedScratch(wl, dev, max(cap, 1))
+        dl = DecodeLayer(wl, 0, dev, prefetch=cap > 0, cap_max=cap, scratch=sc, gen_device=dev)
+        acc = {"index_prefetch_us": [], "topk_us": [], "recall_us": [], "misses": [], "staged": [], "staged_hits": []}
+        for s in range(steps):
+            dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+            st = stage_timing([dl], None, None, torch.cuda.current_stream(), 1, loaded=True)
+            if s >= args.warmup:
+                c = dl.cache.read_counters()
+                for n in ("index_prefetch_us", "topk_us", "recall_us"):
+                    acc[n].append(st[n])
+                acc["misses"].append(c[10]); acc["staged"].append(c[12]); acc["staged_hits"].append(c[9])
+        rows.append({"cap": cap, **{n: statistics.median(v) for n, v in acc.items()}})
+        del dl, sc
+        torch.cuda.empty_cache()
+    print(json.dumps({"mode": "cap-sweep", "workload": wl.name, "steps": args.steps, "warmup": args.warmup,
+                      "per_cap": rows}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -513,9 +633,22 @@ def main(argv=None):
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-stages", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling)")
+    ap.add_argument("--compare-prefetch", action="store_true",
+                    help="fused vs unfused index+top-k+recall latency (default workload: decode-b8-ctx64k)")
+    ap.add_argument("--cap-sweep", action="store_true",
+                    help="prefetch-cap sweep (default workload: lowlocality-b16-ctx100k)")
+    ap.add_argument("--skip-host-link", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()
+    if args.compare_prefetch:
+        if args.workload == DEFAULT_WL:
+            args.workload = "decode-b8-ctx64k"
+        return run_compare_prefetch(args, local)
+    if args.cap_sweep:
+        if args.workload == DEFAULT_WL:
+            args.workload = "lowlocality-b16-ctx100k"
+        return run_cap_sweep(args, local)
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     return run_echo(args, ws, rank, local)

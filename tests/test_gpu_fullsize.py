@@ -1,0 +1,197 @@
+"""Parity at the full sizes of the decode workloads, in the launch configuration the
+benchmark times (one layer of the 64K and of the 80K-100K workloads).
+
+* 64K, batch 8: one steady-state step is checked element by element against the
+  oracle by state hand-off -- the oracle takes the GPU's cache state before the
+  step (residency, priorities, EMA threshold) and recomputes the whole step.
+* 80K-100K, batch 32: sampled scores, exact top-k of sampled requests (the oracle
+  scores those requests itself), sampled attention heads, and invariants over all.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sparse_attention_kv_dsa_gb300 import synth as S
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def build(name, steps_before):
+    from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
+    wl = S.workloads()[name]
+    wl.layers = 1
+    dev = torch.device("cuda")
+    sc = SharedScratch(wl, dev, wl.cap_max)
+    dl = DecodeLayer(wl, 0, dev, scratch=sc, gen_device="cpu")
+    inp = StepInputs(wl, 1, steps_before + 1, dev, gen_device="cpu")
+    for s in range(steps_before):
+        dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+        dl.step()
+    torch.cuda.synchronize()
+    return wl, dl, inp
+
+
+def host_rows(wl, dl, inp, b, ts):
+    """Expected latent rows of request b's tokens ts from the inputs alone: context
+    tokens hold the generator's rows (copied in by torch before any step), later
+    tokens the per-step new_kv input of the step that wrote them back."""
+    ts = np.asarray(ts, dtype=np.int64)
+    out = dl.cache.host_kv[torch.from_numpy(wl.host_base[b] + np.minimum(ts, wl.ctx[b] - 1))].float().numpy()
+    for i, t in enumerate(ts):
+        if t >= wl.ctx[b]:
+            out[i] = inp.new_kv[0][int(t - wl.ctx[b])][b].float().cpu().numpy()
+    return out
+
+
+def handoff_cache(dl, wl):
+    """Oracle cache built from the GPU's pre-step state (a state hand-off)."""
+    oc = O.LayerCache(wl.n_gpu, wl.n_host)
+    oc.host2gpu[:] = dl.cache.host2gpu.cpu().numpy()
+    oc.gpu2host[:] = dl.cache.gpu2host.cpu().numpy()
+    oc.priority[:] = dl.cache.priority.cpu().numpy()
+    oc.free[:] = dl.cache.free_map.cpu().numpy().astype(bool)
+    oc.step = int(dl.cache.counters[0].item())
+    oc.check_invariants()
+    return oc
+
+
+def test_decode_b8_ctx64k_full_step_by_state_handoff():
+    from harness import gpu_residency, check_gpu_maps
+    wl, dl, inp = build("decode-b8-ctx64k", steps_before=3)
+    s = 3
+    oc = handoff_cache(dl, wl)
+    seq = dl.seq_len.cpu().numpy().astype(np.int64)
+    theta = dl.theta.cpu().numpy()
+    # the oracle's own inputs: keys from the generator, plus the appended tokens
+    keys = []
+    for b in range(wl.batch):
+        k0 = S.grid_to_float(S.keys_for(wl, 0, b, wl.ctx[b])).numpy().astype(np.float64)
+        extra = [S.grid_to_float(S.new_ik_for(wl, 0, j)[b:b + 1]).numpy() for j in range(s + 1)]
+        keys.append(np.concatenate([k0] + extra))
+    dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+    dl.step()
+    torch.cuda.synchronize()
+    r = O.decode_layer_step(oc, host_base=wl.host_base, seq_len=seq, keys_of=lambda b, L: keys[b][:L],
+                            q_idx=S.grid_to_float(inp.q_int[0][s].cpu()).numpy(), w_idx=dl.w_idx.cpu().numpy(),
+                            theta=theta, k=wl.topk, cap_max=wl.cap_max, cap_div=wl.cap_div, alpha=wl.alpha,
+                            q_mla=None)
+    scores = dl.scratch.scores.cpu().numpy()
+    sel = dl.sel.cpu().numpy()
+    pf_list, pf_count = dl.pf_list.cpu().numpy(), dl.pf_count.cpu().numpy()
+    miss, n_miss = dl.miss_list.cpu().numpy(), dl.n_miss.cpu().numpy()
+    staged_total = 0
+    for b in range(wl.batch):
+        L = int(seq[b])
+        assert np.array_equal(scores[b, :L], r.scores[b]), f"scores, request {b}"
+        assert set(sel[b].tolist()) == set(r.sel[b].tolist()), f"top-k, request {b}"
+        assert set(pf_list[b, :pf_count[b]].tolist()) == set(r.staged[b].tolist()), f"prefetch, request {b}"
+        assert set(miss[b, :n_miss[b]].tolist()) == set(r.recall.misses[b]), f"misses, request {b}"
+        staged_total += len(r.staged[b])
+    assert np.array_equal(dl.kth.cpu().numpy(), r.kth) and np.array_equal(dl.theta.cpu().numpy(), r.theta)
+    assert gpu_residency(dl.cache) == oc.resident_priority(), "residency / priorities"
+    check_gpu_maps(dl.cache)
+    assert staged_total > 0, "steady state should prefetch"
+    # sampled attention heads against the oracle
+    slot = dl.slot_idx.cpu().numpy()
+    kv = dl.cache.gpu_kv.float().cpu().numpy()
+    qm = inp.q_mla[0][s].float().cpu().numpy()
+    out = dl.out.float().cpu().numpy()
+    rng = np.random.default_rng(0)
+    for b in rng.choice(wl.batch, 3, replace=False):
+        rows = host_rows(wl, dl, inp, b, r.sel[b])
+        assert np.array_equal(kv[slot[b]], host_rows(wl, dl, inp, b, sel[b])), "recalled rows"
+        heads = rng.choice(wl.h_q, 8, replace=False)
+        o, _ = O.sparse_mla_decode(qm[b, heads], rows, wl.scale)
+        assert np.abs(out[b, heads] - o).max() <= 2e-2
+
+
+def test_saturated_b32_ctx80k_100k_sampled_and_invariants():
+    from harness import check_gpu_maps
+    wl, dl, inp = build("saturated-b32-ctx80k-100k-4layer", steps_before=3)
+    s = 3
+    pre_g2h = dl.cache.gpu2host.cpu().numpy().copy()
+    pre_pr = dl.cache.priority.cpu().numpy().copy()
+    theta0 = dl.theta.cpu().numpy().copy()
+    seq0 = dl.seq_len.cpu().numpy().astype(np.int64)
+    dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+    dl.step()
+    torch.cuda.synchronize()
+    assert dl.cache.status() == 0
+    seq = dl.seq_len.cpu().numpy()
+    assert np.array_equal(seq, seq0 + 1)
+    scores = dl.scratch.scores.cpu().numpy()
+    sel = dl.sel.cpu().numpy()
+    kth = dl.kth.cpu().numpy()
+    q = S.grid_to_float(inp.q_int[0][s].cpu()).numpy()
+    w = dl.w_idx.cpu().numpy()
+    rng = np.random.default_rng(1)
+    for b in range(wl.batch):
+        L = int(seq[b])
+        # sampled scores, recomputed by the oracle from the generator's keys
+        keys_b = S.grid_to_float(S.keys_for(wl, 0, b, wl.ctx[b])).numpy().astype(np.float64)
+        ts = rng.choice(wl.ctx[b], 64, replace=False)
+        ref = O.to_f32_exact(O.indexer_scores(q[b], w[b], keys_b[ts]))
+        assert np.array_equal(scores[b, ts], ref), f"sampled scores, request {b}"
+        # top-k invariants on the full row
+        row = scores[b, :L]
+        chosen = np.zeros(L, bool)
+        chosen[sel[b]] = True
+        assert chosen.sum() == wl.topk and np.all(sel[b] >= 0)
+        assert np.all(row[~chosen] <= kth[b]) and np.all(row[chosen] >= kth[b])
+        eq_sel = np.nonzero(chosen & (row == kth[b]))[0]
+        eq_un = np.nonzero(~chosen & (row == kth[b]))[0]
+        assert eq_un.size == 0 or eq_un.min() > eq_sel.max(), "ties go to the lower index"
+        exp_theta = O.ema_update(theta0[b], kth[b], wl.alpha)
+        assert dl.theta[b].item() == exp_theta
+    # exact top-k of two sampled requests: the oracle scores them itself
+    for b in rng.choice(wl.batch, 2, replace=False):
+        L = int(seq[b])
+        keys_b = np.concatenate([S.grid_to_float(S.keys_for(wl, 0, b, wl.ctx[b])).numpy()] +
+                                [S.grid_to_float(S.new_ik_for(wl, 0, j)[b:b + 1]).numpy() for j in range(s + 1)])
+        ref = O.to_f32_exact(O.indexer_scores(q[b], w[b], keys_b[:L]))
+        assert np.array_equal(scores[b, :L], ref)
+        osel, okth = O.topk_select(ref, wl.topk)
+        assert set(sel[b].tolist()) == set(osel.tolist()) and kth[b] == np.float32(okth)
+    # cache invariants, residency of the selection, LRU victims were the smallest keys
+    check_gpu_maps(dl.cache)
+    h2g = dl.cache.host2gpu.cpu().numpy()
+    hb = np.array(wl.host_base)
+    for b in range(wl.batch):
+        assert np.all(h2g[hb[b] + sel[b]] >= 0), "every selected token is resident"
+    # LRU: every evicted token's (priority, host) key is below the key of every
+    # resident token that this step left untouched (priority still < step)
+    post_g2h = dl.cache.gpu2host.cpu().numpy()
+    post_pr = dl.cache.priority.cpu().numpy()
+    step = int(dl.cache.counters[0].item())
+    pre_key = {int(pre_g2h[g]): (int(pre_pr[g]), int(pre_g2h[g])) for g in np.nonzero(pre_g2h >= 0)[0]}
+    evicted = np.setdiff1d(pre_g2h[pre_g2h >= 0], post_g2h[post_g2h >= 0])
+    untouched = [(int(post_pr[g]), int(post_g2h[g])) for g in np.nonzero(post_g2h >= 0)[0] if post_pr[g] < step]
+    if evicted.size and untouched:
+        assert max(pre_key[int(h)] for h in evicted) < min(untouched), "victims were not the LRU-smallest"
+    # sampled attention heads
+    slot = dl.slot_idx.cpu().numpy()
+    qm = inp.q_mla[0][s].float().cpu().numpy()
+    out = dl.out.float().cpu().numpy()
+    for b in rng.choice(wl.batch, 3, replace=False):
+        rows = dl.cache.gpu_kv[torch.from_numpy(slot[b]).long().cuda()].float().cpu().numpy()
+        expect = host_rows(wl, dl, inp, b, sel[b])
+        assert np.array_equal(rows, expect), "recalled rows"
+        heads = rng.choice(wl.h_q, 8, replace=False)
+        o, l = O.sparse_mla_decode(qm[b, heads], expect, wl.scale)
+        assert np.abs(out[b, heads] - o).max() <= 2e-2
+
+
+def test_saturated_lossless_at_full_size():
+    import sparse_attention_kv_dsa_gb300.echo as E
+    wl, dl, inp = build("saturated-b32-ctx80k-100k-4layer", steps_before=2)
+    dense = dl.cache.host_kv.to("cuda")
+    idx = torch.where(dl.sel >= 0, dl.sel + dl.host_base[:, None], torch.full_like(dl.sel, -1)).contiguous()
+    out2 = torch.empty_like(dl.out)
+    lse2 = torch.empty_like(dl.lse)
+    E.sparse_mla_decode(dl.q_mla, dense, idx, wl.scale, out2, lse2, dl.scratch.mla_ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, dl.out) and torch.equal(lse2, dl.lse)
