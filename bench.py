@@ -103,10 +103,15 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # let the sampler start before the timed region: spawning it must not
+            # delay the first launches after the start event
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
@@ -258,7 +263,12 @@ def run_echo(args, ws, rank, local):
     if args.layers:
         wl.layers = int(args.layers)
     layers = wl.layers
-    total_steps = args.warmup + args.steps + args.steps + 2
+    # step inputs: pool fill + warm-up + timed + e2e + stage leg, within the workload's steps
+    base_steps = args.warmup + args.steps + args.steps + 2
+    fill_max = max(0, min(args.fill_max, wl.steps + 8 - base_steps - 1))
+    if base_steps > wl.steps + 8:
+        raise SystemExit(f"--steps/--warmup need {base_steps} decode steps; {wl.name} has {wl.steps}")
+    total_steps = base_steps + fill_max
     prefetch = not args.no_prefetch
     scratch = SharedScratch(wl, dev, wl.cap_max)
     L = [DecodeLayer(wl, l, dev, prefetch=prefetch, scratch=scratch, gen_device=dev) for l in range(layers)]
@@ -266,10 +276,7 @@ def run_echo(args, ws, rank, local):
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
 
-    # pinned host copies of the step inputs / outputs for the e2e leg
-    h_in = [[(inp.q_ik[l][s].cpu().pin_memory(), inp.new_ik_ik[l][s].cpu().pin_memory(),
-              inp.new_kv[l][s].cpu().pin_memory(), inp.q_mla[l][s].cpu().pin_memory())
-             for s in range(total_steps)] for l in range(layers)]
+    h_in = {}                      # pinned host copies of the e2e leg's step inputs (made later)
     h_out = [torch.empty(L[l].out.shape, dtype=L[l].out.dtype, pin_memory=True) for l in range(layers)]
 
     # timing events around the indexer, recorded inside the graph when supported
@@ -296,13 +303,7 @@ def run_echo(args, ws, rank, local):
                 E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap,
                                                a.pf_count, h))
             ix_ev[l][0].record(st)
-            E.check(lib.echo_index_prefetch(a.q_idx, a.w_idx, a.idx_k, a.seq_len, a.B, a.H, a.D, a.Lmax,
-                                            a.idx_dtype, a.theta, a.cap if a.prefetch else None, a.cap_max,
-                                            a.host_base, dl.cache.ref, a.scores, a.pf_list, a.pf_count, a.stage_kv,
-                                            h))
-            ix_ev[l][1].record(st)
-            E.check(lib.echo_topk(a.scores, a.seq_len, a.B, a.Lmax, a.k, a.sel, a.kth, a.theta, ctypes.c_float(a.alpha),
-                                  h))
+            enqueue_index_topk(lib, dl, h, between=lambda: ix_ev[l][1].record(st))
             E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k,
                                           a.pf_list if a.prefetch else None, a.pf_count if a.prefetch else None,
                                           a.cap_max, a.stage_kv, a.miss_list, a.n_miss, a.slot_idx, h))
@@ -317,7 +318,7 @@ def run_echo(args, ws, rank, local):
         with torch.cuda.stream(st):
             for l in range(layers):
                 if from_host:
-                    L[l].load_step_inputs(*h_in[l][s], non_blocking=True)
+                    L[l].load_step_inputs(*h_in[(l, s)], non_blocking=True)
                 else:
                     L[l].load_step_inputs(inp.q_ik[l][s], inp.new_ik_ik[l][s], inp.new_kv[l][s], inp.q_mla[l][s])
 
@@ -344,6 +345,21 @@ def run_echo(args, ws, rank, local):
                 L[l].step(stream=stream)
     torch.cuda.synchronize()
 
+    # steady state of the pool: untimed steps until every layer has fewer free slots
+    # than its last step bound, so that every timed step evicts (or fill_max steps)
+    fill = 0
+    while fill < fill_max:
+        load_inputs(s_idx, stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        s_idx += 1
+        fill += 1
+        stream.synchronize()
+        ctr = [dl.cache.read_counters() for dl in L]
+        if all(c[E.CTR_N_FREE] < max(c[E.CTR_BOUND], 1) for c in ctr):
+            break
+    n_free_at_start = [int(dl.cache.read_counters()[E.CTR_N_FREE]) for dl in L]
+
     for _ in range(max(args.warmup - 1, 0)):
         load_inputs(s_idx, stream)
         with torch.cuda.stream(stream):
@@ -352,6 +368,12 @@ def run_echo(args, ws, rank, local):
     stream.synchronize()
     for dl in L:
         assert dl.cache.status() == 0, f"device status {dl.cache.status()} after warm-up"
+
+    e2e_first = s_idx + args.steps
+    for l in range(layers):
+        for s in range(e2e_first, e2e_first + args.steps):
+            h_in[(l, s)] = (inp.q_ik[l][s].cpu().pin_memory(), inp.new_ik_ik[l][s].cpu().pin_memory(),
+                            inp.new_kv[l][s].cpu().pin_memory(), inp.q_mla[l][s].cpu().pin_memory())
 
     # ---------------- timed region: inputs resident in HBM ----------------
     seq0 = [dl.seq_len.clone() for dl in L]
@@ -381,7 +403,8 @@ def run_echo(args, ws, rank, local):
     value = tokens / (t_ms_max / 1e3)
 
     # ---------------- e2e: inputs from pinned host, outputs back ----------------
-    h2d = sum(sum(x.numel() * x.element_size() for x in h_in[l][0]) for l in range(layers))
+    assert s_idx == e2e_first
+    h2d = sum(sum(x.numel() * x.element_size() for x in h_in[(l, e2e_first)]) for l in range(layers))
     d2h = sum(h_out[l].numel() * h_out[l].element_size() for l in range(layers))
     barrier(ws)
     torch.cuda.synchronize()
@@ -432,10 +455,11 @@ def run_echo(args, ws, rank, local):
                    "ctx": f"{min(wl.ctx)}-{max(wl.ctx)}", "topk": wl.topk, "gpu_slots": wl.n_gpu,
                    "host_slots": wl.n_host, "prefetch": prefetch, "cuda_graph": True,
                    "parallelism": f"replicas x{ws}",
+                   "pool_fill_steps": fill, "gpu_free_slots_at_warmup": n_free_at_start,
                    "l2": "inputs larger than L2 (indexer keys %.0f MB per layer)" % (wl.batch * mean_ctx * 128 / 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": traffic,
-                     "kernel": "indexer_fp8_kernel (+ its cap fix-up launch)",
+                     "kernel": "indexer_fp8_kernel",
                      "algorithmic_bytes_per_launch": ix_bytes,
                      "avg_launch_ms": ix_avg_ms,
                      "timing": "CUDA events inside the timed graph" if ix_ms else "eager stage leg",
@@ -459,9 +483,32 @@ def run_echo(args, ws, rank, local):
 
 
 def launches_per_step(prefetch: bool) -> int:
-    """Kernels of one layer step: write-back 1, reserve 1, indexer 1 + cap fix-up 1,
-    top-k 1, recall 3 (miss detect, evict+bind cluster, copy+translate), MLA 2."""
-    return (1 + 1 + 2 + 1 + 3 + 2) if prefetch else (1 + 1 + 1 + 3 + 2)
+    """Kernels of one layer step: write-back 1, reserve 1, indexer 1, top-k 1 (with the
+    deferred exact prefetch cap), recall 3 (miss detect, evict+bind cluster,
+    copy+translate), MLA 2."""
+    return (1 + 1 + 1 + 1 + 3 + 2) if prefetch else (1 + 1 + 1 + 3 + 2)
+
+
+def enqueue_index_topk(lib, dl, h, between=None):
+    """The indexer and the top-k of one layer step as echo_decode_layer_step issues
+    them (cap fix-up deferred into the top-k launch); between() runs after the indexer
+    call, to record an event."""
+    import ctypes
+    import sparse_attention_kv_dsa_gb300.echo as E
+    a = dl.args
+    pf = bool(a.prefetch)
+    E.check(lib.echo_index_prefetch(a.q_idx, a.w_idx, a.idx_k, a.seq_len, a.B, a.H, a.D, a.Lmax, a.idx_dtype,
+                                    a.theta, a.cap if pf else None, a.cap_max, a.host_base, dl.cache.ref, a.scores,
+                                    a.pf_list, a.pf_count, a.stage_kv, E.PF_DEFER_CAP if pf else 0, h))
+    if between is not None:
+        between()
+    if pf:
+        E.check(lib.echo_topk_prefetch(a.scores, a.seq_len, a.B, a.Lmax, a.k, a.sel, a.kth, a.theta,
+                                       ctypes.c_float(a.alpha), a.cap, a.cap_max, a.host_base, dl.cache.ref,
+                                       a.pf_list, a.pf_count, a.stage_kv, h))
+    else:
+        E.check(lib.echo_topk(a.scores, a.seq_len, a.B, a.Lmax, a.k, a.sel, a.kth, a.theta, ctypes.c_float(a.alpha),
+                              h))
 
 
 def stage_timing(L, inp, s_idx, stream, layers, loaded=False) -> dict:
@@ -489,11 +536,7 @@ def stage_timing(L, inp, s_idx, stream, layers, loaded=False) -> dict:
         if a.prefetch:
             E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap, a.pf_count, h))
         ev[2].record(stream)
-        E.check(lib.echo_index_prefetch(a.q_idx, a.w_idx, a.idx_k, a.seq_len, a.B, a.H, a.D, a.Lmax, a.idx_dtype,
-                                        a.theta, a.cap if a.prefetch else None, a.cap_max, a.host_base,
-                                        dl.cache.ref, a.scores, a.pf_list, a.pf_count, a.stage_kv, h))
-        ev[3].record(stream)
-        E.check(lib.echo_topk(a.scores, a.seq_len, a.B, a.Lmax, a.k, a.sel, a.kth, a.theta, ctypes.c_float(a.alpha), h))
+        enqueue_index_topk(lib, dl, h, between=lambda: ev[3].record(stream))
         ev[4].record(stream)
         E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k, a.pf_list if a.prefetch else None,
                                       a.pf_count if a.prefetch else None, a.cap_max, a.stage_kv, a.miss_list,
@@ -552,7 +595,11 @@ def host_link(dev) -> dict:
 
 def run_compare_prefetch(args, local) -> int:
     """Index + top-k + recall latency per layer-step, fused prefetch against the
-    unfused index -> top-k -> recall sequence, on identical inputs."""
+    unfused index -> top-k -> recall sequence, on identical inputs.  Each mode's
+    whole layer step is captured in one CUDA Graph (as it runs in production) and
+    the segment from the indexer to the end of the recall is timed with events
+    recorded inside the graph; eager per-stage times are reported beside it."""
+    import ctypes
     import torch
     import sparse_attention_kv_dsa_gb300.echo as E
     from sparse_attention_kv_dsa_gb300 import synth as S
@@ -562,30 +609,66 @@ def run_compare_prefetch(args, local) -> int:
     wl = S.workloads()[args.workload]
     wl.layers = 1
     steps = args.warmup + args.steps
-    inp = StepInputs(wl, 1, steps, dev, gen_device=dev)
+    inp = StepInputs(wl, 1, steps + 1, dev, gen_device=dev)
+    lib = E.lib()
     res = {}
     for mode in ("fused", "unfused"):
         sc = SharedScratch(wl, dev, wl.cap_max)
         dl = DecodeLayer(wl, 0, dev, prefetch=(mode == "fused"), scratch=sc, gen_device=dev)
-        t_ir, hits, staged, misses, sel_n = [], 0, 0, 0, 0
-        per = {"index_prefetch_us": [], "topk_us": [], "recall_us": []}
-        for s in range(steps):
+        a = dl.args
+        st = torch.cuda.Stream(dev)
+        ev = (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+
+        def seg(stream):
+            h = stream.cuda_stream
+            E.check(lib.echo_cache_writeback(dl.cache.ref, a.new_kv, a.new_ik, a.idx_k, a.D, a.Lmax, a.idx_dtype,
+                                             a.host_base, a.seq_len, a.B, h))
+            if a.prefetch:
+                E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap,
+                                               a.pf_count, h))
+            ev[0].record(stream)
+            enqueue_index_topk(lib, dl, h)
+            E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k,
+                                          a.pf_list if a.prefetch else None, a.pf_count if a.prefetch else None,
+                                          a.cap_max, a.stage_kv, a.miss_list, a.n_miss, a.slot_idx, h))
+            ev[1].record(stream)
+            E.check(lib.echo_sparse_mla_decode(a.q_mla, dl.cache.struct.gpu_kv, dl.cache.n_gpu,
+                                               dl.cache.struct.kv_dtype, a.slot_idx, a.B, a.Hq, a.k,
+                                               ctypes.c_float(a.scale), a.out, a.lse, a.mla_workspace,
+                                               a.mla_workspace_bytes, h))
+
+        dl.load_step_inputs(inp.q_ik[0][0], inp.new_ik_ik[0][0], inp.new_kv[0][0], inp.q_mla[0][0])
+        with torch.cuda.stream(st):
+            seg(st)                                     # first step eagerly (cold cache)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            seg(st)
+        t_graph, hits, staged, misses, rows, qual = [], 0, 0, 0, 0, 0
+        for s in range(1, steps):
             dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
-            st = stage_timing([dl], None, None, torch.cuda.current_stream(), 1, loaded=True)
+            with torch.cuda.stream(st):
+                g.replay()
+            st.synchronize()
             if s >= args.warmup:
-                t_ir.append(st["index_prefetch_us"] + st["topk_us"] + st["recall_us"])
-                for n in per:
-                    per[n].append(st[n])
+                t_graph.append(ev[0].elapsed_time(ev[1]) * 1e3)
                 c = dl.cache.read_counters()
-                hits += c[8]; staged += c[9]; misses += c[10]
+                hits += c[8]; staged += c[9]; misses += c[10]; rows += c[12]; qual += c[15]
+        # eager per-stage breakdown of one more step
+        dl.load_step_inputs(inp.q_ik[0][steps], inp.new_ik_ik[0][steps], inp.new_kv[0][steps], inp.q_mla[0][steps])
+        stg = stage_timing([dl], None, None, torch.cuda.current_stream(), 1, loaded=True)
         sel_n = hits + staged + misses
-        res[mode] = {"index_topk_recall_us": statistics.median(t_ir),
-                     **{n: statistics.median(v) for n, v in per.items()}, "hit_rate": hits / sel_n,
-                     "hit_rate_after_prefetch": (hits + staged) / sel_n, "misses_per_step": misses / args.steps}
-        del dl, sc
+        res[mode] = {"index_topk_recall_us_in_graph": statistics.median(t_graph),
+                     "eager_stages_us": {k: stg[k] for k in ("index_prefetch_us", "topk_us", "recall_us")},
+                     "hit_rate": hits / sel_n, "hit_rate_after_prefetch": (hits + staged) / sel_n,
+                     "misses_per_step": misses / args.steps,
+                     "staged_rows_per_step": rows / args.steps, "qualifying_per_step": qual / args.steps,
+                     "prefetch_precision": (staged / rows) if rows else None}
+        del g, dl, sc
         torch.cuda.empty_cache()
     line = {"mode": "compare-prefetch", "workload": wl.name, "steps": args.steps, "warmup": args.warmup, **res,
-            "speedup_fused": res["unfused"]["index_topk_recall_us"] / res["fused"]["index_topk_recall_us"]}
+            "speedup_fused": res["unfused"]["index_topk_recall_us_in_graph"] /
+                             res["fused"]["index_topk_recall_us_in_graph"]}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -628,7 +711,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="echo", choices=["echo", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WL)
+    ap.add_argument("--workload", default=None, help=f"default {DEFAULT_WL}")
     ap.add_argument("--no-prefetch", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-stages", action="store_true")
@@ -638,17 +721,18 @@ def main(argv=None):
     ap.add_argument("--cap-sweep", action="store_true",
                     help="prefetch-cap sweep (default workload: lowlocality-b16-ctx100k)")
     ap.add_argument("--skip-host-link", action="store_true")
+    ap.add_argument("--fill-max", type=int, default=96,
+                    help="untimed steps, at most, that bring the GPU pool to its steady (full) state")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()
     if args.compare_prefetch:
-        if args.workload == DEFAULT_WL:
-            args.workload = "decode-b8-ctx64k"
+        args.workload = args.workload or "decode-b8-ctx64k"
         return run_compare_prefetch(args, local)
     if args.cap_sweep:
-        if args.workload == DEFAULT_WL:
-            args.workload = "lowlocality-b16-ctx100k"
+        args.workload = args.workload or "lowlocality-b16-ctx100k"
         return run_cap_sweep(args, local)
+    args.workload = args.workload or DEFAULT_WL
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     return run_echo(args, ws, rank, local)

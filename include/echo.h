@@ -173,14 +173,23 @@ echo_status_t echo_cache_reserve(const echo_cache_layer_t *layer, const int32_t 
  * Prefetch rule: t is staged iff score > theta[b] (strict), host2gpu[h] == -1, and t is
  * among the first cap[b] such tokens by ascending t.  Staged tokens get
  * host2gpu[h] = -2 - staging_row until echo_cache_recall binds them.
+ *   flags  0, or ECHO_PF_DEFER_CAP: rows are claimed in arrival order and, when a
+ *          request's qualifying tokens outnumber its cap, the "first cap by t" rule
+ *          is restored by a later call: pf_count[b] then holds the number of
+ *          qualifying tokens (staged rows = min(pf_count[b], cap)) until
+ *          echo_topk_prefetch, which must run next on the same stream with the same
+ *          scores, theta (before its update), cap and layer.  Without the flag the
+ *          rule is restored by a small extra launch before this call returns.
  * Device errors: STAGING if cap[b] > cap_max; TIMEOUT if a bounded wait gave up.
  */
+#define ECHO_PF_DEFER_CAP 1
 echo_status_t echo_index_prefetch(const void *q, const float *w, const void *idx_k,
                                   const int32_t *seq_len, int32_t B, int32_t H, int32_t D,
                                   int32_t Lmax, int32_t dtype, const float *theta,
                                   const int32_t *cap, int32_t cap_max, const int32_t *host_base,
                                   const echo_cache_layer_t *layer, float *scores, int32_t *pf_list,
-                                  int32_t *pf_count, void *stage_kv, echo_stream_t stream);
+                                  int32_t *pf_count, void *stage_kv, int32_t flags,
+                                  echo_stream_t stream);
 
 /*
  * A5 -- exact top-k with the EMA threshold update ([REV] "Problem and motivation":
@@ -196,6 +205,25 @@ echo_status_t echo_index_prefetch(const void *q, const float *w, const void *idx
 echo_status_t echo_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax,
                         int32_t k, int32_t *out_idx, float *kth, float *theta, float alpha,
                         echo_stream_t stream);
+
+/*
+ * A5 + the deferred end of A4 -- echo_topk, and in the same launch the exact prefetch
+ * cap of an echo_index_prefetch call made with ECHO_PF_DEFER_CAP ([REV] "Decode:
+ * ...": a counter caps the prefetch volume; "Fusing prefetch into the indexer
+ * pipeline": prefetch adds no step of its own to the decode path).  For a request
+ * whose pf_count[b] exceeds min(cap[b], cap_max), tokens claimed beyond the first
+ * cap qualifiers by t give their staging rows to the qualifiers that were left out
+ * (maps, pf_list and stage_kv rows rewritten); then pf_count[b] = min(count, cap).
+ * The threshold used is theta[b] as it was before this call's EMA update.
+ *   top-k arguments as echo_topk; cap, cap_max, host_base, layer, pf_list, pf_count,
+ *   stage_kv as passed to echo_index_prefetch (all required).
+ */
+echo_status_t echo_topk_prefetch(const float *scores, const int32_t *seq_len, int32_t B,
+                                 int32_t Lmax, int32_t k, int32_t *out_idx, float *kth,
+                                 float *theta, float alpha, const int32_t *cap, int32_t cap_max,
+                                 const int32_t *host_base, const echo_cache_layer_t *layer,
+                                 int32_t *pf_list, int32_t *pf_count, void *stage_kv,
+                                 echo_stream_t stream);
 
 /*
  * A7 -- eviction with protection ([REV] "In-graph per-layer cache management":

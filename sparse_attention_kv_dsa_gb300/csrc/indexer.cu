@@ -22,15 +22,16 @@
 //   warps 3-6  epilogue: tcgen05.ld of a token row (64 head dot products), ReLU,
 //              weighted sum, score store; tokens above the threshold go to a ring
 // On the exact grid the tensor-core sums are exact, so scores equal the definition.
-// The cap is exact: claims are optimistic (any order) and pf_finalize_kernel restores
-// "the first cap tokens by ascending t" for the rare request whose qualifiers
-// outnumber its cap.
+// The cap is exact: claims are optimistic (any order) and a fix-up restores "the first
+// cap tokens by ascending t" for the rare request whose qualifiers outnumber its cap,
+// either in its own small launch here or, deferred, inside the top-k kernel.
 
 #include <algorithm>
 #include <cstddef>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "pf_fixup.cuh"
 
 namespace echo {
 
@@ -64,6 +65,7 @@ constexpr int IX_Q_BYTES = IX_H * IX_D;          // 8192
 constexpr int IX_ACC = 4;                        // TMEM accumulator buffers (4 x 64 columns)
 constexpr int IX_WB = ECHO_IX_WB;
 
+
 struct IxParams {
   const float *w;
   const int32_t *seq_len;
@@ -85,6 +87,7 @@ struct IxSmemTail {
   uint32_t tmem_base;
   uint32_t ring_tail;
   uint32_t ring_head;
+  uint32_t ring_claim;
   uint32_t epi_done;
   int32_t tile_pre[IX_MAXB + 1];
   int32_t ring_b[IX_RING];
@@ -157,6 +160,46 @@ __device__ __forceinline__ void claim_and_copy(const IxParams &P, bool cand, int
   }
 }
 
+// One consumer step on the candidate ring: claim up to 32 entries (CAS on the claim
+// cursor), read them, process them (residency check, capped claim, copy).
+// Returns false when nothing was available.  Whole warp.
+__device__ __forceinline__ bool consume_ring(const IxParams &P, IxSmemTail &S, int32_t *ctr) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c = 0, n = 0;
+  if (lane == 0) {
+    while (true) {
+      c = *(volatile uint32_t *)&S.ring_claim;
+      const uint32_t tail = *(volatile uint32_t *)&S.ring_tail;
+      if (c >= tail) { n = 0; break; }
+      n = min(tail - c, 32u);
+      if (atomicCAS(&S.ring_claim, c, c + n) == c) break;
+    }
+  }
+  c = __shfl_sync(0xffffffffu, c, 0);
+  n = __shfl_sync(0xffffffffu, n, 0);
+  if (n == 0) return false;
+  bool cand = false;
+  int b = 0, t = 0;
+  if ((uint32_t)lane < n) {
+    const uint32_t pos = c + lane;
+    const int slot = pos % IX_RING;
+    const uint64_t tw = global_ns();
+    bool ok = true;
+    while (*(volatile int32_t *)&S.ring_seq[slot] != (int32_t)(pos + 1)) {
+      if (global_ns() - tw > kWaitLimitNs) { ok = false; break; }
+    }
+    __threadfence_block();
+    b = S.ring_b[slot];
+    t = S.ring_t[slot];
+    cand = ok && b >= 0;
+    if (!ok) set_status(ctr, ECHO_ERR_TIMEOUT);
+  }
+  __syncwarp();
+  if (lane == 0) atomicAdd(&S.ring_head, n);         // entries read: ring space for producers
+  claim_and_copy(P, cand, b, t);
+  return true;
+}
+
 __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
     indexer_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                        IxParams P) {
@@ -184,6 +227,7 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
     }
     S.ring_tail = 0;
     S.ring_head = 0;
+    S.ring_claim = 0;
     S.epi_done = 0;
     fence_mbar_init();
   }
@@ -345,43 +389,30 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
     }
     __threadfence_block();
     atomicAdd(&S.epi_done, 1u);
+    if (prefetch) {
+      // once every epilogue thread is done (no more pushes), help drain the ring
+      const uint64_t tw = global_ns();
+      while (*(volatile uint32_t *)&S.epi_done < 128u * IX_EPI) {
+        if (global_ns() - tw > kWaitLimitNs) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
+        __nanosleep(128);
+      }
+      __threadfence_block();
+      while (consume_ring(P, S, ctr)) {
+      }
+    }
   } else if (warp == 2 && prefetch) {
     // ---------------------------------------------------------- prefetch --
-    uint32_t head = 0;
     uint64_t t_idle = global_ns();
     while (true) {
       const uint32_t done = *(volatile uint32_t *)&S.epi_done;
       __threadfence_block();
-      const uint32_t tail = *(volatile uint32_t *)&S.ring_tail;
-      const uint32_t avail = tail - head;
-      if (avail == 0) {
-        if (done == 128 * IX_EPI) break;
-        if (global_ns() - t_idle > 4 * kWaitLimitNs) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
-        __nanosleep(256);                      // idle: leave the issue slots to the epilogue warps
+      if (consume_ring(P, S, ctr)) {
+        t_idle = global_ns();
         continue;
       }
-      const uint32_t n = min(avail, 32u);
-      bool cand = false;
-      int b = 0, t = 0;
-      if ((uint32_t)lane < n) {
-        const uint32_t pos = head + lane;
-        const int slot = pos % IX_RING;
-        const uint64_t tw = global_ns();
-        bool ok = true;
-        while (*(volatile int32_t *)&S.ring_seq[slot] != (int32_t)(pos + 1)) {
-          if (global_ns() - tw > kWaitLimitNs) { ok = false; break; }
-        }
-        __threadfence_block();
-        b = S.ring_b[slot];
-        t = S.ring_t[slot];
-        cand = ok && b >= 0;
-        if (!ok) set_status(ctr, ECHO_ERR_TIMEOUT);
-      }
-      __syncwarp();
-      head += n;
-      if (lane == 0) *(volatile uint32_t *)&S.ring_head = head;
-      claim_and_copy(P, cand, b, t);
-      t_idle = global_ns();
+      if (done == 128u * IX_EPI) break;                // all pushed and all claimed
+      if (global_ns() - t_idle > 4 * kWaitLimitNs) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
+      __nanosleep(256);                                // idle: leave the issue slots to the epilogue
     }
   }
 
@@ -428,91 +459,9 @@ __global__ void __launch_bounds__(SX_THREADS)
 }
 
 // --------------------------------------------------- exact cap, rare path --
-// For a request whose qualifying tokens outnumber its cap, the optimistic claims
-// may hold the wrong tokens.  Re-derive the first cap qualifying tokens by
-// ascending t from the stored scores (qualifying = score > theta and not resident
-// at scoring time, i.e. host2gpu < 0 now), then swap wrongly staged tokens for
-// missing ones, reusing their staging rows.  Finally pf_count = min(count, cap).
-constexpr int FX_THREADS = 512;
-constexpr int FX_LIST = 2048;
-__global__ void __launch_bounds__(FX_THREADS) pf_finalize_kernel(IxParams P) {
-  const int b = blockIdx.x;
-  const int cap = min(P.cap[b], P.cap_max);
-  const int q = P.pf_count[b];
-  if (q <= cap) return;
-  const echo_cache_layer_t &L = P.L;
-  const int Lb = min(P.seq_len[b], P.Lmax);
-  const float theta = P.theta[b];
-  const int64_t base = P.host_base[b];
-  const float *sc = P.scores + (int64_t)b * P.Lmax;
-  __shared__ int32_t need_t[FX_LIST], free_row[FX_LIST], free_t[FX_LIST];
-  constexpr int NW = FX_THREADS / 32;
-  __shared__ uint32_t warp_cnt[NW], warp_base[NW];
-  __shared__ int n_need, n_free;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int span = (Lb + NW - 1) / NW;
-  const int w0 = warp * span, w1 = min(Lb, w0 + span);
-  const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-  for (int round = 0; round < 64; ++round) {
-    // pass 1: qualifying count per warp range
-    uint32_t c = 0;
-    for (int t = w0 + lane; t < ((w1 - w0 + 31) / 32) * 32 + w0; t += 32) {
-      bool ql = false;
-      if (t < w1 && sc[t] > theta) ql = L.host2gpu[base + t] < 0;
-      c += __popc(__ballot_sync(0xffffffffu, ql));
-    }
-    if (lane == 0) warp_cnt[warp] = c;
-    if (threadIdx.x == 0) { n_need = 0; n_free = 0; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t a = 0;
-      for (int w = 0; w < NW; ++w) { warp_base[w] = a; a += warp_cnt[w]; }
-    }
-    __syncthreads();
-    // pass 2: ranks; collect tokens to add (rank < cap, unstaged) and to drop
-    uint32_t r = warp_base[warp];
-    for (int t = w0 + lane; t < ((w1 - w0 + 31) / 32) * 32 + w0; t += 32) {
-      bool ql = false;
-      int32_t g = 0;
-      if (t < w1 && sc[t] > theta) { g = L.host2gpu[base + t]; ql = g < 0; }
-      const uint32_t bal = __ballot_sync(0xffffffffu, ql);
-      if (ql) {
-        const uint32_t rk = r + __popc(bal & lanemask_lt());
-        if (rk < (uint32_t)cap && g == -1) {
-          const int i = atomicAdd(&n_need, 1);
-          if (i < FX_LIST) need_t[i] = t;
-        } else if (rk >= (uint32_t)cap && g <= -2) {
-          const int i = atomicAdd(&n_free, 1);
-          if (i < FX_LIST) { free_row[i] = -2 - g; free_t[i] = t; }
-        }
-      }
-      r += __popc(bal);
-    }
-    __syncthreads();
-    const int np = min(min(n_need, n_free), FX_LIST);
-    if (np == 0) break;
-    // swap: the dropped token returns to "host only", the added one takes its row
-    for (int i = threadIdx.x; i < np; i += FX_THREADS) {
-      const int row = free_row[i];
-      L.host2gpu[base + free_t[i]] = -1;
-      L.host2gpu[base + need_t[i]] = -2 - row;
-      P.pf_list[row] = need_t[i];
-    }
-    __syncthreads();
-    for (int i0 = warp * 4; i0 < np; i0 += NW * 4) {
-      const uint4 *src[4] = {nullptr, nullptr, nullptr, nullptr};
-      uint4 *dst[4] = {nullptr, nullptr, nullptr, nullptr};
-      for (int j = 0; j < 4; ++j) {
-        const int i = i0 + j;
-        if (i >= np) break;
-        src[j] = reinterpret_cast<const uint4 *>((const char *)L.host_kv + (base + need_t[i]) * KV_W * esz);
-        dst[j] = reinterpret_cast<uint4 *>((char *)P.stage_kv + (int64_t)free_row[i] * KV_W * esz);
-      }
-      warp_copy_rows4(src, dst, KV_W * esz / 16);
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) P.pf_count[b] = cap;
+__global__ void __launch_bounds__(FX_THREADS) pf_finalize_kernel(const __grid_constant__ PfFix F, const float *theta) {
+  __shared__ PfFixSmem sm;
+  pf_fixup_block(F, blockIdx.x, theta[blockIdx.x], sm);
 }
 
 // ------------------------------------------------------------- host side --
@@ -551,9 +500,11 @@ extern "C" echo_status_t echo_index_prefetch(const void *q, const float *w, cons
                                              int32_t Lmax, int32_t dtype, const float *theta, const int32_t *cap,
                                              int32_t cap_max, const int32_t *host_base,
                                              const echo_cache_layer_t *layer, float *scores, int32_t *pf_list,
-                                             int32_t *pf_count, void *stage_kv, echo_stream_t stream) {
+                                             int32_t *pf_count, void *stage_kv, int32_t flags,
+                                             echo_stream_t stream) {
   if (!q || !w || !idx_k || !seq_len || !theta || !scores || B <= 0 || B > IX_MAXB || Lmax <= 0)
     return ECHO_ERR_INVALID_ARG;
+  if (flags & ~ECHO_PF_DEFER_CAP) return ECHO_ERR_INVALID_ARG;
   if (cap) {
     if (!layer || !host_base || !pf_list || !pf_count || !stage_kv || cap_max <= 0) return ECHO_ERR_INVALID_ARG;
     if (!layer->host2gpu || !layer->host_kv || !layer->counters) return ECHO_ERR_INVALID_ARG;
@@ -593,8 +544,9 @@ extern "C" echo_status_t echo_index_prefetch(const void *q, const float *w, cons
   } else {
     return ECHO_ERR_UNSUPPORTED;
   }
-  if (cap) {
-    pf_finalize_kernel<<<B, FX_THREADS, 0, st>>>(P);
+  if (cap && !(flags & ECHO_PF_DEFER_CAP)) {
+    const PfFix F = {seq_len, Lmax, cap, cap_max, host_base, P.L, scores, pf_list, pf_count, stage_kv};
+    pf_finalize_kernel<<<B, FX_THREADS, 0, st>>>(F, theta);
     ECHO_LAUNCH_OK();
   }
   return ECHO_OK;

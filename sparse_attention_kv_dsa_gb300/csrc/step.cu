@@ -2,6 +2,8 @@
 // "Decode: predict the transfer, then recall exactly": write-back of the new token,
 // prefetch budget, indexer scoring with fused threshold prefetch, exact top-k with
 // the EMA update, recall of every missing selected token, sparse MLA attention.
+// The exact prefetch cap is deferred from the indexer into the top-k launch, so
+// prefetch adds no launch of its own to the step.
 // Host code only: it launches the kernels of the other translation units; every
 // count it depends on stays in device memory, so the sequence can be captured in a
 // CUDA Graph and replayed step after step.
@@ -21,9 +23,11 @@ extern "C" echo_status_t echo_decode_layer_step(const echo_cache_layer_t *layer,
   }
   st = echo_index_prefetch(a->q_idx, a->w_idx, a->idx_k, a->seq_len, a->B, a->H, a->D, a->Lmax, a->idx_dtype,
                            a->theta, pf ? a->cap : nullptr, a->cap_max, a->host_base, layer, a->scores, a->pf_list,
-                           a->pf_count, a->stage_kv, stream);
+                           a->pf_count, a->stage_kv, pf ? ECHO_PF_DEFER_CAP : 0, stream);
   if (st != ECHO_OK) return st;
-  st = echo_topk(a->scores, a->seq_len, a->B, a->Lmax, a->k, a->sel, a->kth, a->theta, a->alpha, stream);
+  st = pf ? echo_topk_prefetch(a->scores, a->seq_len, a->B, a->Lmax, a->k, a->sel, a->kth, a->theta, a->alpha,
+                               a->cap, a->cap_max, a->host_base, layer, a->pf_list, a->pf_count, a->stage_kv, stream)
+          : echo_topk(a->scores, a->seq_len, a->B, a->Lmax, a->k, a->sel, a->kth, a->theta, a->alpha, stream);
   if (st != ECHO_OK) return st;
   st = echo_cache_recall(layer, a->sel, a->host_base, a->B, a->k, pf ? a->pf_list : nullptr,
                          pf ? a->pf_count : nullptr, a->cap_max, a->stage_kv, a->miss_list, a->n_miss, a->slot_idx,

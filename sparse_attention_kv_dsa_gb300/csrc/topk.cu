@@ -15,11 +15,15 @@
 // digit with no broadcast step.  Output: every key > K*, then the tokens equal to
 // K* with the lowest indices (ranks ordered across warps and CTAs), so ties go to
 // the lower token index.  The selection order is ascending t within each class.
+// echo_topk_prefetch also runs the indexer's deferred exact prefetch cap: after the
+// last cluster barrier, the rank-0 CTA of a request whose qualifiers outnumber its
+// cap reuses its shared memory for the fix-up (nothing to do in the common case).
 
 #include <algorithm>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "pf_fixup.cuh"
 
 namespace echo {
 
@@ -29,6 +33,7 @@ constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_BINS = 2048;
 constexpr int TK_BPT = TK_BINS / TK_THREADS;   // bins per thread (4)
 constexpr int TK_KEYCAP = 23 * 1024;    // keys cached per CTA (92 KB)
+static_assert(TK_THREADS == FX_THREADS, "the cap fix-up runs on one top-k CTA");
 
 struct TkShared {
   uint32_t hist[2][TK_BINS];
@@ -73,7 +78,7 @@ __device__ __forceinline__ float ema(float theta, float kth, float alpha) {
 
 __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
-                float *theta, float alpha) {
+                float *theta, float alpha, const __grid_constant__ PfFix F) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char dsm[];
@@ -90,6 +95,8 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   const int n = t1 - t0;
   // keys live in shared memory when the slice for Lmax fits (that is what was allocated)
   const bool cached = (((Lmax + TK_CL - 1) / TK_CL + 3) & ~3) <= TK_KEYCAP;
+  // the threshold the indexer scored against, read before rank 0 updates it
+  const float theta_scored = (F.cap != nullptr && rank == 0) ? theta[b] : 0.f;
 
   if (L <= k) {
     // every token is selected; kth = smallest score
@@ -113,6 +120,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       theta[b] = ema(theta[b], kv, alpha);
     }
     cluster_sync();
+    if (F.cap != nullptr && rank == 0) pf_fixup_block(F, b, theta_scored, *reinterpret_cast<PfFixSmem *>(dsm));
     return;
   }
 
@@ -234,13 +242,29 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     theta[b] = ema(theta[b], kv, alpha);
   }
   cluster_sync();
+  // no other CTA reads this one's shared memory any more: it becomes the fix-up's scratch
+  if (F.cap != nullptr && rank == 0) pf_fixup_block(F, b, theta_scored, *reinterpret_cast<PfFixSmem *>(dsm));
 }
 
-static size_t topk_smem(int Lmax) {
+static size_t topk_smem(int Lmax, bool fix) {
   const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
   size_t s = (sizeof(TkShared) + 15) & ~size_t(15);
   if (per <= TK_KEYCAP) s += (size_t)per * 4;
+  if (fix) s = std::max(s, sizeof(PfFixSmem));
   return s;
+}
+
+static echo_status_t launch_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t k,
+                                 int32_t *out_idx, float *kth, float *theta, float alpha, const PfFix &F,
+                                 echo_stream_t stream) {
+  if (!scores || !seq_len || !out_idx || !kth || !theta || B <= 0 || Lmax <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
+  if (!(alpha >= 0.f && alpha <= 1.f)) return ECHO_ERR_INVALID_ARG;
+  const size_t smem = topk_smem(Lmax, F.cap != nullptr);
+  ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  topk_kernel<<<B * TK_CL, TK_THREADS, smem, (cudaStream_t)stream>>>(scores, seq_len, Lmax, k, out_idx, kth, theta,
+                                                                     alpha, F);
+  ECHO_LAUNCH_OK();
+  return ECHO_OK;
 }
 
 }  // namespace echo
@@ -249,12 +273,17 @@ using namespace echo;
 
 extern "C" echo_status_t echo_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t k,
                                    int32_t *out_idx, float *kth, float *theta, float alpha, echo_stream_t stream) {
-  if (!scores || !seq_len || !out_idx || !kth || !theta || B <= 0 || Lmax <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
-  if (!(alpha >= 0.f && alpha <= 1.f)) return ECHO_ERR_INVALID_ARG;
-  const size_t smem = topk_smem(Lmax);
-  ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  topk_kernel<<<B * TK_CL, TK_THREADS, smem, (cudaStream_t)stream>>>(scores, seq_len, Lmax, k, out_idx, kth, theta,
-                                                                     alpha);
-  ECHO_LAUNCH_OK();
-  return ECHO_OK;
+  const PfFix none = {};
+  return launch_topk(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, none, stream);
+}
+
+extern "C" echo_status_t echo_topk_prefetch(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax,
+                                            int32_t k, int32_t *out_idx, float *kth, float *theta, float alpha,
+                                            const int32_t *cap, int32_t cap_max, const int32_t *host_base,
+                                            const echo_cache_layer_t *layer, int32_t *pf_list, int32_t *pf_count,
+                                            void *stage_kv, echo_stream_t stream) {
+  if (!cap || cap_max <= 0 || !host_base || !layer || !pf_list || !pf_count || !stage_kv) return ECHO_ERR_INVALID_ARG;
+  if (!layer->host2gpu || !layer->host_kv) return ECHO_ERR_INVALID_ARG;
+  const PfFix F = {seq_len, Lmax, cap, cap_max, host_base, *layer, scores, pf_list, pf_count, stage_kv};
+  return launch_topk(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, F, stream);
 }

@@ -18,6 +18,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_POOL_EXHAUSTED, ERR_HOST_INDEX, ERR_STAGING = range(8)
 ERR_SCRATCH_LIMIT = 8
 MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
+PF_DEFER_CAP = 1            # echo_index_prefetch flag: exact cap restored by echo_topk_prefetch
 F32, BF16, E4M3 = 0, 1, 2
 KV_WIDTH, V_WIDTH = 576, 512
 CTR_STEP, CTR_N_FREE, CTR_STATUS, CTR_NEED, CTR_CURSOR, CTR_EVICT_M = 0, 1, 2, 3, 4, 5
@@ -66,8 +67,9 @@ SIGNATURES = {
     "echo_cache_reset": (_I, [_P, _P]),
     "echo_cache_writeback": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P]),
     "echo_cache_reserve": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
-    "echo_index_prefetch": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "echo_index_prefetch": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "echo_topk": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _F, _P]),
+    "echo_topk_prefetch": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _F, _P, _I, _P, _P, _P, _P, _P, _P]),
     "echo_cache_evict": (_I, [_P, _P, _P]),
     "echo_cache_alloc": (_I, [_P, _P, _P, _I, _P, _P]),
     "echo_cache_recall": (_I, [_P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
@@ -196,19 +198,30 @@ def cache_reserve(layer: LayerCache, seq_len, cap_max: int, cap_div: int, cap, p
 
 
 def index_prefetch(q, w, idx_k, seq_len, theta, scores, *, layer: LayerCache | None = None, cap=None,
-                   cap_max: int = 0, host_base=None, pf_list=None, pf_count=None, stage_kv=None, stream=None):
+                   cap_max: int = 0, host_base=None, pf_list=None, pf_count=None, stage_kv=None,
+                   defer_cap: bool = False, stream=None):
     B, H, D = q.shape
     Lmax = idx_k.shape[1]
     check(lib().echo_index_prefetch(ptr(q), ptr(w), ptr(idx_k), ptr(seq_len), B, H, D, Lmax, dtype_code(q.dtype),
                                     ptr(theta), ptr(cap), cap_max, ptr(host_base),
                                     layer.ref if layer is not None else None, ptr(scores), ptr(pf_list),
-                                    ptr(pf_count), ptr(stage_kv), stream_handle(stream)), "index_prefetch")
+                                    ptr(pf_count), ptr(stage_kv), PF_DEFER_CAP if defer_cap else 0,
+                                    stream_handle(stream)), "index_prefetch")
 
 
 def topk(scores, seq_len, k: int, out_idx, kth, theta, alpha: float = 0.5, stream=None):
     B, Lmax = scores.shape
     check(lib().echo_topk(ptr(scores), ptr(seq_len), B, Lmax, k, ptr(out_idx), ptr(kth), ptr(theta), alpha,
                           stream_handle(stream)), "topk")
+
+
+def topk_prefetch(scores, seq_len, k: int, out_idx, kth, theta, alpha: float, *, layer: LayerCache, cap,
+                  cap_max: int, host_base, pf_list, pf_count, stage_kv, stream=None):
+    """Top-k plus the exact prefetch cap deferred by index_prefetch(defer_cap=True)."""
+    B, Lmax = scores.shape
+    check(lib().echo_topk_prefetch(ptr(scores), ptr(seq_len), B, Lmax, k, ptr(out_idx), ptr(kth), ptr(theta), alpha,
+                                   ptr(cap), cap_max, ptr(host_base), layer.ref, ptr(pf_list), ptr(pf_count),
+                                   ptr(stage_kv), stream_handle(stream)), "topk_prefetch")
 
 
 def cache_evict(layer: LayerCache, n_needed, stream=None):

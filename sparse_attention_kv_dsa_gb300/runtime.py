@@ -130,6 +130,30 @@ class DecodeLayer:
     def step(self, stream=None, args: E.StepArgsT | None = None):
         E.decode_layer_step(self.cache, args or self.args, stream)
 
+    def step_ops(self, stream=None, *, defer_cap: bool = True):
+        """The same step issued as its separate entry points.  defer_cap=False keeps
+        the exact prefetch cap inside the indexer call (its own small launch) and uses
+        the plain top-k; True defers it into the top-k launch, as the fused step does."""
+        wl, sc, c = self.wl, self.scratch, self.cache
+        pf = self.prefetch
+        E.cache_writeback(c, self.new_kv, self.new_ik, self.idx_k, self.host_base, self.seq_len, stream)
+        if pf:
+            E.cache_reserve(c, self.seq_len, self.cap_max, wl.cap_div, self.cap, self.pf_count, stream)
+        E.index_prefetch(self.q_idx, self.w_idx, self.idx_k, self.seq_len, self.theta, sc.scores, layer=c,
+                         cap=self.cap if pf else None, cap_max=self.cap_max, host_base=self.host_base,
+                         pf_list=self.pf_list, pf_count=self.pf_count, stage_kv=sc.stage_kv,
+                         defer_cap=pf and defer_cap, stream=stream)
+        if pf and defer_cap:
+            E.topk_prefetch(sc.scores, self.seq_len, wl.topk, self.sel, self.kth, self.theta, wl.alpha, layer=c,
+                            cap=self.cap, cap_max=self.cap_max, host_base=self.host_base, pf_list=self.pf_list,
+                            pf_count=self.pf_count, stage_kv=sc.stage_kv, stream=stream)
+        else:
+            E.topk(sc.scores, self.seq_len, wl.topk, self.sel, self.kth, self.theta, wl.alpha, stream)
+        E.cache_recall(c, self.sel, self.host_base, self.miss_list, self.n_miss, self.slot_idx,
+                       pf_list=self.pf_list if pf else None, pf_count=self.pf_count if pf else None,
+                       cap_max=self.cap_max, stage_kv=sc.stage_kv, stream=stream)
+        E.sparse_mla_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, sc.mla_ws, stream)
+
     # ------------------------------------------------------------- snapshot --
     def snapshot(self) -> dict:
         """Host copy of the cache state (for hand-off to the oracle)."""

@@ -57,11 +57,16 @@ class Lockstep:
         self.prefetch = self.dl.prefetch
         self.s = 0
 
-    def step(self, args=None):
+    def step(self, args=None, ops=None):
+        """One step on both sides; ops (a dict of DecodeLayer.step_ops arguments)
+        issues the GPU step as separate entry-point calls instead of the fused one."""
         wl, l, s = self.wl, self.layer, self.s
         dl = self.dl
         dl.set_step_inputs(self.inp.q_int[l][s], self.inp.new_ik[l][s], self.inp.new_kv[l][s], self.inp.q_mla[l][s])
-        dl.step(args=args)
+        if ops is not None:
+            dl.step_ops(**ops)
+        else:
+            dl.step(args=args)
         torch.cuda.synchronize()
         new_ik = S.grid_to_float(self.inp.new_ik[l][s].cpu()).numpy()
         new_kv = self.inp.new_kv[l][s].float().cpu().numpy()

@@ -11,12 +11,12 @@ from sparse_attention_kv_dsa_gb300 import synth as S
 pytestmark = pytest.mark.gpu
 
 
-def run(wl, steps=None, **kw):
+def run(wl, steps=None, ops=None, **kw):
     from harness import Lockstep
     ls = Lockstep(wl, **kw)
     stats = []
     for _ in range(steps or wl.steps):
-        r = ls.step()
+        r = ls.step(ops=ops)
         stats.append(ls.compare(r))
     return ls, stats
 
@@ -43,6 +43,17 @@ def test_fp8_cap_binds_exact_first_tokens():
     # a tiny cap: qualifying tokens outnumber it, the exact "first cap by t" rule applies
     wl = S.small_workload("fp8-capbind", ctx=(1800, 2500), topk=256, n_gpu=4096, steps=4, cap_max=8, rho=0.5)
     ls, st = run(wl)
+    ctr = ls.dl.cache.read_counters()
+    assert ctr[15] > ctr[12], "qualifying tokens did not exceed the cap"
+
+
+@pytest.mark.parametrize("defer_cap", [False, True])
+def test_fp8_cap_binds_through_separate_entry_points(defer_cap):
+    # the exact cap restored by the indexer's own fix-up launch, or deferred into the
+    # top-k launch (echo_topk_prefetch): both must give the oracle's staged set
+    wl = S.small_workload("fp8-capbind-ops", ctx=(1800, 2500, 400), topk=256, n_gpu=4096, steps=4, cap_max=8,
+                          rho=0.5)
+    ls, st = run(wl, ops={"defer_cap": defer_cap})
     ctr = ls.dl.cache.read_counters()
     assert ctr[15] > ctr[12], "qualifying tokens did not exceed the cap"
 
