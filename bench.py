@@ -483,10 +483,10 @@ def run_echo(args, ws, rank, local):
 
 
 def launches_per_step(prefetch: bool) -> int:
-    """Kernels of one layer step: write-back 1, reserve 1, indexer 1, top-k 1 (with the
-    deferred exact prefetch cap), recall 3 (miss detect, evict+bind cluster,
-    copy+translate), MLA 2."""
-    return (1 + 1 + 1 + 1 + 3 + 2) if prefetch else (1 + 1 + 1 + 3 + 2)
+    """Kernels of one layer step: write-back 1 (cooperative manager), reserve 1,
+    indexer 1, top-k 1 (with the deferred exact prefetch cap), recall 1 (cooperative
+    manager: protect, miss list, evict+bind, copy, translate), MLA 2."""
+    return (1 + 1 + 1 + 1 + 1 + 2) if prefetch else (1 + 1 + 1 + 1 + 2)
 
 
 def enqueue_index_topk(lib, dl, h, between=None):

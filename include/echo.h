@@ -72,6 +72,8 @@ enum {
   ECHO_CTR_WB_EVICTED = 13, /*   tokens evicted by the write-back                       */
   ECHO_CTR_BOUND = 14,      /*   tokens bound to slots by the recall                    */
   ECHO_CTR_QUALIFIED = 15,  /*   tokens that met the prefetch rule (before the cap)     */
+                            /* 16..31: the manager's own words (grid barrier, cursors);  */
+                            /*   zero between calls, set to zero by echo_cache_reset     */
   ECHO_NUM_COUNTERS = 32
 };
 
@@ -84,11 +86,17 @@ enum {
  *                      this step at staging row (-2 - value), until the recall binds it
  *   gpu2host[n_gpu]  : host token in each slot; -1 = free
  *   priority[n_gpu]  : step of the slot's last touch (LRU key with the host index)
- *   index_buf[n_gpu] : scratch index buffer used by allocation
+ *   index_buf[n_gpu] : the manager's scratch (victim-selection histograms, at most
+ *                      3 x 2048 words; pools under 6 slots use counter words 24..29);
+ *                      zero between calls
  *   free_map[n_gpu]  : one byte per slot, 1 = free
  * Metadata = 4*n_host + 13*n_gpu bytes (echo_cache_metadata_bytes) plus the fixed
- * 128-byte counters block.  gpu2host and priority must be 16-byte aligned (they are
- * read as int4 vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
+ * 128-byte counters block.  gpu2host, priority and counters must be 16-byte aligned
+ * (read as vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
+ * The manager calls (write-back, recall, alloc, evict) are cooperative launches over
+ * the whole device, one CTA per SM; calls on one layer must not run concurrently.
+ * A manager call whose grid barrier waited more than ~1 s sets ECHO_ERR_TIMEOUT and
+ * leaves the layer undefined until echo_cache_reset.
  */
 typedef struct {
   int32_t n_gpu;

@@ -10,18 +10,27 @@
 // grids with device-side counts so a whole step can be captured in one CUDA Graph.
 //
 // Kernels
-//   reset_kernel          empty cache
-//   reserve_kernel        per-request prefetch budget (A2)
-//   manage_kernel<CL>     one thread-block cluster: LRU victim selection by radix
-//                         select over keys held in shared memory, eviction, and
-//                         allocation by warp-ballot scan of the free bitmap with one
-//                         atomic per warp; modes write-back (A1), recall bind (A7+A8),
-//                         alloc (A8), evict (A7)
-//   miss_kernel           protect hits, list misses (A6)
-//   copy_translate_kernel zero-copy host reads + staged rows into slots, slot ids (A9, A10)
+//   reset_kernel    empty cache
+//   reserve_kernel  per-request prefetch budget (A2)
+//   mgr_kernel      one cooperative launch over the whole GPU (one CTA per SM) per
+//                   call, in phases separated by bounded grid barriers:
+//                   recall only: protect hits and list misses (A6);
+//                   LRU victim selection: every CTA keeps the victim keys of its
+//                   slice of slots in shared memory; an MSB-first radix select
+//                   builds each digit's histogram from per-CTA shared histograms
+//                   added into a global one, and every CTA derives the same digit
+//                   from it (no broadcast step); only the bits below the largest
+//                   key's top bit are visited;
+//                   eviction and binding: victims ranked by one global atomic per
+//                   warp and rebound at once to the tokens that need a slot; free
+//                   slots found by a warp-ballot scan of the free bitmap with one
+//                   atomic per warp (A7 + A8);
+//                   then the data: write-back of the new token (A1), or the recall's
+//                   zero-copy host reads and staged rows into slots plus the slot
+//                   translation (A9 + A10).
+//                   Modes: write-back, recall, alloc, evict.
 
 #include <algorithm>
-#include <cooperative_groups.h>
 
 #include "common.cuh"
 
@@ -55,12 +64,28 @@ __global__ void reserve_kernel(echo_cache_layer_t L, const int32_t *seq_len, int
   }
 }
 
-// ------------------------------------------------------ cluster management --
+// ---------------------------------------------------------------- manager --
 enum { MODE_WRITEBACK = 0, MODE_RECALL = 1, MODE_ALLOC = 2, MODE_EVICT = 3 };
+
+// Counter words 16..31 belong to the manager (zero between calls, except the barrier
+// count, which only grows):
+enum {
+  MG_BAR = 16,         // words 16-17: grid barrier arrivals (uint64, a multiple of the grid between barriers)
+  MG_ABORT = 18,       // a barrier wait gave up: every CTA leaves
+  MG_VCUR = 22,        // victim rank cursor
+  MG_SCUR = 23,        // free-slot scan cursor
+  MG_SMALL_HIST = 24,  // words 24..29: the histograms of pools with fewer than 6 slots
+};
 
 struct ManageParams {
   echo_cache_layer_t L;
   int mode;
+  int dbits;              // radix digit width
+  uint32_t *hist;         // 3 global histograms of 2^dbits words: index_buf, or counter words 24..29
+                          // for pools too small to hold them
+  int32_t *miss_cnt;      // per-request miss counters (zero between calls) after the histograms in
+                          // index_buf, or null: n_miss is zeroed and a grid barrier follows
+  int cached;             // victim keys fit in shared memory
   // write-back
   const void *new_kv;
   const void *new_ik;
@@ -70,12 +95,15 @@ struct ManageParams {
   int32_t *seq_len;
   int B;
   // recall
+  const int32_t *sel;
+  int k;
   const int32_t *pf_list;
   const int32_t *pf_count;
   int cap_max;
-  const int32_t *miss_list;
-  const int32_t *n_miss;
-  int k;
+  const void *stage_kv;
+  int32_t *miss_list;
+  int32_t *n_miss;
+  int32_t *slot_idx;
   // alloc
   const int32_t *host_idx;
   const int32_t *n_ptr;
@@ -85,21 +113,83 @@ struct ManageParams {
   const int32_t *n_needed;
 };
 
-constexpr int MG_THREADS = 1024;
-constexpr int NBINS = 2048;          // 11-bit radix digits
-constexpr int KEYCAP = 24 * 1024;    // 64-bit keys cached per CTA (192 KB)
-constexpr int MAXB = 1024;           // requests per call handled by the manager
+constexpr int MG_THREADS = 512;
+constexpr int MG_WARPS = MG_THREADS / 32;
+constexpr int MG_MAXBITS = 11;                  // 2048-bin digits at most
+constexpr int MG_BPT = (1 << MG_MAXBITS) / MG_THREADS;   // bins per thread in the digit search
+constexpr int MAXB = 1024;                      // requests per call handled by the manager
+constexpr size_t MG_KEY_SMEM = 192 * 1024;      // victim keys cached per CTA (bytes)
 
 struct MgShared {
-  uint32_t hist[2][NBINS];
-  uint32_t warp_sums[32];
-  uint32_t res[4];                   // [0] chosen digit, [1] count above it
-  uint32_t cursor;                   // allocation cursor (CTA 0's copy is used)
-  uint32_t cnt;                      // eligible count of this CTA
-  uint32_t vcnt, vcur;               // victims of this CTA, victim-rank cursor
-  int32_t pre_a[MAXB + 1];           // prefixes of the token lists
+  uint32_t hist[1 << MG_MAXBITS];
+  int32_t pre_a[MAXB + 1];             // prefixes of the token lists
   int32_t pre_b[MAXB + 1];
+  uint32_t warp_sums[32];
+  uint32_t wcnt[MG_WARPS];             // per-warp counts (block reductions, victim ranks)
+  uint32_t res[2];                     // [0] chosen digit, [1] count above it
+  uint32_t base;                       // this CTA's first rank from a global cursor
 };
+
+__device__ __forceinline__ int bitlen_u64(uint64_t x) { return x ? 64 - __clzll((long long)x) : 0; }
+
+// Reads of words that other CTAs of the same launch write go around L1.
+__device__ __forceinline__ int32_t ldcg(const int32_t *p) { return __ldcg(p); }
+
+// Grid-wide barrier of a cooperative launch with a bounded wait.  Arrivals count up
+// a 64-bit word by one per CTA; a barrier is complete when it reaches the next
+// multiple of the grid size.  A CTA that has waited ~1 s sets TIMEOUT and the abort
+// word; every CTA then leaves the kernel.  All CTAs must call it the same number of
+// times.  Returns false on abort.
+__device__ __noinline__ bool grid_sync(int32_t *ctr) {
+  __shared__ int32_t gs_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long *cnt = reinterpret_cast<unsigned long long *>(ctr + MG_BAR);
+    unsigned long long old, cur;
+    asm volatile("fence.acq_rel.gpu;\n\tatom.relaxed.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(cnt) : "memory");
+    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    int ok = 1, spins = 0;
+    uint64_t t0 = 0;
+    while (true) {
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(cnt) : "memory");
+      if (cur >= target) break;
+      if (++spins == 256) {
+        spins = 0;
+        if (*reinterpret_cast<volatile int32_t *>(ctr + MG_ABORT)) { ok = 0; break; }
+        if (!t0) {
+          t0 = global_ns();
+        } else if (global_ns() - t0 > kWaitLimitNs) {
+          set_status(ctr, ECHO_ERR_TIMEOUT);
+          atomicExch(ctr + MG_ABORT, 1);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    gs_ok = ok;
+  }
+  __syncthreads();
+  return gs_ok != 0;
+}
+
+// Sum over the CTA (every thread gets it); ends with a barrier.
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t *wcnt) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) wcnt[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t t = 0;
+#pragma unroll
+  for (int w = 0; w < MG_WARPS; ++w) t += wcnt[w];
+  __syncthreads();
+  return t;
+}
+
+// Victim key of a slot: larger key = smaller (priority, host index) = evicted first;
+// 0 = not evictable (free, or touched in the current step).
+__device__ __forceinline__ uint64_t victim_key(int32_t h, int32_t p, int32_t step, int hbits, uint64_t hmax) {
+  if (h < 0 || p >= step || p < 0) return 0;
+  return (((uint64_t)(int64_t)(step - 1 - p) << hbits) | (hmax - (uint64_t)h)) + 1;
+}
 
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
   const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -126,77 +216,101 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_s
   return v;
 }
 
-__device__ __forceinline__ int bitlen_u64(uint64_t x) { return x ? 64 - __clzll((long long)x) : 0; }
-
-// Victim key of slot g: larger key = smaller (priority, host index) = evicted first.
-// 0 = not evictable (free, or touched in the current step).
-__device__ __forceinline__ uint64_t victim_key(const echo_cache_layer_t &L, int g, int32_t step, int hbits,
-                                               uint64_t hmax) {
-  const int32_t h = L.gpu2host[g];
-  if (h < 0) return 0;
-  const int32_t p = L.priority[g];
-  if (p >= step || p < 0) return 0;
-  const uint64_t age = (uint64_t)(int64_t)(step - 1 - p);
-  return ((age << hbits) | (hmax - (uint64_t)h)) + 1;
-}
-
-template <int CL>
-__global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
-  namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
+__global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constant__ ManageParams P) {
   extern __shared__ __align__(16) unsigned char dsm[];
   MgShared &S = *reinterpret_cast<MgShared *>(dsm);
   uint64_t *keys = reinterpret_cast<uint64_t *>(dsm + ((sizeof(MgShared) + 15) & ~size_t(15)));
   const echo_cache_layer_t &L = P.L;
-  const int tid = threadIdx.x;
-  const uint32_t rank = cluster_rank();
   int32_t *ctr = L.counters;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t gtid = blockIdx.x * (int64_t)MG_THREADS + tid;
+  const int64_t gthreads = (int64_t)gridDim.x * MG_THREADS;
+  const int64_t gwarp = gtid >> 5, gwarps = gthreads >> 5;
 
-  const int32_t step0 = ctr[ECHO_CTR_STEP];
+  const int32_t step0 = ldcg(ctr + ECHO_CTR_STEP);
   const int32_t step = P.mode == MODE_WRITEBACK ? step0 + 1 : step0;
-  const int32_t n_free0 = ctr[ECHO_CTR_N_FREE];
+  const int32_t n_free0 = ldcg(ctr + ECHO_CTR_N_FREE);
 
-  // ---- the tokens that need a slot: list A (+ list B) ------------------
+  // ---- recall: protect every selected resident token, list the misses (A6) ----
+  // Miss positions come from per-request counters that are zero on entry (the
+  // manager's scratch), or from n_miss zeroed behind a grid barrier.
+  int32_t *mcnt = P.miss_cnt ? P.miss_cnt : P.n_miss;
+  if (P.mode == MODE_RECALL) {
+    if (!P.miss_cnt) {
+      if (blockIdx.x == 0)
+        for (int b = tid; b < P.B; b += MG_THREADS) P.n_miss[b] = 0;
+      if (!grid_sync(ctr)) return;
+    }
+    uint32_t hit = 0, staged = 0, miss = 0;
+    const int64_t nsel = (int64_t)P.B * P.k;
+    for (int64_t i = gtid; i < nsel; i += gthreads) {
+      const int b = (int)(i / P.k);
+      const int32_t t = P.sel[i];
+      if (t < 0) continue;
+      const int64_t h = (int64_t)P.host_base[b] + t;
+      if (h >= L.n_host) {
+        set_status(ctr, ECHO_ERR_HOST_INDEX);
+        continue;
+      }
+      const int32_t g = ldcg(L.host2gpu + h);
+      if (g >= 0) {
+        L.priority[g] = step;                            // protect the selection
+        ++hit;
+      } else if (g <= -2) {
+        ++staged;
+      } else {
+        const int32_t pos = atomicAdd(mcnt + b, 1);
+        P.miss_list[(int64_t)b * P.k + pos] = t;
+        ++miss;
+      }
+    }
+    hit = block_sum(hit, S.wcnt);
+    staged = block_sum(staged, S.wcnt);
+    miss = block_sum(miss, S.wcnt);
+    if (tid == 0) {
+      if (hit) atomicAdd(ctr + ECHO_CTR_HITS, (int)hit);
+      if (staged) atomicAdd(ctr + ECHO_CTR_STAGED_HITS, (int)staged);
+      if (miss) atomicAdd(ctr + ECHO_CTR_MISSES, (int)miss);
+    }
+    if (!grid_sync(ctr)) return;
+    if (P.miss_cnt && blockIdx.x == 0)
+      for (int b = tid; b < P.B; b += MG_THREADS) P.n_miss[b] = ldcg(P.miss_cnt + b);
+  }
+
+  // ---- the tokens that need a slot: list A (+ list B), same in every CTA ----
   // write-back: A = new tokens not yet resident; recall: A = staged rows,
   // B = misses; alloc: A = host_idx[0..n).
-  int nA = 0, nB = 0;
   if (P.mode == MODE_WRITEBACK) {
     block_prefix(P.B, [&](int b) {
       const int32_t l = P.seq_len[b];
       const int64_t h = (int64_t)P.host_base[b] + l;
       const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
-      return (ok && L.host2gpu[h] < 0) ? 1 : 0;
+      return (ok && ldcg(L.host2gpu + h) < 0) ? 1 : 0;
     }, S.pre_a);
   } else if (P.mode == MODE_RECALL) {
     const int32_t *pfc = P.pf_count;
     const int cm = P.cap_max;
     block_prefix(P.B, [&](int b) { return pfc ? min(max(pfc[b], 0), cm) : 0; }, S.pre_a);
-    block_prefix(P.B, [&](int b) { return (int)P.n_miss[b]; }, S.pre_b);
+    block_prefix(P.B, [&](int b) { return (int)ldcg(mcnt + b); }, S.pre_b);
   }
-  if (tid == 0) { S.cursor = 0; S.cnt = 0; S.vcnt = 0; S.vcur = 0; }
   __syncthreads();
+  int nA = 0, nB = 0;
   if (P.mode == MODE_WRITEBACK) nA = S.pre_a[P.B];
   if (P.mode == MODE_RECALL) { nA = S.pre_a[P.B]; nB = S.pre_b[P.B]; }
   if (P.mode == MODE_ALLOC) nA = min(max(*P.n_ptr, 0), P.n_max);
   const int n_bind = (P.mode == MODE_EVICT) ? 0 : nA + nB;
-
-  int m_req = 0;                           // victims wanted
+  int m_req = 0;                                         // victims wanted
   if (P.mode == MODE_WRITEBACK || P.mode == MODE_RECALL) m_req = max(0, n_bind - n_free0);
   if (P.mode == MODE_EVICT) m_req = max(0, *P.n_needed - n_free0);
-
-  // ---- this CTA's slot range ----------------------------------------------
-  const int per = ((L.n_gpu + CL - 1) / CL + 3) & ~3;     // slices start 16-byte aligned
-  const int g0 = min(L.n_gpu, (int)rank * per), g1 = min(L.n_gpu, g0 + per);
-  const int nloc = g1 - g0;
-  const bool cached = per <= KEYCAP;
-  int hbits = bitlen_u64((uint64_t)max(L.n_host - 1, 1));
-  const uint64_t hmax = (1ull << hbits) - 1;
-  const int nb = bitlen_u64((uint64_t)max(step, 1)) + hbits + 1;
-
   // tokens of ranks [0, n_scan) go to slots that were already free (bitmap scan);
   // tokens of ranks [n_scan, n_bind) go straight to this call's victims
   const int n_scan = min(max((int)n_free0, 0), n_bind);
-  // host index of the token of rank r
+  // the write-back's list reads host2gpu, which bindings change: no CTA may bind
+  // before every CTA has its list (with eviction the barrier after the keys does it)
+  if (P.mode == MODE_WRITEBACK && m_req == 0)
+    if (!grid_sync(ctr)) return;
+
+  // host index of the token of rank r (and its request)
   auto token_of = [&](uint32_t r, int *req) -> int64_t {
     if (P.mode == MODE_WRITEBACK) {
       int b = 0;                                   // rank r -> request (B is small)
@@ -212,14 +326,14 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
         if (pre[mid] <= rr) lo = mid; else hi = mid - 1;
       }
       const int b = lo, ii = rr - pre[b];
-      const int32_t t = (int)r < nA ? P.pf_list[(int64_t)b * P.cap_max + ii] : P.miss_list[(int64_t)b * P.k + ii];
+      const int32_t t = (int)r < nA ? P.pf_list[(int64_t)b * P.cap_max + ii] : ldcg(P.miss_list + (int64_t)b * P.k + ii);
       *req = b;
       return (int64_t)P.host_base[b] + t;
     }
     *req = 0;
     return P.host_idx[r];
   };
-  // bind the token of rank r to slot g (slot already removed from the free bitmap)
+  // bind the token of rank r to slot g (a victim, or a slot taken from the bitmap)
   auto bind = [&](int g, uint32_t r) {
     int b = 0;
     const int64_t h = token_of(r, &b);
@@ -228,7 +342,6 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
       L.gpu2host[g] = (int32_t)h;
       L.host2gpu[h] = g;
       L.priority[g] = step;
-      if (P.mode == MODE_WRITEBACK) L.index_buf[b] = g;
       if (P.mode == MODE_ALLOC && P.out_slot) P.out_slot[r] = g;
     } else {
       L.gpu2host[g] = -1;
@@ -238,112 +351,122 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
     }
   };
 
-  uint32_t m_eff = 0;
-  uint64_t kstar = ~0ull;
-  if (m_req > 0) {                                         // uniform across the cluster
-    // load keys (4 slots per thread and iteration, both arrays as int4), count evictable
-    uint32_t c = 0;
-    const int n4 = nloc >> 2;
-    const int4 *g2h4 = reinterpret_cast<const int4 *>(L.gpu2host + g0);
-    const int4 *pr4 = reinterpret_cast<const int4 *>(L.priority + g0);
-    auto key_of = [&](int32_t hh, int32_t pp) -> uint64_t {
-      if (hh < 0 || pp >= step || pp < 0) return 0;
-      return (((uint64_t)(int64_t)(step - 1 - pp) << hbits) | (hmax - (uint64_t)hh)) + 1;
-    };
-    for (int j = tid; j < n4; j += MG_THREADS) {
-      const int4 hv = g2h4[j], pv = pr4[j];
-      const uint64_t k0 = key_of(hv.x, pv.x), k1 = key_of(hv.y, pv.y), k2 = key_of(hv.z, pv.z),
-                     k3 = key_of(hv.w, pv.w);
-      if (cached) {
-        keys[4 * j] = k0; keys[4 * j + 1] = k1; keys[4 * j + 2] = k2; keys[4 * j + 3] = k3;
-      }
-      c += (k0 != 0) + (k1 != 0) + (k2 != 0) + (k3 != 0);
-    }
-    for (int i = 4 * n4 + tid; i < nloc; i += MG_THREADS) {
-      const uint64_t kk = victim_key(L, g0 + i, step, hbits, hmax);
-      if (cached) keys[i] = kk;
-      c += kk != 0;
-    }
-    c = __reduce_add_sync(0xffffffffu, c);
-    if ((tid & 31) == 0) atomicAdd(&S.cnt, c);
-    __syncthreads();
-    cluster_sync();
-    uint32_t total = 0;
-    for (uint32_t r = 0; r < CL; ++r) total += *cluster.map_shared_rank(&S.cnt, r);
-    m_eff = min((uint32_t)m_req, total);
-    if (rank == 0 && tid == 0 && m_eff < (uint32_t)m_req) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
+  // ---- this CTA's slice of slots ----------------------------------------------
+  const int per = ((L.n_gpu + (int)gridDim.x - 1) / (int)gridDim.x + 3) & ~3;   // 16-byte aligned starts
+  const int g0 = min(L.n_gpu, (int)blockIdx.x * per), g1 = min(L.n_gpu, g0 + per);
+  const int nloc = g1 - g0;
+  const bool cached = P.cached != 0;
+  const int hbits = bitlen_u64((uint64_t)max(L.n_host - 1, 1));
+  const uint64_t hmax = (1ull << hbits) - 1;
+  auto key_at = [&](int i) -> uint64_t {        // i: index within the slice
+    return cached ? keys[i] : victim_key(ldcg(L.gpu2host + g0 + i), ldcg(L.priority + g0 + i), step, hbits, hmax);
+  };
 
-    if (m_eff > 0) {
-      // MSB-first radix select of the m_eff-th largest key (keys are unique).
-      uint64_t prefix = 0;
-      uint32_t above = 0;
-      int left = nb, buf = 0;
-      while (left > 0) {
-        const int w = min(11, left), shift = left - w;
-        uint32_t *h = S.hist[buf];
-        for (int i = tid; i < NBINS; i += MG_THREADS) h[i] = 0;
-        __syncthreads();
-        const uint64_t hi_mask = (shift + w >= 64) ? 0ull : (~0ull << (shift + w));
-        for (int base = 0; base < nloc; base += MG_THREADS) {   // uniform trip count per warp
-          const int i = base + tid;
-          uint64_t kk = 0;
-          if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
-          hist_add_warp(h, kk != 0 && (kk & hi_mask) == (prefix & hi_mask),
-                        (uint32_t)((kk >> shift) & ((1u << w) - 1)));
-        }
-        __syncthreads();
-        cluster_sync();
-        // global counts of my two bins; find the digit (descending)
-        const int d1 = 2 * tid + 1, d0 = 2 * tid;
-        uint32_t c1 = 0, c0 = 0;
-#pragma unroll
-        for (uint32_t r = 0; r < CL; ++r) {             // plain loads, issued together
-          const uint2 v = *reinterpret_cast<const uint2 *>(cluster.map_shared_rank(&h[d0], r));
-          c0 += v.x;
-          c1 += v.y;
-        }
-        uint32_t tot;
-        const uint32_t incl = block_incl_scan(c0 + c1, S.warp_sums, &tot);
-        const uint32_t sfx = tot - incl;                     // keys in bins above mine
-        const uint32_t need = m_eff - above;
-        if (sfx < need && need <= sfx + c1) { S.res[0] = d1; S.res[1] = sfx; }
-        else if (sfx + c1 < need && need <= sfx + c1 + c0) { S.res[0] = d0; S.res[1] = sfx + c1; }
-        __syncthreads();
-        prefix |= (uint64_t)S.res[0] << shift;
-        above += S.res[1];
-        left = shift;
-        buf ^= 1;
-        __syncthreads();
+  uint32_t m_eff = 0;
+  if (m_req > 0) {                                        // uniform across the grid
+    // keys of the slice (4 slots per thread and iteration)
+    if (cached) {
+      const int n4 = nloc >> 2;
+      const int4 *g2h4 = reinterpret_cast<const int4 *>(L.gpu2host + g0);
+      const int4 *pr4 = reinterpret_cast<const int4 *>(L.priority + g0);
+      for (int j = tid; j < n4; j += MG_THREADS) {
+        const int4 hv = __ldcg(g2h4 + j), pv = __ldcg(pr4 + j);
+        keys[4 * j] = victim_key(hv.x, pv.x, step, hbits, hmax);
+        keys[4 * j + 1] = victim_key(hv.y, pv.y, step, hbits, hmax);
+        keys[4 * j + 2] = victim_key(hv.z, pv.z, step, hbits, hmax);
+        keys[4 * j + 3] = victim_key(hv.w, pv.w, step, hbits, hmax);
       }
-      kstar = prefix;
-      // evict every key >= kstar (exactly m_eff tokens).  Victims are ranked across
-      // the cluster (prefix of per-CTA counts; any order inside a CTA) and victim v
-      // is rebound at once to the token of rank n_scan + v, or freed if none is left.
+      for (int i = 4 * n4 + tid; i < nloc; i += MG_THREADS)
+        keys[i] = victim_key(ldcg(L.gpu2host + g0 + i), ldcg(L.priority + g0 + i), step, hbits, hmax);
+      __syncthreads();
+    }
+    // MSB-first radix select of the m_eff-th largest key (keys are unique) over the
+    // bitlen(step) + hbits + 1 bits a key can have.  The first digit's histogram
+    // also counts the evictable slots, which bounds m_eff.
+    uint64_t prefix = 0;
+    uint32_t above = 0;
+    int left = bitlen_u64((uint64_t)max(step, 0)) + hbits + 1, pass = 0;
+    const int nb_all = 1 << P.dbits;
+    while (left > 0) {
+      const int w = min(P.dbits, left), shift = left - w, nbins = 1 << w;
+      uint32_t *gh = P.hist + (pass % 3) * nb_all;
+      for (int i = tid; i < nbins; i += MG_THREADS) S.hist[i] = 0;
+      __syncthreads();
+      const uint64_t hi_mask = (shift + w >= 64) ? 0ull : (~0ull << (shift + w));
+      for (int base = 0; base < nloc; base += MG_THREADS) {   // uniform trip count per warp
+        const int i = base + tid;
+        const uint64_t kk = i < nloc ? key_at(i) : 0;
+        hist_add_warp(S.hist, kk != 0 && (kk & hi_mask) == (prefix & hi_mask),
+                      (uint32_t)((kk >> shift) & (uint64_t)(nbins - 1)));
+      }
+      __syncthreads();
+      for (int i = tid; i < nbins; i += MG_THREADS)
+        if (S.hist[i]) atomicAdd(gh + i, S.hist[i]);
+      if (!grid_sync(ctr)) return;
+      // the histogram of two passes ago was read by every CTA before this barrier:
+      // clear it for the pass after next
+      {
+        uint32_t *old = P.hist + ((pass + 2) % 3) * nb_all;
+        for (int64_t i = gtid; i < nb_all; i += gthreads) old[i] = 0;
+      }
+      // the digit, from the global counts of this thread's MG_BPT consecutive bins
+      uint32_t cb[MG_BPT], mine = 0;
+#pragma unroll
+      for (int j = 0; j < MG_BPT; ++j) {
+        const int d = MG_BPT * tid + j;
+        cb[j] = d < nbins ? (uint32_t)__ldcg(reinterpret_cast<const int32_t *>(gh + d)) : 0u;
+        mine += cb[j];
+      }
+      uint32_t tot;
+      const uint32_t incl = block_incl_scan(mine, S.warp_sums, &tot);
+      if (pass == 0) {                                   // tot = evictable slots
+        m_eff = min((uint32_t)m_req, tot);
+        if (blockIdx.x == 0 && tid == 0 && m_eff < (uint32_t)m_req) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
+        if (m_eff == 0) break;                           // uniform: every CTA read the same counts
+      }
+      uint32_t sfx = tot - incl;                         // keys in bins above mine
+      const uint32_t need = m_eff - above;
+#pragma unroll
+      for (int j = MG_BPT - 1; j >= 0; --j) {            // my bins, from the top
+        if (sfx < need && need <= sfx + cb[j]) { S.res[0] = MG_BPT * tid + j; S.res[1] = sfx; }
+        sfx += cb[j];
+      }
+      __syncthreads();
+      prefix |= (uint64_t)S.res[0] << shift;
+      above += S.res[1];
+      left = shift;
+      ++pass;
+      __syncthreads();
+    }
+    if (m_eff > 0) {
+      const uint64_t kstar = prefix;
+      // evict every key >= kstar (exactly m_eff tokens).  The CTA counts its victims,
+      // takes a block of ranks with one atomic, and victim v is rebound at once to
+      // the token of rank n_scan + v, or freed if none is left (evict mode).
       uint32_t nv = 0;
       for (int base = 0; base < nloc; base += MG_THREADS) {
         const int i = base + tid;
-        uint64_t kk = 0;
-        if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
+        const uint64_t kk = i < nloc ? key_at(i) : 0;
         nv += __popc(__ballot_sync(0xffffffffu, kk != 0 && kk >= kstar));
       }
-      if ((tid & 31) == 0) atomicAdd(&S.vcnt, nv);
+      if (lane == 0) S.wcnt[tid >> 5] = nv;              // per-warp victim counts
       __syncthreads();
-      cluster_sync();
-      uint32_t vbase = 0;
-      for (uint32_t r = 0; r < rank; ++r) vbase += *cluster.map_shared_rank(&S.vcnt, r);
+      if (tid == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < MG_WARPS; ++w) { const uint32_t x = S.wcnt[w]; S.wcnt[w] = t; t += x; }
+        S.base = t ? atomicAdd(reinterpret_cast<unsigned int *>(ctr + MG_VCUR), t) : 0u;
+      }
+      __syncthreads();
+      uint32_t rank = S.base + S.wcnt[tid >> 5];
       for (int base = 0; base < nloc; base += MG_THREADS) {
         const int i = base + tid;
-        uint64_t kk = 0;
-        if (i < nloc) kk = cached ? keys[i] : victim_key(L, g0 + i, step, hbits, hmax);
+        const uint64_t kk = i < nloc ? key_at(i) : 0;
         const bool isv = kk != 0 && kk >= kstar;
         const uint32_t bal = __ballot_sync(0xffffffffu, isv);
-        uint32_t wb = 0;
-        if ((tid & 31) == 0 && bal) wb = atomicAdd(&S.vcur, (uint32_t)__popc(bal));
-        wb = __shfl_sync(0xffffffffu, wb, 0);
         if (isv) {
           const int g = g0 + i;
-          L.host2gpu[L.gpu2host[g]] = -1;
-          const uint32_t r = (uint32_t)n_scan + vbase + wb + __popc(bal & lanemask_lt());
+          L.host2gpu[ldcg(L.gpu2host + g)] = -1;
+          const uint32_t r = (uint32_t)n_scan + rank + __popc(bal & lanemask_lt());
           if (r < (uint32_t)n_bind) {
             bind(g, r);
           } else {
@@ -351,54 +474,57 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
             L.free_map[g] = 1;
           }
         }
+        rank += __popc(bal);
       }
+      __syncthreads();
     }
   }
-  cluster_sync();                                      // evictions visible cluster-wide
 
-  // ---- allocation of already-free slots: warp-ballot scan of the free bitmap
-  // with one atomic count per warp (ranks [0, n_scan)) ----------------------
-  const uint32_t cursor_addr = map_dsmem(&S.cursor, 0);
+  // ---- slots that were already free: warp-ballot scan of this CTA's slice of the
+  // bitmap; the CTA takes a block of ranks with one atomic; ranks [0, n_scan) bind ----
   if (n_scan > 0) {
-    const int lane = tid & 31;
+    uint32_t nf = 0;
     for (int base = 0; base < nloc; base += MG_THREADS) {
-      // stop early once every token has a slot (one read per warp, uniform)
-      uint32_t cur = 0;
-      if (lane == 0) cur = ld_dsmem_u32(cursor_addr);
-      if (__shfl_sync(0xffffffffu, cur, 0) >= (uint32_t)n_scan) break;
       const int i = base + tid;
-      const bool fr = i < nloc && L.free_map[g0 + i] != 0;
+      nf += __popc(__ballot_sync(0xffffffffu, i < nloc && __ldcg(L.free_map + g0 + i) != 0));
+    }
+    if (lane == 0) S.wcnt[tid >> 5] = nf;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t t = 0;
+      for (int w = 0; w < MG_WARPS; ++w) { const uint32_t x = S.wcnt[w]; S.wcnt[w] = t; t += x; }
+      S.base = t ? atomicAdd(reinterpret_cast<unsigned int *>(ctr + MG_SCUR), t) : 0u;
+    }
+    __syncthreads();
+    uint32_t rank = S.base + S.wcnt[tid >> 5];
+    for (int base = 0; base < nloc && rank < (uint32_t)n_scan; base += MG_THREADS) {   // warp-uniform
+      const int i = base + tid;
+      const bool fr = i < nloc && __ldcg(L.free_map + g0 + i) != 0;
       const uint32_t bal = __ballot_sync(0xffffffffu, fr);
-      uint32_t wbase = 0;
-      if (lane == 0 && bal) {
-        uint32_t old;
-        asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(cursor_addr), "r"((uint32_t)__popc(bal)) : "memory");
-        wbase = old;
-      }
-      wbase = __shfl_sync(0xffffffffu, wbase, 0);
       if (fr) {
-        const uint32_t r = wbase + __popc(bal & lanemask_lt());
+        const uint32_t r = rank + __popc(bal & lanemask_lt());
         if (r < (uint32_t)n_scan) bind(g0 + i, r);
       }
+      rank += __popc(bal);
     }
   }
-  cluster_sync();                                      // bindings visible cluster-wide
+  if (!grid_sync(ctr)) return;                           // every binding visible
 
-  // ---- write-back data: host pool row, GPU slot row, indexer key ----------
+  // ---- data ---------------------------------------------------------------------
+  const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
+  const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
   if (P.mode == MODE_WRITEBACK) {
-    const int warps = MG_THREADS / 32, wid = tid >> 5, lane = tid & 31;
-    const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-    const int row_chunks = KV_W * esz / 16;
-    for (int b = rank * warps + wid; b < P.B; b += CL * warps) {
+    // host pool row, GPU slot row and indexer key of each new token; one warp per request
+    for (int64_t b = gwarp; b < P.B; b += gwarps) {
       const int32_t l = P.seq_len[b];
       const int64_t h = (int64_t)P.host_base[b] + l;
       if (h < 0 || h >= L.n_host) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); continue; }
       if (l >= P.Lmax) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); continue; }
-      const int32_t g = L.host2gpu[h];
-      const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + (int64_t)b * KV_W * esz);
+      const int32_t g = ldcg(L.host2gpu + h);
+      const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + b * KV_W * esz);
       uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
       uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz) : nullptr;
-      for (int c = lane; c < row_chunks; c += 32) {
+      for (int c = lane; c < chunks; c += 32) {
         const uint4 v = src[c];
         hdst[c] = v;
         if (gdst) gdst[c] = v;
@@ -406,19 +532,70 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
       if (g >= 0 && lane == 0) L.priority[g] = step;     // refresh an already resident token
       if (g < 0 && lane == 0) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
       const int kesz = P.ik_dtype == ECHO_F32 ? 4 : 1;
-      const char *ks = (const char *)P.new_ik + (int64_t)b * P.D * kesz;
-      char *kd = (char *)P.idx_k + ((int64_t)b * P.Lmax + l) * P.D * kesz;
+      const char *ks = (const char *)P.new_ik + b * P.D * kesz;
+      char *kd = (char *)P.idx_k + (b * P.Lmax + l) * P.D * kesz;
       for (int c = lane; c < P.D * kesz / 4; c += 32)
         reinterpret_cast<uint32_t *>(kd)[c] = reinterpret_cast<const uint32_t *>(ks)[c];
       __syncwarp();
       if (lane == 0) P.seq_len[b] = l + 1;
     }
+  } else if (P.mode == MODE_RECALL) {
+    // rows: rank r < nA from staging, else from the host pool (zero-copy reads).
+    // Lane j < 4 resolves row r0 + j (list entry, host index, slot) so the four
+    // lookups run in parallel; then the warp moves the four rows together.
+    const int n = nA + nB;
+    for (int64_t r0 = gwarp * 4; r0 < n; r0 += gwarps * 4) {
+      const uint4 *my_src = nullptr;
+      uint4 *my_dst = nullptr;
+      const int64_t r = r0 + lane;
+      if (lane < 4 && r < n) {
+        int b = 0;
+        const int64_t h = token_of((uint32_t)r, &b);
+        if (h >= 0 && h < L.n_host) {
+          const int32_t g = ldcg(L.host2gpu + h);
+          if (g >= 0) {                                     // not bound: pool exhausted
+            if (r < nA) {
+              const int ii = (int)r - S.pre_a[b];
+              my_src = reinterpret_cast<const uint4 *>((const char *)P.stage_kv +
+                                                       ((int64_t)b * P.cap_max + ii) * KV_W * esz);
+            } else {
+              my_src = reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * KV_W * esz);
+            }
+            my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz);
+          }
+        }
+      }
+      const uint4 *src[4];
+      uint4 *dst[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        src[j] = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), j));
+        dst[j] = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), j));
+      }
+      warp_copy_rows4(src, dst, chunks);
+    }
+    // slot translation for every selected entry (A10)
+    for (int64_t i = gtid; i < (int64_t)P.B * P.k; i += gthreads) {
+      const int32_t t = P.sel[i];
+      int32_t g = -1;
+      if (t >= 0) {
+        const int64_t h = (int64_t)P.host_base[i / P.k] + t;
+        if (h >= 0 && h < L.n_host) g = ldcg(L.host2gpu + h);
+        if (g < 0) g = -1;
+      }
+      P.slot_idx[i] = g;
+    }
   }
 
-  // ---- counters (CTA 0, after everything) ---------------------------------
-  cluster_sync();
-  if (rank == 0 && tid == 0) {
-    const uint32_t bound_scan = min(S.cursor, (uint32_t)n_scan);
+  // ---- counters and the manager's scratch words ---------------------------------
+  if (m_req > 0) {                                      // clear the global histograms
+    for (int64_t i = gtid; i < (int64_t)3 << P.dbits; i += gthreads) P.hist[i] = 0;
+  }
+  if (P.mode == MODE_RECALL && P.miss_cnt)               // and the miss counters
+    for (int64_t b = gtid; b < P.B; b += gthreads) P.miss_cnt[b] = 0;
+  if (blockIdx.x == 0 && tid == 0) {
+    const uint32_t scur = (uint32_t)ldcg(ctr + MG_SCUR);
+    const uint32_t bound_scan = min(scur, (uint32_t)n_scan);
     const uint32_t bound_victims = min(m_eff, (uint32_t)(n_bind - n_scan));
     const uint32_t bound = bound_scan + bound_victims;
     if (n_bind > 0 && bound < (uint32_t)n_bind) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
@@ -434,192 +611,12 @@ __global__ void __launch_bounds__(MG_THREADS, 1) manage_kernel(ManageParams P) {
       ctr[ECHO_CTR_EVICTED] = (int32_t)m_eff;
       ctr[ECHO_CTR_BOUND] = (int32_t)bound;
     }
-  }
-}
-
-// --------------------------------------------------------- miss detection --
-__global__ void miss_kernel(echo_cache_layer_t L, const int32_t *sel, const int32_t *host_base, int B, int k,
-                            int32_t *miss_list, int32_t *n_miss, int32_t *slot_idx) {
-  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const int32_t step = L.counters[ECHO_CTR_STEP];
-  uint32_t hit = 0, staged = 0, miss = 0;
-  if (i < (int64_t)B * k) {
-    const int b = (int)(i / k);
-    const int32_t t = sel[i];
-    int32_t out = -1;
-    if (t >= 0) {
-      const int64_t h = (int64_t)host_base[b] + t;
-      if (h >= L.n_host) {
-        set_status(L.counters, ECHO_ERR_HOST_INDEX);
-      } else {
-        const int32_t g = L.host2gpu[h];
-        if (g >= 0) {
-          L.priority[g] = step;                      // protect the selection
-          out = g;
-          hit = 1;
-        } else if (g <= -2) {
-          staged = 1;
-        } else {
-          const int32_t pos = atomicAdd(&n_miss[b], 1);
-          miss_list[(int64_t)b * k + pos] = t;
-          miss = 1;
-        }
-      }
-    }
-    slot_idx[i] = out;
-  }
-  hit = __reduce_add_sync(0xffffffffu, hit);
-  staged = __reduce_add_sync(0xffffffffu, staged);
-  miss = __reduce_add_sync(0xffffffffu, miss);
-  if ((threadIdx.x & 31) == 0) {
-    if (hit) atomicAdd(&L.counters[ECHO_CTR_HITS], (int)hit);
-    if (staged) atomicAdd(&L.counters[ECHO_CTR_STAGED_HITS], (int)staged);
-    if (miss) atomicAdd(&L.counters[ECHO_CTR_MISSES], (int)miss);
-  }
-}
-
-// --------------------------------------------------- copy + slot translate --
-constexpr int CT_THREADS = 256;
-constexpr int CT_ROWS = 4;           // rows in flight per warp
-
-__global__ void __launch_bounds__(CT_THREADS) copy_translate_kernel(
-    echo_cache_layer_t L, const int32_t *sel, const int32_t *host_base, int B, int k, const int32_t *pf_list,
-    const int32_t *pf_count, int cap_max, const void *stage_kv, const int32_t *miss_list, const int32_t *n_miss,
-    int32_t *slot_idx) {
-  __shared__ int32_t pre_a[MAXB + 1], pre_b[MAXB + 1];
-  block_prefix(B, [&](int b) { return pf_count ? min(max(pf_count[b], 0), cap_max) : 0; }, pre_a);
-  block_prefix(B, [&](int b) { return (int)n_miss[b]; }, pre_b);
-  const int nA = pre_a[B], n = nA + pre_b[B];
-  const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-  const int chunks = KV_W * esz / 16;                 // 72 (bf16) or 144 (f32)
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (blockIdx.x * (int64_t)CT_THREADS + threadIdx.x) >> 5;
-  const int64_t nw = (gridDim.x * (int64_t)CT_THREADS) >> 5;
-
-  // rows: r < nA from staging, else from the host pool.  Lane j < CT_ROWS resolves
-  // row r0 + j (list entry, host index, slot) so the 4 lookups run in parallel.
-  for (int64_t r0 = gw * CT_ROWS; r0 < n; r0 += nw * CT_ROWS) {
-    const uint4 *my_src = nullptr;
-    uint4 *my_dst = nullptr;
-    const int64_t r = r0 + lane;
-    if (lane < CT_ROWS && r < n) {
-      const bool staged = r < nA;
-      const int32_t *pre = staged ? pre_a : pre_b;
-      const int rr = staged ? (int)r : (int)(r - nA);
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= rr) lo = mid; else hi = mid - 1;
-      }
-      const int b = lo, ii = rr - pre[b];
-      const int32_t t = staged ? pf_list[(int64_t)b * cap_max + ii] : miss_list[(int64_t)b * k + ii];
-      const int64_t h = (int64_t)host_base[b] + t;
-      if (h >= 0 && h < L.n_host) {
-        const int32_t g = L.host2gpu[h];
-        if (g >= 0) {                                       // not bound: pool exhausted
-          my_src = staged ? reinterpret_cast<const uint4 *>((const char *)stage_kv +
-                                                            ((int64_t)b * cap_max + ii) * KV_W * esz)
-                          : reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * KV_W * esz);
-          my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz);
-        }
-      }
-    }
-    const uint4 *src[CT_ROWS];
-    uint4 *dst[CT_ROWS];
-#pragma unroll
-    for (int j = 0; j < CT_ROWS; ++j) {
-      src[j] = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), j));
-      dst[j] = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), j));
-    }
-    warp_copy_rows4(src, dst, chunks);
-  }
-
-  // slot translation for every selected entry (A10)
-  const int64_t tid = blockIdx.x * (int64_t)CT_THREADS + threadIdx.x;
-  const int64_t nt = gridDim.x * (int64_t)CT_THREADS;
-  for (int64_t i = tid; i < (int64_t)B * k; i += nt) {
-    const int32_t t = sel[i];
-    int32_t g = -1;
-    if (t >= 0) {
-      const int64_t h = (int64_t)host_base[i / k] + t;
-      if (h >= 0 && h < L.n_host) g = L.host2gpu[h];
-      if (g < 0) g = -1;
-    }
-    slot_idx[i] = g;
+    ctr[MG_VCUR] = 0;
+    ctr[MG_SCUR] = 0;
   }
 }
 
 // ------------------------------------------------------------- host side --
-static int g_cluster = 0;  // chosen cluster size for manage_kernel (16 if allowed, else 8)
-
-static size_t manage_smem(int CL, int n_gpu) {
-  const int per = ((n_gpu + CL - 1) / CL + 3) & ~3;
-  size_t s = (sizeof(MgShared) + 15) & ~size_t(15);
-  if (per <= KEYCAP) s += (size_t)per * 8;
-  return s;
-}
-
-template <int CL>
-static cudaError_t launch_manage(const ManageParams &P, cudaStream_t st) {
-  const size_t smem = manage_smem(CL, P.L.n_gpu);
-  cudaError_t e = cudaFuncSetAttribute(manage_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (CL > 8) {
-    e = cudaFuncSetAttribute(manage_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, 1, 1);
-  cfg.blockDim = dim3(MG_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, manage_kernel<CL>, P);
-}
-
-static int pick_cluster(int n_gpu) {
-  if (g_cluster) return g_cluster;
-  int cl = 8;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(16, 1, 1);
-  cfg.blockDim = dim3(MG_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = manage_smem(16, std::max(n_gpu, 1));
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 16;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaFuncSetAttribute(manage_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-      cudaFuncSetAttribute(manage_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)cfg.dynamicSmemBytes) == cudaSuccess) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, manage_kernel<16>, &cfg) == cudaSuccess && n > 0) cl = 16;
-  }
-  cudaGetLastError();
-  g_cluster = cl;
-  return cl;
-}
-
-static cudaError_t run_manage(const ManageParams &P, cudaStream_t st) {
-  const int cl = pick_cluster(P.L.n_gpu);
-  return cl == 16 ? launch_manage<16>(P, st) : launch_manage<8>(P, st);
-}
-
-static bool layer_ok(const echo_cache_layer_t *L) {
-  return L && L->n_gpu > 0 && L->n_host > 0 && L->host2gpu && L->gpu2host && L->priority && L->index_buf &&
-         L->free_map && L->counters && L->gpu_kv && L->host_kv &&
-         (L->kv_dtype == ECHO_F32 || L->kv_dtype == ECHO_BF16) &&
-         ((reinterpret_cast<uintptr_t>(L->gpu2host) | reinterpret_cast<uintptr_t>(L->priority)) & 15) == 0;
-}
-
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -629,6 +626,48 @@ int sm_count() {
     if (n <= 0) n = 1;
   }
   return n;
+}
+
+static int digit_bits(int n_gpu, int reserve) {   // 3 histograms of 2^bits words (+ reserve) in index_buf
+  int b = 1;
+  while (b < MG_MAXBITS && (3 << (b + 1)) + reserve <= n_gpu) ++b;
+  return b;
+}
+
+static cudaError_t run_manage(ManageParams P, cudaStream_t st) {
+  const int grid = sm_count();                  // one CTA per SM, all co-resident
+  const int per = ((P.L.n_gpu + grid - 1) / grid + 3) & ~3;
+  P.cached = (size_t)per * 8 <= MG_KEY_SMEM;
+  // the recall's miss counters follow the histograms when the pool leaves room for them
+  const int nmc = P.mode == MODE_RECALL ? P.B : 0;
+  P.dbits = digit_bits(P.L.n_gpu, nmc);
+  if ((3 << P.dbits) + nmc > P.L.n_gpu) P.dbits = digit_bits(P.L.n_gpu, 0);
+  const bool in_buf = (3 << P.dbits) <= P.L.n_gpu;
+  P.hist = in_buf ? reinterpret_cast<uint32_t *>(P.L.index_buf)
+                  : reinterpret_cast<uint32_t *>(P.L.counters + MG_SMALL_HIST);
+  P.miss_cnt = (nmc > 0 && (3 << P.dbits) + nmc <= P.L.n_gpu) ? P.L.index_buf + (3 << P.dbits) : nullptr;
+  const size_t smem = ((sizeof(MgShared) + 15) & ~size_t(15)) + (P.cached ? (size_t)per * 8 : 0);
+  cudaError_t e = cudaFuncSetAttribute(mgr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(MG_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mgr_kernel, P);
+}
+
+static bool layer_ok(const echo_cache_layer_t *L) {
+  return L && L->n_gpu > 0 && L->n_host > 0 && L->host2gpu && L->gpu2host && L->priority && L->index_buf &&
+         L->free_map && L->counters && L->gpu_kv && L->host_kv &&
+         (L->kv_dtype == ECHO_F32 || L->kv_dtype == ECHO_BF16) &&
+         ((reinterpret_cast<uintptr_t>(L->gpu2host) | reinterpret_cast<uintptr_t>(L->priority) |
+           reinterpret_cast<uintptr_t>(L->counters)) & 15) == 0;
 }
 
 }  // namespace echo
@@ -721,28 +760,21 @@ echo_status_t echo_cache_recall(const echo_cache_layer_t *layer, const int32_t *
   if (!layer_ok(layer) || !sel || !host_base || !miss_list || !n_miss || !slot_idx) return ECHO_ERR_INVALID_ARG;
   if (B <= 0 || B > MAXB || k <= 0) return ECHO_ERR_INVALID_ARG;
   if (pf_count && (!pf_list || !stage_kv || cap_max <= 0)) return ECHO_ERR_INVALID_ARG;
-  cudaStream_t st = (cudaStream_t)stream;
-  ECHO_CUDA_OK(cudaMemsetAsync(n_miss, 0, sizeof(int32_t) * B, st));
-  const int64_t nsel = (int64_t)B * k;
-  miss_kernel<<<(unsigned)((nsel + 255) / 256), 256, 0, st>>>(*layer, sel, host_base, B, k, miss_list, n_miss,
-                                                                slot_idx);
-  ECHO_LAUNCH_OK();
   ManageParams P = {};
   P.L = *layer;
   P.mode = MODE_RECALL;
   P.host_base = host_base;
   P.B = B;
+  P.sel = sel;
+  P.k = k;
   P.pf_list = pf_list;
   P.pf_count = pf_count;
   P.cap_max = pf_count ? cap_max : 0;
+  P.stage_kv = stage_kv;
   P.miss_list = miss_list;
   P.n_miss = n_miss;
-  P.k = k;
-  ECHO_CUDA_OK(run_manage(P, st));
-  const int grid = sm_count() * 4;
-  copy_translate_kernel<<<grid, CT_THREADS, 0, st>>>(*layer, sel, host_base, B, k, pf_list, pf_count,
-                                                     pf_count ? cap_max : 0, stage_kv, miss_list, n_miss, slot_idx);
-  ECHO_LAUNCH_OK();
+  P.slot_idx = slot_idx;
+  ECHO_CUDA_OK(run_manage(P, (cudaStream_t)stream));
   return ECHO_OK;
 }
 
