@@ -126,6 +126,7 @@ struct MgShared {
   int32_t pre_b[MAXB + 1];
   uint32_t warp_sums[32];
   uint32_t wcnt[MG_WARPS];             // per-warp counts (block reductions, victim ranks)
+  int64_t tok0[MAXB];                  // per request: host index of token 0 (write-back: of the new token)
   uint32_t res[2];                     // [0] chosen digit, [1] count above it
   uint32_t base;                       // this CTA's first rank from a global cursor
 };
@@ -277,6 +278,21 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
       for (int b = tid; b < P.B; b += MG_THREADS) P.n_miss[b] = ldcg(P.miss_cnt + b);
   }
 
+  // ---- this CTA's slice of slots; its first key vectors are loaded now, so the
+  // loads overlap the list prefixes below (used only if victims are needed) ----
+  const int per = ((L.n_gpu + (int)gridDim.x - 1) / (int)gridDim.x + 3) & ~3;   // 16-byte aligned starts
+  const int g0 = min(L.n_gpu, (int)blockIdx.x * per), g1 = min(L.n_gpu, g0 + per);
+  const int nloc = g1 - g0;
+  const bool cached = P.cached != 0;
+  const int n4 = nloc >> 2;
+  const int4 *g2h4 = reinterpret_cast<const int4 *>(L.gpu2host + g0);
+  const int4 *pr4 = reinterpret_cast<const int4 *>(L.priority + g0);
+  int4 hv0 = make_int4(-1, -1, -1, -1), pv0 = make_int4(0, 0, 0, 0);
+  if (cached && P.mode != MODE_ALLOC && tid < n4) {
+    hv0 = __ldcg(g2h4 + tid);
+    pv0 = __ldcg(pr4 + tid);
+  }
+
   // ---- the tokens that need a slot: list A (+ list B), same in every CTA ----
   // write-back: A = new tokens not yet resident; recall: A = staged rows,
   // B = misses; alloc: A = host_idx[0..n).
@@ -293,6 +309,9 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     block_prefix(P.B, [&](int b) { return pfc ? min(max(pfc[b], 0), cm) : 0; }, S.pre_a);
     block_prefix(P.B, [&](int b) { return (int)ldcg(mcnt + b); }, S.pre_b);
   }
+  if (P.mode == MODE_WRITEBACK || P.mode == MODE_RECALL)
+    for (int b = tid; b < P.B; b += MG_THREADS)
+      S.tok0[b] = (int64_t)P.host_base[b] + (P.mode == MODE_WRITEBACK ? P.seq_len[b] : 0);
   __syncthreads();
   int nA = 0, nB = 0;
   if (P.mode == MODE_WRITEBACK) nA = S.pre_a[P.B];
@@ -316,7 +335,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
       int b = 0;                                   // rank r -> request (B is small)
       while (b + 1 < P.B && S.pre_a[b + 1] <= (int)r) ++b;
       *req = b;
-      return (int64_t)P.host_base[b] + P.seq_len[b];
+      return S.tok0[b];
     } else if (P.mode == MODE_RECALL) {
       const int32_t *pre = (int)r < nA ? S.pre_a : S.pre_b;
       const int rr = (int)r < nA ? (int)r : (int)r - nA;
@@ -328,7 +347,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
       const int b = lo, ii = rr - pre[b];
       const int32_t t = (int)r < nA ? P.pf_list[(int64_t)b * P.cap_max + ii] : ldcg(P.miss_list + (int64_t)b * P.k + ii);
       *req = b;
-      return (int64_t)P.host_base[b] + t;
+      return S.tok0[b] + t;
     }
     *req = 0;
     return P.host_idx[r];
@@ -351,11 +370,6 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     }
   };
 
-  // ---- this CTA's slice of slots ----------------------------------------------
-  const int per = ((L.n_gpu + (int)gridDim.x - 1) / (int)gridDim.x + 3) & ~3;   // 16-byte aligned starts
-  const int g0 = min(L.n_gpu, (int)blockIdx.x * per), g1 = min(L.n_gpu, g0 + per);
-  const int nloc = g1 - g0;
-  const bool cached = P.cached != 0;
   const int hbits = bitlen_u64((uint64_t)max(L.n_host - 1, 1));
   const uint64_t hmax = (1ull << hbits) - 1;
   auto key_at = [&](int i) -> uint64_t {        // i: index within the slice
@@ -366,11 +380,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
   if (m_req > 0) {                                        // uniform across the grid
     // keys of the slice (4 slots per thread and iteration)
     if (cached) {
-      const int n4 = nloc >> 2;
-      const int4 *g2h4 = reinterpret_cast<const int4 *>(L.gpu2host + g0);
-      const int4 *pr4 = reinterpret_cast<const int4 *>(L.priority + g0);
       for (int j = tid; j < n4; j += MG_THREADS) {
-        const int4 hv = __ldcg(g2h4 + j), pv = __ldcg(pr4 + j);
+        const int4 hv = j == tid ? hv0 : __ldcg(g2h4 + j), pv = j == tid ? pv0 : __ldcg(pr4 + j);
         keys[4 * j] = victim_key(hv.x, pv.x, step, hbits, hmax);
         keys[4 * j + 1] = victim_key(hv.y, pv.y, step, hbits, hmax);
         keys[4 * j + 2] = victim_key(hv.z, pv.z, step, hbits, hmax);
@@ -465,7 +476,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
         const uint32_t bal = __ballot_sync(0xffffffffu, isv);
         if (isv) {
           const int g = g0 + i;
-          L.host2gpu[ldcg(L.gpu2host + g)] = -1;
+          const int64_t h_old = cached ? (int64_t)(hmax - ((kk - 1) & hmax)) : (int64_t)ldcg(L.gpu2host + g);
+          L.host2gpu[h_old] = -1;
           const uint32_t r = (uint32_t)n_scan + rank + __popc(bal & lanemask_lt());
           if (r < (uint32_t)n_bind) {
             bind(g, r);
