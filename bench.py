@@ -264,7 +264,7 @@ def run_echo(args, ws, rank, local):
         wl.layers = int(args.layers)
     layers = wl.layers
     # step inputs: pool fill + warm-up + timed + e2e + stage leg, within the workload's steps
-    base_steps = args.warmup + args.steps + args.steps + 2
+    base_steps = args.warmup + args.steps + args.steps + 1 + PROBE_STEPS
     fill_max = max(0, min(args.fill_max, wl.steps + 8 - base_steps - 1))
     if base_steps > wl.steps + 8:
         raise SystemExit(f"--steps/--warmup need {base_steps} decode steps; {wl.name} has {wl.steps}")
@@ -281,36 +281,44 @@ def run_echo(args, ws, rank, local):
 
     # timing events around the indexer, recorded inside the graph when supported
     ext_ok = True
-    ix_ev = []
+    ix_ev, st_ev = [], []
     try:
         ix_ev = [(torch.cuda.Event(enable_timing=True, external=True),
                   torch.cuda.Event(enable_timing=True, external=True)) for _ in range(layers)]
+        st_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)] for _ in range(layers)]
     except TypeError:
         ext_ok = False
 
     import ctypes
     lib = E.lib()
 
-    def layer_step(l, st):
+    def layer_step(l, st, stages=False):
         dl = L[l]
         if ext_ok:
-            # same sequence as echo_decode_layer_step, with events around the indexer
+            # the step's kernels issued through the separate entry points (the prefetch
+            # budget as its own launch), with events between the stages
             a = dl.args
             h = st.cuda_stream
+            mark = (lambda i: st_ev[l][i].record(st)) if stages else (lambda i: None)
+            mark(0)
             E.check(lib.echo_cache_writeback(dl.cache.ref, a.new_kv, a.new_ik, a.idx_k, a.D, a.Lmax, a.idx_dtype,
                                              a.host_base, a.seq_len, a.B, h))
+            mark(1)
             if a.prefetch:
                 E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap,
                                                a.pf_count, h))
-            ix_ev[l][0].record(st)
-            enqueue_index_topk(lib, dl, h, between=lambda: ix_ev[l][1].record(st))
+            mark(2)
+            enqueue_index_topk(lib, dl, h, between=lambda: mark(3))
+            mark(4)
             E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k,
                                           a.pf_list if a.prefetch else None, a.pf_count if a.prefetch else None,
                                           a.cap_max, a.stage_kv, a.miss_list, a.n_miss, a.slot_idx, h))
+            mark(5)
             E.check(lib.echo_sparse_mla_decode(a.q_mla, dl.cache.struct.gpu_kv, dl.cache.n_gpu,
                                                dl.cache.struct.kv_dtype, a.slot_idx, a.B, a.Hq, a.k,
                                                ctypes.c_float(a.scale), a.out, a.lse, a.mla_workspace,
                                                a.mla_workspace_bytes, h))
+            mark(6)
         else:
             dl.step(stream=st)
 
@@ -327,22 +335,27 @@ def run_echo(args, ws, rank, local):
     load_inputs(s_idx, stream)
     with torch.cuda.stream(stream):
         for l in range(layers):
-            layer_step(l, stream)
+            L[l].step(stream=stream)
     s_idx += 1
     stream.synchronize()
+    # the timed graph is the library's own step (echo_decode_layer_step) with its
+    # profiling hook recording events around each layer's indexer launch
+    if ext_ok:
+        for l in range(layers):
+            for j in range(2):
+                ix_ev[l][j].record(stream)                # creates the events
+                L[l].args.index_events[j] = ix_ev[l][j].cuda_event
+        stream.synchronize()
     graph = torch.cuda.CUDAGraph()
-    try:
-        with torch.cuda.graph(graph, stream=stream):
+    with torch.cuda.graph(graph, stream=stream):
+        for l in range(layers):
+            L[l].step(stream=stream)
+    probe = None                                         # the same step with events between stages
+    if ext_ok:
+        probe = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(probe, stream=stream):
             for l in range(layers):
-                layer_step(l, stream)
-    except Exception:
-        if not ext_ok:
-            raise
-        ext_ok = False                                   # events not capturable here: plain step
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for l in range(layers):
-                L[l].step(stream=stream)
+                layer_step(l, stream, stages=True)
     torch.cuda.synchronize()
 
     # steady state of the pool: untimed steps until every layer has fewer free slots
@@ -423,11 +436,22 @@ def run_echo(args, ws, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = tokens / (e2e_ms / 1e3)
 
-    # ---------------- per-stage timing leg (eager, same launch configuration) ----------------
+    # ---------------- per-stage times inside the graph (probe replays, untimed) ----------------
     stages = {}
-    if not args.skip_stages:
-        stages = stage_timing(L, inp, s_idx, stream, layers)
-        s_idx += 1
+    if not args.skip_stages and probe is not None:
+        names = ["writeback", "reserve", "index_prefetch", "topk", "recall", "mla"]
+        per = {n: [] for n in names}
+        for _ in range(PROBE_STEPS):
+            load_inputs(s_idx, stream)
+            with torch.cuda.stream(stream):
+                probe.replay()
+            s_idx += 1
+            stream.synchronize()
+            for i, n in enumerate(names):
+                per[n].append(sum(st_ev[l][i].elapsed_time(st_ev[l][i + 1]) for l in range(layers)) * 1e3 / layers)
+        stages = {n + "_us": round(statistics.median(v), 2) for n, v in per.items()}
+        stages["how"] = "CUDA events between the stages inside a graph of the step issued through the separate " \
+                        "entry points (reserve as its own launch), median of %d steps, mean over layers" % PROBE_STEPS
 
     # ---------------- roofline of the dominant kernel (indexer) ----------------
     peaks = measured_peaks()
@@ -480,6 +504,9 @@ def run_echo(args, ws, rank, local):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+PROBE_STEPS = 3
 
 
 def launches_per_step(prefetch: bool) -> int:

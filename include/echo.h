@@ -367,6 +367,9 @@ typedef struct {
   float *lse;               /* [B,Hq]                               */
   void *mla_workspace;
   size_t mla_workspace_bytes;
+  /* optional profiling hook: two cudaEvent_t recorded around the indexer launch
+   * (as external event nodes when the step is captured in a graph); NULL: none */
+  void *index_events[2];
 } echo_step_args_t;
 
 echo_status_t echo_decode_layer_step(const echo_cache_layer_t *layer, const echo_step_args_t *a,

@@ -111,6 +111,10 @@ struct ManageParams {
   int32_t *out_slot;
   // evict
   const int32_t *n_needed;
+  // write-back followed by the prefetch budget of the step (echo_cache_reserve's rule)
+  int32_t *rs_cap;
+  int32_t *rs_pf_count;
+  int rs_cap_max, rs_cap_div;
 };
 
 constexpr int MG_THREADS = 512;
@@ -530,8 +534,17 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     for (int64_t b = gwarp; b < P.B; b += gwarps) {
       const int32_t l = P.seq_len[b];
       const int64_t h = (int64_t)P.host_base[b] + l;
-      if (h < 0 || h >= L.n_host) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); continue; }
-      if (l >= P.Lmax) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); continue; }
+      const bool bad_h = h < 0 || h >= L.n_host, bad_l = l >= P.Lmax;
+      if (P.rs_cap && lane == 0) {                       // budget from the length after this write-back
+        const int32_t len = (bad_h || bad_l) ? l : l + 1;
+        int c = 0;
+        if (P.rs_cap_max > 0)
+          c = max(P.rs_cap_div > 0 ? min(P.rs_cap_max, (len + P.rs_cap_div - 1) / P.rs_cap_div) : P.rs_cap_max, 0);
+        P.rs_cap[b] = c;
+        P.rs_pf_count[b] = 0;
+      }
+      if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); continue; }
+      if (bad_l) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); continue; }
       const int32_t g = ldcg(L.host2gpu + h);
       const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + b * KV_W * esz);
       uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
@@ -711,7 +724,22 @@ echo_status_t echo_cache_reset(const echo_cache_layer_t *layer, echo_stream_t st
 echo_status_t echo_cache_writeback(const echo_cache_layer_t *layer, const void *new_kv, const void *new_ik,
                                    void *idx_k, int32_t D, int32_t Lmax, int32_t ik_dtype,
                                    const int32_t *host_base, int32_t *seq_len, int32_t B, echo_stream_t stream) {
+  return echo::cache_writeback_reserve(layer, new_kv, new_ik, idx_k, D, Lmax, ik_dtype, host_base, seq_len, B, 0, 0,
+                                       nullptr, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace echo {
+
+// echo_cache_writeback, optionally followed in the same launch by echo_cache_reserve
+// (cap != NULL); used by the step executor.
+echo_status_t cache_writeback_reserve(const echo_cache_layer_t *layer, const void *new_kv, const void *new_ik,
+                                      void *idx_k, int32_t D, int32_t Lmax, int32_t ik_dtype,
+                                      const int32_t *host_base, int32_t *seq_len, int32_t B, int32_t cap_max,
+                                      int32_t cap_div, int32_t *cap, int32_t *pf_count, echo_stream_t stream) {
   if (!layer_ok(layer) || !new_kv || !new_ik || !idx_k || !host_base || !seq_len) return ECHO_ERR_INVALID_ARG;
+  if (cap && (!pf_count || cap_max < 0 || cap_div < 0)) return ECHO_ERR_INVALID_ARG;
   if (B <= 0 || B > MAXB || D <= 0 || Lmax <= 0 || (ik_dtype != ECHO_E4M3 && ik_dtype != ECHO_F32))
     return ECHO_ERR_INVALID_ARG;
   if ((D * (ik_dtype == ECHO_F32 ? 4 : 1)) % 4 != 0 || layer->n_gpu < B) return ECHO_ERR_UNSUPPORTED;
@@ -727,9 +755,17 @@ echo_status_t echo_cache_writeback(const echo_cache_layer_t *layer, const void *
   P.host_base = host_base;
   P.seq_len = seq_len;
   P.B = B;
+  P.rs_cap = cap;
+  P.rs_pf_count = pf_count;
+  P.rs_cap_max = cap_max;
+  P.rs_cap_div = cap_div;
   ECHO_CUDA_OK(run_manage(P, (cudaStream_t)stream));
   return ECHO_OK;
 }
+
+}  // namespace echo
+
+extern "C" {
 
 echo_status_t echo_cache_reserve(const echo_cache_layer_t *layer, const int32_t *seq_len, int32_t B,
                                  int32_t cap_max, int32_t cap_div, int32_t *cap, int32_t *pf_count,

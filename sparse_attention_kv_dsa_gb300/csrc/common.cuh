@@ -241,6 +241,10 @@ __device__ __forceinline__ void atom_add_dsmem_u32(uint32_t addr, uint32_t v) {
 // ------------------------------------------------------------ host utils --
 int sm_count();
 cudaError_t check_launch();
+echo_status_t cache_writeback_reserve(const echo_cache_layer_t *layer, const void *new_kv, const void *new_ik,
+                                      void *idx_k, int32_t D, int32_t Lmax, int32_t ik_dtype,
+                                      const int32_t *host_base, int32_t *seq_len, int32_t B, int32_t cap_max,
+                                      int32_t cap_div, int32_t *cap, int32_t *pf_count, echo_stream_t stream);
 
 }  // namespace echo
 

@@ -9,9 +9,11 @@
 //
 // One thread-block cluster (8 CTAs x 512 threads, two CTAs per SM) per request.  Each CTA holds the
 // order-preserving uint32 keys of a contiguous slice of the request's scores in
-// shared memory.  An MSB-first radix select (11 + 11 + 10 bit digits) finds the
-// k-th largest key K*; each CTA histograms its slice and reads the other CTAs'
-// histograms through distributed shared memory, so every CTA derives the same
+// shared memory.  A first pass histograms a window of keys around the key of the EMA
+// threshold (the predicted k-th score); when the k-th key falls inside, one more
+// 11-bit pass finds the k-th largest key K*, otherwise an MSB-first radix select
+// (11 + 11 + 10 bit digits) does.  Each CTA histograms its slice and reads the other
+// CTAs' histograms through distributed shared memory, so every CTA derives the same
 // digit with no broadcast step.  Output: every key > K*, then the tokens equal to
 // K* with the lowest indices (ranks ordered across warps and CTAs), so ties go to
 // the lower token index.  The selection order is ascending t within each class.
@@ -39,7 +41,7 @@ struct TkShared {
   uint32_t hist[2][TK_BINS];
   uint32_t warp_sums[32];
   uint32_t res[4];
-  uint32_t cta_cnt[2];                  // [0] keys > K*, [1] keys == K* in this CTA
+  uint32_t cta_cnt[2];                  // [0] keys > K* (window pass: above the window), [1] keys == K*
   uint32_t warp_gt[TK_WARPS], warp_eq[TK_WARPS];
   uint32_t minkey;
 };
@@ -139,9 +141,69 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   }
   __syncthreads();
 
-  // ---- radix select of the k-th largest key -----------------------------
+  // ---- window pass around the predicted k-th key ----------------------------
+  // The EMA threshold theta[b] predicts this step's k-th score.  One pass counts the
+  // keys above a window of 2^22 key values around it and histograms the window's
+  // keys in 2048 bins of 2048 values.  When the k-th key falls in the window, one
+  // more 11-bit pass finishes the select; otherwise the full radix select runs.
+  // Either way the result is the exact k-th key.
   uint32_t prefix = 0, above = 0;
   int left = 32, buf = 0;
+  const float th_pred = theta[b];
+  if (isfinite(th_pred)) {                                // uniform across the cluster
+    const uint32_t kt = f32_key(th_pred);
+    const uint32_t wlo = (kt > (1u << 21) ? kt - (1u << 21) : 0u) & ~((1u << 11) - 1u);
+    const uint64_t whi = (uint64_t)wlo + (1ull << 22);
+    uint32_t *h = S.hist[0];
+    for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
+    __syncthreads();
+    uint32_t nab = 0;
+    for (int base = 0; base < n; base += TK_THREADS) {     // uniform trip count per warp
+      const int i = base + tid;
+      uint32_t kk = 0;
+      if (i < n) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+      nab += __popc(__ballot_sync(0xffffffffu, i < n && (uint64_t)kk >= whi));
+      if (i < n && kk >= wlo && (uint64_t)kk < whi) atomicAdd(&h[(kk - wlo) >> 11], 1u);
+    }
+    if (lane == 0) S.warp_gt[warp] = nab;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t t = 0;
+      for (int w = 0; w < TK_WARPS; ++w) t += S.warp_gt[w];
+      S.cta_cnt[0] = t;
+    }
+    __syncthreads();
+    cluster_sync();
+    uint32_t tab = 0;                                      // keys above the window
+    uint32_t c[TK_BPT];
+#pragma unroll
+    for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) {                 // plain loads, issued together
+      tab += *cluster.map_shared_rank(&S.cta_cnt[0], r);
+      const uint4 v = *reinterpret_cast<const uint4 *>(cluster.map_shared_rank(h + TK_BPT * tid, r));
+      c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+    }
+    uint32_t tot;
+    const uint32_t incl = tk_block_scan(c[0] + c[1] + c[2] + c[3], S.warp_sums, &tot);
+    if (tab < (uint32_t)k && (uint32_t)k <= tab + tot) {   // the k-th key is in the window
+      uint32_t sfx = tot - incl;
+      const uint32_t need = (uint32_t)k - tab;
+#pragma unroll
+      for (int j = TK_BPT - 1; j >= 0; --j) {
+        if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
+        sfx += c[j];
+      }
+      __syncthreads();
+      prefix = wlo + (S.res[0] << 11);
+      above = tab + S.res[1];
+      left = 11;
+    }
+    buf = 1;                        // other CTAs may still read hist[0]
+    __syncthreads();
+  }
+
+  // ---- radix select of the k-th largest key -----------------------------
   while (left > 0) {
     const int w = min(11, left), shift = left - w;
     uint32_t *h = S.hist[buf];
@@ -152,7 +214,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       const int i = base + tid;
       uint32_t kk = 0;
       if (i < n) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
-      hist_add_warp(h, i < n && (kk & hi_mask) == (prefix & hi_mask), (kk >> shift) & ((1u << w) - 1));
+      if (i < n && (kk & hi_mask) == (prefix & hi_mask)) atomicAdd(&h[(kk >> shift) & ((1u << w) - 1)], 1u);
     }
     __syncthreads();
     cluster_sync();

@@ -55,7 +55,7 @@ class StepArgsT(ctypes.Structure):
                 ("miss_list", ctypes.c_void_p), ("n_miss", ctypes.c_void_p), ("slot_idx", ctypes.c_void_p),
                 ("Hq", ctypes.c_int32), ("q_mla", ctypes.c_void_p), ("scale", ctypes.c_float),
                 ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("mla_workspace", ctypes.c_void_p),
-                ("mla_workspace_bytes", ctypes.c_size_t)]
+                ("mla_workspace_bytes", ctypes.c_size_t), ("index_events", ctypes.c_void_p * 2)]
 
 
 # Declared signatures: name -> (restype, argtypes).  P = pointer, I = int32.
