@@ -55,6 +55,16 @@ Readings taken where the pages are silent (each is listed again in the design doc):
   R11 the GPU cache starts empty; the host pool holds every context token.
   R15 host index of token t of request b is host_base[b] + t.
   R16 the write-back begins a step: s <- s + 1.
+  R18 prefill: query j of a block that starts at position pos0 scores the tokens
+      t <= pos0 + j (causal; its own key included).
+  R19 prefill bucket of a token: d = score - kth_pred in float32 (one rounding);
+      bucket = top 8 bits of the order-preserving 32-bit key of d (non-negative:
+      sign bit set; negative: every bit inverted; -0 counts as +0).
+  R20 prefill threshold bucket = the bucket holding the query's k-th largest d
+      (histogram counted down from bucket 255); candidates = tokens in buckets
+      strictly above it, so every candidate is in the exact top-k.  A query with
+      at most k tokens has every token as a candidate.
+  R21 the block's recall list is the union of its queries' tokens, ascending.
 """
 
 from __future__ import annotations
@@ -443,3 +453,91 @@ def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, 
             o, l = sparse_mla_decode(q_mla[b], latent_of(hosts), scale)
             out[b], lse[b] = o, l
     return StepResult(new_h, scores, caps, staged, sels, kth, theta_new, rec, out, lse)
+
+
+# --------------------------------------------------------------------------
+# prefill chunk indexing -- [REV] "Prefill: overlap recall across query blocks"
+# (a 256-bucket coarse histogram picks the strictly-high buckets now and leaves
+# the threshold bucket for later; subtracting the predicted k-th score makes the
+# buckets near the boundary finer); the exact top-k and recall follow.
+# --------------------------------------------------------------------------
+def prefill_scores(q_blk: np.ndarray, w_blk: np.ndarray, keys: np.ndarray, pos0: int) -> list:
+    """Scores of every query of a block over its causal range (R18).
+
+    q_blk [Q, H, D], w_blk [Q, H], keys [>= pos0 + Q, D]  ->  list of Q float64
+    arrays, query j of length pos0 + j + 1."""
+    return [indexer_scores(q_blk[j], w_blk[j], keys[:pos0 + j + 1]) for j in range(q_blk.shape[0])]
+
+
+def order_key_f32(x) -> np.ndarray:
+    """Order-preserving uint32 key of float32 values, from the IEEE-754 bit
+    pattern: larger float -> larger key; -0 and +0 share the key of +0."""
+    x = np.asarray(x, dtype=np.float32).copy()
+    x[x == 0] = 0.0                                  # -0 -> +0
+    u = x.view(np.uint32).astype(np.uint64)
+    neg = (u >> 31) == 1
+    key = np.where(neg, (~u) & 0xFFFFFFFF, u | 0x80000000)
+    return key.astype(np.uint64)
+
+
+def prefill_buckets(scores_f32: np.ndarray, kth_pred: float) -> np.ndarray:
+    """Bucket 0..255 of each score (R19): top byte of the key of score - kth_pred,
+    the difference taken in float32."""
+    d = np.asarray(scores_f32, dtype=np.float32) - np.float32(kth_pred)   # float32 op
+    return (order_key_f32(d) >> 24).astype(np.int64)
+
+
+def prefill_histogram(scores_f32: np.ndarray, kth_pred: float) -> np.ndarray:
+    """The 256-bucket histogram of one query's scores."""
+    return np.bincount(prefill_buckets(scores_f32, kth_pred), minlength=256).astype(np.int64)
+
+
+def prefill_candidates(scores_f32: np.ndarray, kth_pred: float, k: int):
+    """Threshold bucket and candidate tokens of one query (R20).
+
+    Returns (thr, cand): thr = bucket of the k-th largest d (-1 when the query has
+    at most k tokens); cand = ascending token indices with bucket > thr."""
+    s = np.asarray(scores_f32, dtype=np.float32)
+    L = s.shape[0]
+    bk = prefill_buckets(s, kth_pred)
+    if L <= k:
+        return -1, np.arange(L, dtype=np.int64)
+    hist = np.bincount(bk, minlength=256)
+    above = 0
+    thr = 0
+    for bkt in range(255, -1, -1):                   # count down from the top bucket
+        if above + hist[bkt] >= k:
+            thr = bkt
+            break
+        above += hist[bkt]
+    return thr, np.nonzero(bk > thr)[0].astype(np.int64)
+
+
+def token_union(lists) -> np.ndarray:
+    """Union of token index lists, ascending (R21)."""
+    lists = [np.asarray(x, dtype=np.int64) for x in lists]
+    if not lists:
+        return np.zeros(0, dtype=np.int64)
+    return np.unique(np.concatenate(lists))
+
+
+def prefill_block(q_blk, w_blk, keys, pos0: int, kth_pred, k: int):
+    """One query block: scores, histograms, candidates and their union, then the
+    exact per-query top-k and the union of the selections.
+
+    Returns a dict with 'scores' (float32 per query), 'hist' [Q, 256], 'thr' [Q],
+    'cand' (per query), 'cand_union', 'sel' (per query, selection order), 'kth' [Q]
+    and 'sel_union'."""
+    Q = q_blk.shape[0]
+    scores = [to_f32_exact(s) for s in prefill_scores(q_blk, w_blk, keys, pos0)]
+    hist = np.stack([prefill_histogram(scores[j], kth_pred[j]) for j in range(Q)])
+    thr, cand, sel, kth = [], [], [], np.zeros(Q, dtype=np.float32)
+    for j in range(Q):
+        t_j, c_j = prefill_candidates(scores[j], kth_pred[j], k)
+        thr.append(t_j)
+        cand.append(c_j)
+        s_j, kv = topk_select(scores[j], k)
+        sel.append(s_j)
+        kth[j] = np.float32(kv)
+    return {"scores": scores, "hist": hist, "thr": np.array(thr), "cand": cand,
+            "cand_union": token_union(cand), "sel": sel, "kth": kth, "sel_union": token_union(sel)}

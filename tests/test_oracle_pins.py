@@ -385,3 +385,93 @@ def test_decode_step_small_properties():
             assert np.array_equal(o, r.out[b])
         theta = r.theta
         qi = S.qidx_next(wl, 0, s, qi)
+
+
+# ------------------------------------------------------------------ prefill --
+def test_order_key_sorts_like_the_floats():
+    # order-preserving key: sorting by key sorts the values; -0 and +0 share a key
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(500) * 10.0 ** rng.integers(-30, 30, 500),
+                        [0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45]]).astype(np.float32)
+    key = O.order_key_f32(x)
+    xs = np.sort(x.astype(np.float64))
+    ks = np.sort(key)
+    assert np.array_equal(O.order_key_f32(xs.astype(np.float32)), ks)
+    for i in range(len(x)):                              # pairwise order on a sample
+        for j in range(0, len(x), 37):
+            assert (x[i] < x[j]) == (key[i] < key[j]) or x[i] == x[j]
+    assert O.order_key_f32(np.float32(-0.0)) == O.order_key_f32(np.float32(0.0)) == 0x80000000
+
+
+def test_prefill_bucket_hand_values():
+    # bucket = top byte of the key of d = score - kth_pred (IEEE-754 worked by hand):
+    #   d = 1.0  -> bits 0x3F800000 -> key 0xBF800000 -> 191;  d = 0.5 -> 0xBF000000 -> 191
+    #   d = 2.0  -> 0x40000000 -> key 0xC0000000 -> 192;       d = 0 -> 0x80000000 -> 128
+    #   d = -1.0 -> bits 0xBF800000 -> key ~bits = 0x407FFFFF -> 64
+    #   d = 1e-38 (subnormal-adjacent) -> key 0x806CE3EE -> 128
+    kth = 10.0
+    scores = np.array([11.0, 10.5, 12.0, 10.0, 9.0, 10.0 + 1e-6], dtype=np.float32)
+    got = O.prefill_buckets(scores, kth)
+    d = scores - np.float32(kth)
+    assert got.tolist()[:5] == [191, 191, 192, 128, 64]
+    # 1e-6 above 10 is not representable exactly: the float32 difference decides
+    assert got[5] == (O.order_key_f32(d[5:6])[0] >> 24)
+    assert O.prefill_buckets(np.array([1e-38], np.float32), 0.0)[0] == 128
+
+
+def test_prefill_candidates_brute_force():
+    # threshold bucket holds the k-th largest d; candidates are exactly the tokens in
+    # strictly higher buckets; they all rank above the k-th, so they are in the top-k
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        L = int(rng.integers(1, 90))
+        k = int(rng.integers(1, 40))
+        s = (rng.integers(-40, 41, L) * 0.125).astype(np.float32)
+        kth_pred = float(rng.integers(-20, 21) * 0.25)
+        thr, cand = O.prefill_candidates(s, kth_pred, k)
+        d = s - np.float32(kth_pred)
+        bk = [(int(O.order_key_f32(d[t:t + 1])[0]) >> 24) for t in range(L)]   # per element
+        if L <= k:
+            assert thr == -1 and cand.tolist() == list(range(L))
+            continue
+        kth_d = sorted(d.tolist(), reverse=True)[k - 1]
+        assert thr == int(O.order_key_f32(np.float32(kth_d))) >> 24
+        assert cand.tolist() == [t for t in range(L) if bk[t] > thr]
+        top, _ = O.topk_select(s, k)
+        assert set(cand.tolist()) <= set(top.tolist())
+        assert len(cand) <= k - 1
+
+
+def test_prefill_scores_causal_brute_force():
+    # explicit loops over heads and dims for one token of each query
+    rng = np.random.default_rng(3)
+    Q, H, D, pos0 = 3, 4, 8, 5
+    q = rng.integers(-8, 9, (Q, H, D)) * 0.125
+    w = rng.integers(1, 17, (Q, H)) / 16.0
+    keys = rng.integers(-8, 9, (pos0 + Q, D)) * 0.125
+    sc = O.prefill_scores(q, w, keys, pos0)
+    assert [len(x) for x in sc] == [pos0 + 1, pos0 + 2, pos0 + 3]
+    for j in range(Q):
+        for t in (0, pos0 + j):
+            tot = 0.0
+            for h in range(H):
+                dot = 0.0
+                for c in range(D):
+                    dot += q[j, h, c] * keys[t, c]
+                tot += w[j, h] * max(dot, 0.0)
+            assert sc[j][t] == tot
+
+
+def test_token_union_and_block_properties():
+    assert O.token_union([[5, 1, 3], [3, 9], []]).tolist() == [1, 3, 5, 9]
+    rng = np.random.default_rng(5)
+    Q, H, D, pos0, k = 4, 4, 8, 40, 6
+    q = rng.integers(-8, 9, (Q, H, D)) * 0.125
+    w = rng.integers(1, 17, (Q, H)) / 16.0
+    keys = rng.integers(-8, 9, (pos0 + Q, D)) * 0.125
+    kth_pred = np.full(Q, 1.5, dtype=np.float32)
+    r = O.prefill_block(q, w, keys, pos0, kth_pred, k)
+    assert set(r["cand_union"].tolist()) <= set(r["sel_union"].tolist())
+    for j in range(Q):
+        assert r["hist"][j].sum() == pos0 + j + 1
+        assert r["kth"][j] == np.float32(np.sort(r["scores"][j])[::-1][k - 1])
