@@ -700,6 +700,71 @@ def run_compare_prefetch(args, local) -> int:
     return 0
 
 
+def run_prefill(args, local) -> int:
+    """Prefill chunk indexing of one request (a 2048-token chunk at positions 100K...):
+    the time until every block's exact selection is resident, for the serial
+    pipeline, the overlapped one, and the overlapped one with the histogram
+    candidates recalled early; plus the scoring kernel against the FP8 tensor roof
+    (FP8 peak = 2 x the measured bf16 GEMM peak, the nominal dense ratio)."""
+    import torch
+    import sparse_attention_kv_dsa_gb300.echo as E
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    from sparse_attention_kv_dsa_gb300.runtime import PrefillChunk
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = S.workloads()[args.workload]
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    out = {"mode": "prefill", "workload": wl.name, "ctx": wl.ctx[0], "chunk": wl.prefill_chunk, "topk": wl.topk,
+           "reps": args.steps, "blocks": {}}
+    for block in wl.prefill_blocks:
+        pc = PrefillChunk(wl, block, dev)
+        res = {}
+        for mode in ("serial", "overlap", "echo"):
+            ts = []
+            for rep in range(args.warmup + args.steps):
+                pc.reset()
+                torch.cuda.synchronize()
+                t0, t1 = pc.run(mode)
+                torch.cuda.synchronize()
+                if rep >= args.warmup:
+                    ts.append(t0.elapsed_time(t1) * 1e3)
+            assert int(pc.status.item()) == 0 and pc.cache.status() == 0
+            res[mode + "_us"] = round(statistics.median(ts), 1)
+        # candidate recall vs exact recall of the last block (echo mode state)
+        res["last_block_candidates"] = int(pc.cand[(pc.nblocks - 1) % 2].sum().item())
+        res["last_block_misses_after_candidates"] = int(pc.nmiss[(pc.nblocks - 1) % 2].item())
+        res["last_block_candidate_recall_misses"] = int(pc.nmiss_c[(pc.nblocks - 1) % 2].item())
+        res["speedup_echo_vs_serial"] = round(res["serial_us"] / res["echo_us"], 3)
+        res["speedup_echo_vs_overlap"] = round(res["overlap_us"] / res["echo_us"], 3)
+        # the scoring kernel alone: middle block, CUDA events after a device-side delay
+        i = pc.nblocks // 2
+        pos0 = pc.ctx + i * block
+        kp = torch.full((block,), 40.0, device=dev)
+        ks = []
+        for rep in range(5):
+            torch.cuda._sleep(400000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            E.prefill_index(pc.q_all[i * block:(i + 1) * block], pc.w_all[i * block:(i + 1) * block], pc.idx_k,
+                            pos0, kp, pc.scores[0], pc.hist[0], pc.status)
+            e1.record()
+            torch.cuda.synchronize()
+            ks.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(ks)
+        flops = 2.0 * 64 * 128 * sum(pos0 + j + 1 for j in range(block))
+        res["prefill_index_us"] = round(us, 1)
+        res["prefill_index_roofline"] = {"bound": "tensor", "achieved": flops / (us * 1e-6) / 1e12,
+                                         "peak": fp8_peak, "unit": "TFLOP/s",
+                                         "frac": flops / (us * 1e-6) / 1e12 / fp8_peak,
+                                         "peak_source": peaks["source"] + " bf16 GEMM x 2 (FP8 nominal ratio)"}
+        out["blocks"][str(block)] = res
+        del pc
+        torch.cuda.empty_cache()
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_cap_sweep(args, local) -> int:
     """Low-locality workload: miss-list size and recall time against the prefetch cap."""
     import torch
@@ -748,6 +813,9 @@ def main(argv=None):
     ap.add_argument("--cap-sweep", action="store_true",
                     help="prefetch-cap sweep (default workload: lowlocality-b16-ctx100k)")
     ap.add_argument("--skip-host-link", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="prefill chunk indexing: serial / overlapped / candidate-prefetch pipelines "
+                         "(default workload: prefill-chunk2048-ctx100k)")
     ap.add_argument("--fill-max", type=int, default=96,
                     help="untimed steps, at most, that bring the GPU pool to its steady (full) state")
     args = ap.parse_args(argv)
@@ -759,6 +827,9 @@ def main(argv=None):
     if args.cap_sweep:
         args.workload = args.workload or "lowlocality-b16-ctx100k"
         return run_cap_sweep(args, local)
+    if args.prefill:
+        args.workload = args.workload or "prefill-chunk2048-ctx100k"
+        return run_prefill(args, local)
     args.workload = args.workload or DEFAULT_WL
     if args.impl == "reference":
         return run_reference(args, ws, rank)

@@ -382,6 +382,55 @@ echo_status_t echo_cache_status(const echo_cache_layer_t *layer, int32_t *host_s
 /* Synchronising copy of the whole counters block to host_counters[ECHO_NUM_COUNTERS]. */
 echo_status_t echo_cache_read_counters(const echo_cache_layer_t *layer, int32_t *host_counters);
 
+/*
+ * P1 -- prefill chunk indexing ([REV] "Prefill: overlap recall across query blocks":
+ * the chunk is scored in query blocks; a 256-bucket coarse histogram picks the
+ * buckets certainly above the selection boundary and leaves the threshold bucket
+ * for later, after the predicted k-th score is subtracted; the KV of block i's
+ * candidates moves while block i+1 is scored; exact top-k and recall follow).
+ *
+ * echo_prefill_index: scores of one query block of one request.  Query j sits at
+ * position pos0 + j and scores the tokens t <= pos0 + j (causal, its own key
+ * included): scores[j, t] = sum_h w[j,h] * ReLU(q[j,h,:] . idx_k[t,:]).  Also the
+ * per-query histogram hist[j, b] = #{t : bucket(scores[j,t] - kth_pred[j]) == b},
+ * bucket(d) = top 8 bits of the order-preserving 32-bit key of d (non-negative d:
+ * sign bit set; negative d: every bit inverted; -0 counts as +0), d in float32.
+ *   q [Q,64,128] e4m3 (16-byte aligned), w [Q,64] f32, idx_k [Lmax,128] e4m3 (this
+ *   request's indexer keys, 16-byte aligned), pos0 + Q <= Lmax, kth_pred [Q] f32;
+ *   scores [Q,Lmax] f32 out (entries past each query's causal range untouched);
+ *   hist [Q,256] u32 out (zeroed by the call); status: optional device int32 that
+ *   receives ECHO_ERR_TIMEOUT if a bounded wait gave up.
+ *   H must be 64 and D 128 (ECHO_ERR_UNSUPPORTED otherwise).
+ */
+echo_status_t echo_prefill_index(const void *q, const float *w, const void *idx_k, int32_t Q, int32_t H,
+                                 int32_t D, int32_t Lmax, int32_t pos0, const float *kth_pred,
+                                 float *scores, uint32_t *hist, int32_t *status, echo_stream_t stream);
+
+/*
+ * P1 -- candidates of a scored block.  For query j with L_j = pos0 + j + 1 tokens:
+ * thr[j] = the bucket holding the k-th largest d (counted from bucket 255 down), or
+ * -1 when L_j <= k; candidates = tokens whose bucket is strictly above thr[j] (each
+ * is in the exact top-k).  Candidate tokens are OR-ed into bitmap (bit t of word
+ * t/32; the union over the block's queries); cand_count[j] = their number.
+ *   scores/hist as produced by echo_prefill_index; thr, cand_count [Q] (may be
+ *   NULL); bitmap [ceil(Lmax/32)] u32, in/out.
+ */
+echo_status_t echo_prefill_candidates(const float *scores, const uint32_t *hist, int32_t Q, int32_t Lmax,
+                                      int32_t pos0, int32_t k, const float *kth_pred, int32_t *thr,
+                                      int32_t *cand_count, uint32_t *bitmap, echo_stream_t stream);
+
+/* P1 -- OR the tokens of rows x row_len token lists (entries < 0 or >= nbits are
+ * skipped) into bitmap [ceil(nbits/32)]: the union of a block's exact selections. */
+echo_status_t echo_mark_tokens(const int32_t *tok, int32_t rows, int32_t row_len, uint32_t *bitmap,
+                               int32_t nbits, echo_stream_t stream);
+
+/* P1 -- bitmap -> list: list[0..count) = the set tokens in ascending order, the rest
+ * of list[0..cap) = -1; *count (device int32) = number of set tokens (only the first
+ * cap are written).  The bitmap is left all-zero.  The list is the selection row of
+ * a one-request echo_cache_recall (the block's union, recalled once). */
+echo_status_t echo_token_list(uint32_t *bitmap, int32_t nbits, int32_t *list, int32_t cap, int32_t *count,
+                              echo_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -241,6 +241,8 @@ __device__ __forceinline__ void atom_add_dsmem_u32(uint32_t addr, uint32_t v) {
 // ------------------------------------------------------------ host utils --
 int sm_count();
 cudaError_t check_launch();
+// 2-D byte tensor [rows, 128] with a [box_rows, 128] box and 128-byte swizzle (TMA).
+bool make_map_128B(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows);
 echo_status_t cache_writeback_reserve(const echo_cache_layer_t *layer, const void *new_kv, const void *new_ik,
                                       void *idx_k, int32_t D, int32_t Lmax, int32_t ik_dtype,
                                       const int32_t *host_base, int32_t *seq_len, int32_t B, int32_t cap_max,

@@ -479,7 +479,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D byte tensor [rows, 128] with a [box_rows, 128] box and 128-byte swizzle.
-static bool make_map_128B(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows) {
+bool make_map_128B(CUtensorMap *m, const void *base, uint64_t rows, uint32_t box_rows) {
   auto enc = get_encode();
   if (!enc) return false;
   const cuuint64_t dims[2] = {128, rows};

@@ -77,6 +77,10 @@ SIGNATURES = {
     "echo_sparse_mla_decode": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "echo_sparse_mla_decode_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P]),
     "echo_decode_layer_step": (_I, [_P, _P, _P]),
+    "echo_prefill_index": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "echo_prefill_candidates": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "echo_mark_tokens": (_I, [_P, _I, _I, _P, _I, _P]),
+    "echo_token_list": (_I, [_P, _I, _P, _I, _P, _P]),
     "echo_cache_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "echo_cache_read_counters": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
 }
@@ -266,3 +270,27 @@ def sparse_mla_decode_noalloc(q, kv, slot_idx, scale: float, out, lse, stream=No
     check(lib().echo_sparse_mla_decode_noalloc(ptr(q), ptr(kv), kv.shape[0], dtype_code(q.dtype), ptr(slot_idx), B,
                                                Hq, k, scale, ptr(out), ptr(lse), stream_handle(stream)),
           "sparse_mla_decode_noalloc")
+
+
+# ------------------------------------------------------------------- prefill --
+def prefill_index(q, w, idx_k, pos0: int, kth_pred, scores, hist, status=None, stream=None):
+    """q [Q,64,128] e4m3, w [Q,64] f32, idx_k [Lmax,128] e4m3 -> scores [Q,Lmax], hist [Q,256]."""
+    Q, H, D = q.shape
+    check(lib().echo_prefill_index(ptr(q), ptr(w), ptr(idx_k), Q, H, D, idx_k.shape[0], pos0, ptr(kth_pred),
+                                   ptr(scores), ptr(hist), ptr(status), stream_handle(stream)), "prefill_index")
+
+
+def prefill_candidates(scores, hist, pos0: int, k: int, kth_pred, bitmap, thr=None, cand_count=None, stream=None):
+    Q, Lmax = scores.shape
+    check(lib().echo_prefill_candidates(ptr(scores), ptr(hist), Q, Lmax, pos0, k, ptr(kth_pred), ptr(thr),
+                                        ptr(cand_count), ptr(bitmap), stream_handle(stream)), "prefill_candidates")
+
+
+def mark_tokens(tok, bitmap, nbits: int, stream=None):
+    rows, row_len = tok.shape
+    check(lib().echo_mark_tokens(ptr(tok), rows, row_len, ptr(bitmap), nbits, stream_handle(stream)), "mark_tokens")
+
+
+def token_list(bitmap, nbits: int, out_list, count, stream=None):
+    check(lib().echo_token_list(ptr(bitmap), nbits, ptr(out_list), out_list.numel(), ptr(count),
+                                stream_handle(stream)), "token_list")

@@ -187,3 +187,115 @@ class StepInputs:
         cast = (lambda x: S.grid_to_float(x)) if wl.kv_fp32 else (lambda x: S.grid_to_fp8(x))
         self.q_ik = [[cast(x) for x in ql] for ql in self.q_int]
         self.new_ik_ik = [[cast(x) for x in il] for il in self.new_ik]
+
+
+class PrefillChunk:
+    """One request's prefill chunk through the library's prefill entry points.
+
+    The chunk's queries are scored in blocks of `block` queries.  A block is ready
+    when every token selected by its exact per-query top-k is resident.  Modes:
+      "serial"  one stream: score block i, top-k, recall the union, then block i+1;
+      "overlap" scoring and top-k on s1; block i's recall on s2 overlaps block i+1;
+      "echo"    as "overlap", and block i's histogram candidates are recalled on s2
+                as soon as it is scored, before its top-k finishes; the exact recall
+                afterwards only fetches what the candidates missed.
+    The exact k-th scores of block i are block i+1's predictions (query j for query
+    j); the first block predicts +inf, i.e. it has no candidates."""
+
+    def __init__(self, wl: S.Workload, block: int, device="cuda", layer: int = 0, gen_device=None):
+        dev = torch.device(device)
+        self.wl, self.block, self.device = wl, int(block), dev
+        gd = gen_device or (dev if dev.type == "cuda" else "cpu")
+        self.ctx, self.chunk = int(wl.ctx[0]), int(wl.prefill_chunk)
+        assert self.chunk % self.block == 0
+        self.nblocks = self.chunk // self.block
+        self.k = wl.topk
+        self.Lmax = self.ctx + self.chunk
+        L = self.Lmax
+        self.cache = E.LayerCache(wl.n_gpu, wl.n_host, torch.bfloat16, dev)
+        self.cache.reset()
+        # host pool rows of this request (context and chunk), keys, chunk queries
+        for r0 in range(0, L, 1 << 20):
+            r1 = min(L, r0 + (1 << 20))
+            self.cache.host_kv[r0:r1].copy_(S.latents_for(wl, layer, r1 - r0, r0, gd).cpu())
+        self.idx_k = S.grid_to_fp8(S.keys_for(wl, layer, 0, L, gd).to(dev)).contiguous()
+        self.q_all = S.grid_to_fp8(S.prefill_queries(wl, layer, L, "cpu")[self.ctx:].to(dev)).contiguous()
+        self.w_all = S.prefill_weights(wl, layer, L, "cpu")[self.ctx:].to(dev).contiguous()
+        Q, nw = self.block, (L + 31) // 32
+        i32 = torch.int32
+        self.scores = [torch.empty(Q, L, device=dev) for _ in range(2)]
+        self.hist = [torch.empty(Q, 256, dtype=i32, device=dev) for _ in range(2)]
+        self.kth = [torch.empty(Q, device=dev) for _ in range(2)]
+        self.theta = [torch.empty(Q, device=dev) for _ in range(2)]
+        self.sel = [torch.empty(Q, self.k, dtype=i32, device=dev) for _ in range(2)]
+        self.thr = [torch.empty(Q, dtype=i32, device=dev) for _ in range(2)]
+        self.cand = [torch.empty(Q, dtype=i32, device=dev) for _ in range(2)]
+        self.bitmap = [torch.zeros(nw, dtype=i32, device=dev) for _ in range(2)]
+        self.lst = [torch.empty(1, L, dtype=i32, device=dev) for _ in range(2)]
+        self.count = [torch.empty(1, dtype=i32, device=dev) for _ in range(2)]
+        self.miss = [torch.empty(1, L, dtype=i32, device=dev) for _ in range(2)]
+        self.nmiss = [torch.zeros(1, dtype=i32, device=dev) for _ in range(2)]
+        self.nmiss_c = [torch.zeros(1, dtype=i32, device=dev) for _ in range(2)]
+        self.slot = [torch.empty(1, L, dtype=i32, device=dev) for _ in range(2)]
+        self.seq = [torch.arange(self.ctx + i * Q + 1, self.ctx + (i + 1) * Q + 1, dtype=i32, device=dev)
+                    for i in range(self.nblocks)]
+        self.kpred = [torch.empty(Q, device=dev) for _ in range(2)]   # the block's predictions
+        self.hb = torch.zeros(1, dtype=i32, device=dev)
+        self.status = torch.zeros(1, dtype=i32, device=dev)
+        self.s1 = torch.cuda.Stream(dev)
+        self.s2 = torch.cuda.Stream(dev)
+
+    def reset(self):
+        self.cache.reset()
+        for b in self.bitmap:
+            b.zero_()
+
+    def run(self, mode: str = "echo"):
+        """Enqueue the whole chunk; returns (start, end) events on s1."""
+        assert mode in ("serial", "overlap", "echo")
+        Q, k, L = self.block, self.k, self.Lmax
+        s1 = self.s1
+        s2 = self.s1 if mode == "serial" else self.s2
+        ev_topk = [torch.cuda.Event() for _ in range(self.nblocks)]
+        ev_done = [torch.cuda.Event() for _ in range(self.nblocks)]
+        ev_scored = [torch.cuda.Event() for _ in range(self.nblocks)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(s1)
+        s2.wait_stream(s1)
+        for i in range(self.nblocks):
+            p = i % 2
+            pos0 = self.ctx + i * Q
+            kp = self.kpred[p]
+            with torch.cuda.stream(s1):
+                if i >= 2:
+                    s1.wait_event(ev_done[i - 2])                # buffers of parity p are free
+                if i == 0:
+                    kp.fill_(float("inf"))
+                else:
+                    kp.copy_(self.kth[(i - 1) % 2])
+                E.prefill_index(self.q_all[i * Q:(i + 1) * Q], self.w_all[i * Q:(i + 1) * Q], self.idx_k, pos0,
+                                kp, self.scores[p], self.hist[p], self.status, s1)
+                ev_scored[i].record(s1)
+            if mode == "echo":
+                with torch.cuda.stream(s2):                      # candidates move while s1 goes on
+                    s2.wait_event(ev_scored[i])
+                    E.prefill_candidates(self.scores[p], self.hist[p], pos0, k, kp, self.bitmap[p], self.thr[p],
+                                         self.cand[p], s2)
+                    E.token_list(self.bitmap[p], L, self.lst[p], self.count[p], s2)
+                    E.cache_recall(self.cache, self.lst[p], self.hb, self.miss[p], self.nmiss_c[p], self.slot[p],
+                                   stream=s2)
+            with torch.cuda.stream(s1):
+                self.theta[p].copy_(kp)
+                E.topk(self.scores[p], self.seq[i], k, self.sel[p], self.kth[p], self.theta[p], 0.5, s1)
+                ev_topk[i].record(s1)
+            with torch.cuda.stream(s2):
+                s2.wait_event(ev_topk[i])
+                E.mark_tokens(self.sel[p], self.bitmap[p], L, s2)
+                E.token_list(self.bitmap[p], L, self.lst[p], self.count[p], s2)
+                E.cache_recall(self.cache, self.lst[p], self.hb, self.miss[p], self.nmiss[p], self.slot[p],
+                               stream=s2)
+                ev_done[i].record(s2)
+        s1.wait_stream(s2)
+        end.record(s1)
+        return start, end

@@ -125,7 +125,7 @@ def workloads() -> dict:
     out["prefill-chunk2048-ctx100k"] = Workload(
         name="prefill-chunk2048-ctx100k", cfg_id=5, layers=1, batch=1, ctx=[100_000], h_idx=64,
         d_idx=128, grid=8, w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=200_000,
-        n_host=2_000_000, steps=0, rho=1.0, cap_max=0, cap_div=32, prefill_chunk=2048,
+        n_host=2_000_000, steps=0, rho=0.9, cap_max=0, cap_div=32, prefill_chunk=2048,
         prefill_blocks=[256, 512])
     return out
 
@@ -182,7 +182,7 @@ def grid_to_fp8(x_int: torch.Tensor) -> torch.Tensor:
 
 
 # ---------------------------------------------------- per-purpose streams ----
-P_KEYS, P_QIDX, P_W, P_DRIFT, P_LAT, P_QMLA, P_NEWKV, P_NEWIK = range(1, 9)
+P_KEYS, P_QIDX, P_W, P_DRIFT, P_LAT, P_QMLA, P_NEWKV, P_NEWIK, P_PFQ, P_PFW = range(1, 11)
 
 
 def keys_for(wl: Workload, layer: int, b: int, L: int, device="cpu") -> torch.Tensor:
@@ -218,3 +218,19 @@ def new_kv_for(wl: Workload, layer: int, step: int, device="cpu") -> torch.Tenso
 
 def new_ik_for(wl: Workload, layer: int, step: int, device="cpu") -> torch.Tensor:
     return grid_ints(mix_seed(wl.seed, P_NEWIK, layer, step), (wl.batch, wl.d_idx), wl.grid, device)
+
+
+def prefill_queries(wl: Workload, layer: int, n: int, device="cpu") -> torch.Tensor:
+    """Indexer queries of n consecutive prefill positions [n, H, D] (grid integers):
+    an AR(1) chain with correlation wl.rho from one position to the next."""
+    q = grid_ints(mix_seed(wl.seed, P_PFQ, layer), (wl.h_idx, wl.d_idx), wl.grid, "cpu")
+    out = torch.empty((n, wl.h_idx, wl.d_idx), dtype=torch.int8)
+    for j in range(n):
+        out[j] = q
+        q = grid_drift(mix_seed(wl.seed, P_PFQ, layer, j + 1), q, wl.grid, wl.rho)
+    return out.to(device)
+
+
+def prefill_weights(wl: Workload, layer: int, n: int, device="cpu") -> torch.Tensor:
+    """Indexer head weights of n prefill positions [n, H]."""
+    return choice(mix_seed(wl.seed, P_PFW, layer), (n, wl.h_idx), wl.w_values, device)
