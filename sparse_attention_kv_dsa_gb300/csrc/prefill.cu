@@ -16,7 +16,8 @@
 //                         forms sum_h w_h ReLU(.) per (token, query), stores the causal
 //                         scores and histograms bucket(score - kth_pred) per query.
 //                         Persistent CTAs walk (query quad, range of key tiles) items.
-//                         Warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue.
+//                         Warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue (two
+//                         warps per TMEM lane quadrant, two queries each).
 //   prefill_cand_kernel   one CTA per query: threshold bucket from the histogram,
 //                         then a pass over the query's scores marking the tokens of
 //                         higher buckets in a token bitmap (one OR per warp and word).
@@ -38,7 +39,8 @@ constexpr int PF_N = PF_QG * PF_H;               // 256
 constexpr int PF_STAGES = 4;                     // key tiles in flight
 constexpr int PF_ACC = 2;                        // TMEM accumulators of 256 columns
 constexpr int PF_RANGE = 64;                     // key tiles per work item
-constexpr int PF_THREADS = 192;                  // producer, MMA, 4 epilogue warps
+constexpr int PF_EPI = 256;                       // epilogue threads: two warps per TMEM lane quadrant
+constexpr int PF_THREADS = 64 + PF_EPI;           // producer, MMA, 8 epilogue warps
 constexpr int PF_KTILE_BYTES = PF_TILE * PF_D;   // 16 KB
 constexpr int PF_Q_BYTES = PF_N * PF_D;          // 32 KB
 constexpr int PF_BUCKETS = 256;
@@ -67,8 +69,8 @@ constexpr size_t PF_SMEM = 1024 + PF_STAGES * PF_KTILE_BYTES + 2 * PF_Q_BYTES + 
 __device__ __forceinline__ void pf_status(int32_t *st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
 }
-// Named barrier of the 128 epilogue threads (barrier 1; barrier 0 is __syncthreads).
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the epilogue threads (barrier 1; barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(PF_EPI) : "memory"); }
 
 // Tiles [ja, jb) of work item i: query quad g, key-tile range r; tiles past the
 // quad's last causal position are skipped.
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     for (int s = 0; s < PF_ACC; ++s) {
       mbar_init(&S.tfull[s], 1);
-      mbar_init(&S.tempty[s], 128);
+      mbar_init(&S.tempty[s], PF_EPI);
     }
     fence_mbar_init();
   }
@@ -187,13 +189,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     // ---------------------------------------------------------- epilogue --
     const int quad = warp & 3;                         // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;                  // token within the tile
-    const int et = threadIdx.x - 64;                   // 0..127
+    const int et = threadIdx.x - 64;                   // 0..PF_EPI-1
+    const int qh = (warp - 2) >> 2;                    // which two of the quad's four queries
     int it = 0, cur = -1;
     bool ok = true;
     // adds the quad's histograms into the global ones and clears them
     auto flush = [&](int g) {
       epi_sync();
-      for (int i = et; i < PF_QG * PF_BUCKETS; i += 128) {
+      for (int i = et; i < PF_QG * PF_BUCKETS; i += PF_EPI) {
         const uint32_t v = S.hist_s[i];
         const int q = PF_QG * g + i / PF_BUCKETS;
         if (v && q < P.Q) atomicAdd(&P.hist[(int64_t)q * PF_BUCKETS + (i % PF_BUCKETS)], v);
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (w.ja >= w.jb) continue;
       if (w.g != cur) {
         if (cur >= 0) flush(cur);
-        for (int x = et; x < PF_QG * PF_H; x += 128) {
+        for (int x = et; x < PF_QG * PF_H; x += PF_EPI) {
           const int q = PF_QG * w.g + x / PF_H;
           S.w_s[x] = q < P.Q ? P.w[(int64_t)q * PF_H + (x % PF_H)] : 0.f;
         }
@@ -225,9 +228,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + acc * PF_N;
         const int t = j * PF_TILE + row;
-        float sc[PF_QG];
+        float sc[2];
 #pragma unroll
-        for (int qi = 0; qi < PF_QG; ++qi) {
+        for (int qq = 0; qq < 2; ++qq) {
+          const int qi = 2 * qh + qq;
           uint32_t r0[32], r1[32];
           tmem_ld32(taddr + qi * PF_H, r0);
           tmem_ld32(taddr + qi * PF_H + 32, r1);
@@ -242,16 +246,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             a2 = fmaf(wq[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), a2);
             a3 = fmaf(wq[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), a3);
           }
-          sc[qi] = (a0 + a1) + (a2 + a3);
+          sc[qq] = (a0 + a1) + (a2 + a3);
         }
         tc_fence_before();
         mbar_arrive(&S.tempty[acc]);
 #pragma unroll
-        for (int qi = 0; qi < PF_QG; ++qi) {
+        for (int qq = 0; qq < 2; ++qq) {
+          const int qi = 2 * qh + qq;
           const int q = PF_QG * w.g + qi;
           if (q < P.Q && t <= P.pos0 + q && t < P.Lmax) {      // causal range of query q
-            P.scores[(int64_t)q * P.Lmax + t] = sc[qi];
-            const uint32_t bkt = pf_key(__fsub_rn(sc[qi], S.kth_s[qi])) >> 24;
+            P.scores[(int64_t)q * P.Lmax + t] = sc[qq];
+            const uint32_t bkt = pf_key(__fsub_rn(sc[qq], S.kth_s[qi])) >> 24;
             atomicAdd(&S.hist_s[qi * PF_BUCKETS + bkt], 1u);
           }
         }
