@@ -168,7 +168,7 @@ static int mla_splits(int k) { return (k + MS_SPLIT - 1) / MS_SPLIT; }
 // MMAs from one thread.  256 TMEM columns and ~100 KB shared memory per CTA: two
 // CTAs per SM overlap each other's phases.
 constexpr int TC_T = 256;                 // selected entries per CTA
-constexpr int TC_THREADS = 160;
+constexpr int TC_THREADS = 288;         // warps 0-3 loads/softmax/epilogue, 4 MMA, 5-8 softmax
 constexpr int TC_QCH = 128 * 128;         // Q chunk bytes (128 heads x 64 dims)
 constexpr int TC_KCH = TC_T * 128;        // C chunk bytes (256 rows x 64 dims)
 constexpr int TC_STAGE = TC_QCH + TC_KCH; // 48 KB
@@ -187,6 +187,7 @@ struct TcShared {
   uint32_t tmem_base;
   int32_t slots[TC_T];
   uint32_t vmask[TC_T / 32];
+  float mpart[2][128], lpart[2][128];      // per head: max and sum of each half of the columns
 };
 constexpr size_t TC_SMEM = 1024 + TC_REGION + sizeof(TcShared);
 
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       mbar_init(&S.vempty[i], 1);
     }
     mbar_init(&S.s_full, 1);
-    mbar_init(&S.p_full, 128);
+    mbar_init(&S.p_full, 256);
     mbar_init(&S.o_full, 1);
     mbar_init(&S.o_empty, 128);
     fence_mbar_init();
@@ -246,6 +247,70 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   bool ok = true;
+
+  // Softmax of one half of the 256 columns (half 0: warps 0-3, half 1: warps 5-8) for
+  // head row (warp & 3) * 32 + lane: row max and sum exchanged between the halves
+  // through shared memory (named barriers 1 and 2 of the 256 softmax threads); writes
+  // bf16 P for its columns and arrives on p_full.  Returns the row's max and sum.
+  auto softmax_half = [&](int half, float &m_out, float &l_out) {
+    const int hr = (warp & 3) * 32 + lane;
+    const uint32_t tr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t *vmask = S.vmask;             // validity of the 256 entries (set before the first barrier)
+    const int cb = half * (TC_T / 2), ce = cb + TC_T / 2;
+    float m = -INFINITY;
+    for (int c0 = cb; c0 < ce; c0 += 64) {       // two TMEM loads per wait
+      uint32_t r[32], r2[32];
+      tmem_ld32(tr + c0, r);
+      tmem_ld32(tr + c0 + 32, r2);
+      tmem_wait_ld();
+      const uint32_t vm = vmask[c0 >> 5], vm2 = vmask[(c0 >> 5) + 1];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]));
+        if ((vm2 >> j) & 1u) m = fmaxf(m, __uint_as_float(r2[j]));
+      }
+    }
+    S.mpart[half][hr] = m;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    m = fmaxf(S.mpart[0][hr], S.mpart[1][hr]);
+    const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
+    const float mc = m * c2;
+    float l = 0.f;
+    // 32 probabilities -> bf16 -> four 16-byte chunks of P (half an atom column)
+    auto write_p = [&](int c0, const uint32_t (&r)[32], uint32_t vm) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float p0 = ((vm >> j) & 1u) ? exp2f(fmaf(__uint_as_float(r[j]), c2, -mc)) : 0.f;
+        const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[j + 1]), c2, -mc)) : 0.f;
+        l += p0 + p1;
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+        pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+      }
+      unsigned char *pa = P + (c0 >> 6) * (128 * 128);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ch = ((c0 & 63) >> 3) + q;
+        *reinterpret_cast<uint4 *>(pa + sw128(hr, ch)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                                    pk[4 * q + 3]);
+      }
+    };
+    for (int c0 = cb; c0 < ce; c0 += 64) {       // two TMEM loads per wait
+      uint32_t r[32], r2[32];
+      tmem_ld32(tr + c0, r);
+      tmem_ld32(tr + c0 + 32, r2);
+      tmem_wait_ld();
+      write_p(c0, r, vmask[c0 >> 5]);
+      write_p(c0 + 32, r2, vmask[(c0 >> 5) + 1]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(&S.p_full);
+    S.lpart[half][hr] = l;
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    m_out = m;
+    l_out = S.lpart[0][hr] + S.lpart[1][hr];
+  };
 
   if (warp < 4) {
     // ------------------------------------------------ phase 1 loads --
@@ -297,56 +362,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       cp_async_commit();
     };
     for (int vc = 0; vc < TC_VST; ++vc) load_v(vc);
-    // validity of the 256 entries as a bit mask (written before the first barrier)
-    const uint32_t *vmask = S.vmask;
     const int h = tid;                                  // head row = TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float m = -INFINITY;
-    for (int c0 = 0; c0 < TC_T; c0 += 64) {                // two TMEM loads per wait
-      uint32_t r[32], r2[32];
-      tmem_ld32(trow + c0, r);
-      tmem_ld32(trow + c0 + 32, r2);
-      tmem_wait_ld();
-      const uint32_t vm = vmask[c0 >> 5], vm2 = vmask[(c0 >> 5) + 1];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]));
-        if ((vm2 >> j) & 1u) m = fmaxf(m, __uint_as_float(r2[j]));
-      }
-    }
-    const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
-    const float mc = m * c2;
-    float l = 0.f;
-    // 32 probabilities -> bf16 -> four 16-byte chunks of P (half an atom column)
-    auto write_p = [&](int c0, const uint32_t (&r)[32], uint32_t vm) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = ((vm >> j) & 1u) ? exp2f(fmaf(__uint_as_float(r[j]), c2, -mc)) : 0.f;
-        const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[j + 1]), c2, -mc)) : 0.f;
-        l += p0 + p1;
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-        pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
-      }
-      unsigned char *pa = P + (c0 >> 6) * (128 * 128);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int ch = ((c0 & 63) >> 3) + q;
-        *reinterpret_cast<uint4 *>(pa + sw128(h, ch)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                                                                   pk[4 * q + 3]);
-      }
-    };
-    for (int c0 = 0; c0 < TC_T; c0 += 64) {                // two TMEM loads per wait
-      uint32_t r[32], r2[32];
-      tmem_ld32(trow + c0, r);
-      tmem_ld32(trow + c0 + 32, r2);
-      tmem_wait_ld();
-      write_p(c0, r, vmask[c0 >> 5]);
-      write_p(c0 + 32, r2, vmask[(c0 >> 5) + 1]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(&S.p_full);
+    float m = 0.f, l = 0.f;
+    softmax_half(0, m, l);
 
     // ------------------------------------------- phase 2 loads + epilogue --
     for (int vc = 0; vc < TC_NV; ++vc) {
@@ -396,6 +415,12 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     }
     part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
     part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1] = l;
+  } else if (warp > 4) {
+    // ------------------------------------------- second half of the softmax --
+    if (!mbar_wait(&S.s_full, 0)) ok = false;
+    tc_fence_after();
+    float m = 0.f, l = 0.f;
+    softmax_half(1, m, l);
   } else if (lane == 0) {
     // ------------------------------------------------------------- MMA --
     constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, TC_T);
@@ -441,27 +466,50 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 
 // Merge the bf16 partials of one (request, head) in split order.  A block of 256
 // threads covers 4 heads; each thread produces 8 consecutive output dims.
+template <int NSMAX>
 __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out,
                                                              float *lse) {
   const int b = blockIdx.y;
   const int h = blockIdx.x * 4 + (threadIdx.x >> 6);
   const int d0 = (threadIdx.x & 63) * 8;
   const float *ml = part.ml + ((int64_t)b * nsplit * 128 + h) * 2;   // split s at ml[s * 256]
+  const __nv_bfloat16 *po = part.o + ((int64_t)b * nsplit * 128 + h) * 512 + d0;   // split s at po[s * 65536]
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * 256));
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float Lsum = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float m = __ldg(ml + (int64_t)s * 256), l = __ldg(ml + (int64_t)s * 256 + 1);
+  auto add = [&](float m, float l, const uint4 &v) {
     const float w = (m == -INFINITY || l <= 0.f) ? 0.f : expf(m - M) * l;
     Lsum += w;
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(part.o + (((int64_t)b * nsplit + s) * 128 + h) * 512 + d0));
     const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       acc[2 * j] = fmaf(w, __bfloat162float(p2[j].x), acc[2 * j]);
       acc[2 * j + 1] = fmaf(w, __bfloat162float(p2[j].y), acc[2 * j + 1]);
     }
+  };
+  if (nsplit <= NSMAX) {
+    // every split's (m, l) and partial issued together, then merged in split order
+    float m[NSMAX], l[NSMAX];
+    uint4 v[NSMAX];
+#pragma unroll
+    for (int s = 0; s < NSMAX; ++s) {
+      if (s < nsplit) {
+        m[s] = __ldg(ml + (int64_t)s * 256);
+        l[s] = __ldg(ml + (int64_t)s * 256 + 1);
+        v[s] = __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 128 * 512));
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < NSMAX; ++s)
+      if (s < nsplit) M = fmaxf(M, m[s]);
+#pragma unroll
+    for (int s = 0; s < NSMAX; ++s)
+      if (s < nsplit) add(m[s], l[s], v[s]);
+  } else {
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * 256));
+    for (int s = 0; s < nsplit; ++s)
+      add(__ldg(ml + (int64_t)s * 256), __ldg(ml + (int64_t)s * 256 + 1),
+          __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 128 * 512)));
   }
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   uint4 o;
@@ -539,7 +587,7 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
     mla_tc_kernel<<<dim3(ns, B), TC_THREADS, TC_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
                                                             scale, tp);
     ECHO_LAUNCH_OK();
-    mla_tc_combine_kernel<<<dim3(32, B), 256, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
+    mla_tc_combine_kernel<8><<<dim3(32, B), 256, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
   } else {
     return ECHO_ERR_UNSUPPORTED;
   }
