@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         if (!mbar_wait(&S.o_full, hf & 1)) ok = false;
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *dst = part.o + ((((int64_t)b * nsplit + s) * 128 + h) * 512 + hf * 256);
+        // partials are stored in groups of 8 dims, heads innermost: [b][s][dim/8][head][8], so
+        // the 32 heads of a warp write one contiguous 512-byte run per store
+        __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + hf * 32) * 128 * 8 + (int64_t)h * 8;
         auto store_o = [&](int c0, const uint32_t (&r)[32]) {
           uint32_t pk[16];
 #pragma unroll
@@ -398,8 +400,9 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
             pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<uint4 *>(dst + c0)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)                      // dims c0 + 8q .. c0 + 8q + 7 of this half
+            *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         };
         for (int c0 = 0; c0 < 256; c0 += 64) {             // two TMEM loads per wait
           uint32_t r[32], r2[32];
@@ -469,11 +472,13 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 template <int NSMAX>
 __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out,
                                                              float *lse) {
-  const int b = blockIdx.y;
-  const int h = blockIdx.x * 4 + (threadIdx.x >> 6);
-  const int d0 = (threadIdx.x & 63) * 8;
-  const float *ml = part.ml + ((int64_t)b * nsplit * 128 + h) * 2;   // split s at ml[s * 256]
-  const __nv_bfloat16 *po = part.o + ((int64_t)b * nsplit * 128 + h) * 512 + d0;   // split s at po[s * 65536]
+  // block: two groups of 8 dims (j) x 128 heads; warp w: heads 32 (w & 3) + lane of group
+  // j = 2 blockIdx.x + (w >> 2), so every load of a partial is a contiguous 512-byte run
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = 32 * (warp & 3) + lane;
+  const int j = 2 * blockIdx.x + (warp >> 2);
+  const float *ml = part.ml + ((int64_t)b * nsplit * 128 + h) * 2;                  // split s at ml[s * 256]
+  const __nv_bfloat16 *po = part.o + (((int64_t)b * nsplit * 64 + j) * 128 + h) * 8;  // split s at po[s * 65536]
   float M = -INFINITY;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float Lsum = 0.f;
@@ -482,9 +487,9 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int ns
     Lsum += w;
     const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[2 * j] = fmaf(w, __bfloat162float(p2[j].x), acc[2 * j]);
-      acc[2 * j + 1] = fmaf(w, __bfloat162float(p2[j].y), acc[2 * j + 1]);
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] = fmaf(w, __bfloat162float(p2[q].x), acc[2 * q]);
+      acc[2 * q + 1] = fmaf(w, __bfloat162float(p2[q].y), acc[2 * q + 1]);
     }
   };
   if (nsplit <= NSMAX) {
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int ns
       if (s < nsplit) {
         m[s] = __ldg(ml + (int64_t)s * 256);
         l[s] = __ldg(ml + (int64_t)s * 256 + 1);
-        v[s] = __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 128 * 512));
+        v[s] = __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 64 * 128 * 8));
       }
     }
 #pragma unroll
@@ -509,16 +514,16 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int ns
     for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * 256));
     for (int s = 0; s < nsplit; ++s)
       add(__ldg(ml + (int64_t)s * 256), __ldg(ml + (int64_t)s * 256 + 1),
-          __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 128 * 512)));
+          __ldg(reinterpret_cast<const uint4 *>(po + (int64_t)s * 64 * 128 * 8)));
   }
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   uint4 o;
   __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) o2[j] = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-  *reinterpret_cast<uint4 *>(out + ((int64_t)b * 128 + h) * V_W + d0) = o;
+  for (int q = 0; q < 4; ++q) o2[q] = __floats2bfloat162_rn(acc[2 * q] * inv, acc[2 * q + 1] * inv);
+  *reinterpret_cast<uint4 *>(out + ((int64_t)b * 128 + h) * V_W + 8 * j) = o;
   // the per-split logits are scaled, so M and lse are in logit units
-  if (d0 == 0) lse[(int64_t)b * 128 + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
+  if (j == 0) lse[(int64_t)b * 128 + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
 }
 
 // Q as a 2-D bf16 tensor [rows, 576] with a [128 rows x 64 dims] box, 128-byte swizzle.
