@@ -178,11 +178,19 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     uint32_t c[TK_BPT];
 #pragma unroll
     for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
+    {                                                      // all remote loads issued before any use
+      uint4 v[TK_CL];
+      uint32_t ab[TK_CL];
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) {                 // plain loads, issued together
-      tab += *cluster.map_shared_rank(&S.cta_cnt[0], r);
-      const uint4 v = *reinterpret_cast<const uint4 *>(cluster.map_shared_rank(h + TK_BPT * tid, r));
-      c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+      for (uint32_t r = 0; r < TK_CL; ++r) {
+        v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
+        ab[r] = ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r));
+      }
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) {
+        tab += ab[r];
+        c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w;
+      }
     }
     uint32_t tot;
     const uint32_t incl = tk_block_scan(c[0] + c[1] + c[2] + c[3], S.warp_sums, &tot);
@@ -223,10 +231,12 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     uint32_t c[TK_BPT];
 #pragma unroll
     for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
+    {                                                      // all remote loads issued before any use
+      uint4 v[TK_CL];
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(cluster.map_shared_rank(h + TK_BPT * tid, r));
-      c[0] += v.x; c[1] += v.y; c[2] += v.z; c[3] += v.w;
+      for (uint32_t r = 0; r < TK_CL; ++r) v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) { c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w; }
     }
     uint32_t tot;
     const uint32_t mine = c[0] + c[1] + c[2] + c[3];
@@ -277,10 +287,15 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   __syncthreads();
   cluster_sync();
   uint32_t gt_base = 0, eq_base = 0;
-  for (uint32_t r = 0; r < rank; ++r) {
-    const uint32_t *rc = cluster.map_shared_rank(S.cta_cnt, r);
-    gt_base += rc[0];
-    eq_base += rc[1];
+  {
+    uint32_t g[TK_CL], e[TK_CL];
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) {
+      g[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r)) : 0u;
+      e[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r)) : 0u;
+    }
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
   }
   uint32_t gpos = gt_base + S.warp_gt[warp];
   uint32_t epos = eq_base + S.warp_eq[warp];
