@@ -52,34 +52,62 @@ static __device__ __noinline__ void pf_fixup_block(const PfFix &P, int b, float 
   const int Lb = min(P.seq_len[b], P.Lmax);
   const int64_t base = P.host_base[b];
   const float *sc = P.scores + (int64_t)b * P.Lmax;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = FX_THREADS / 32;
-  // thread tid owns the contiguous token segment [t0, t1): independent loads, and
-  // its qualifiers' ranks follow from a block scan of the per-thread counts
-  const int seg = (Lb + FX_THREADS - 1) / FX_THREADS;
-  const int t0 = min(Lb, tid * seg), t1 = min(Lb, t0 + seg);
+  // warp w owns the 32-aligned token segment [w0, w1); its lanes read consecutive
+  // tokens (coalesced), four chunks of 32 per iteration with their loads issued
+  // together, and the qualifiers' ranks follow from per-warp counts
+  const int wseg = ((Lb + NW - 1) / NW + 31) & ~31;
+  const int w0 = min(Lb, warp * wseg), w1 = min(Lb, w0 + wseg);
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
+  // qualifier test of token t with its map entry g (resident at scoring time: not one)
+  auto load4 = [&](int t0, bool (&q)[4], int32_t (&g)[4]) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = t0 + 32 * j + lane;
+      v[j] = t < w1 ? sc[t] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = t0 + 32 * j + lane;
+      const bool above = t < w1 && v[j] > theta;
+      g[j] = above ? L.host2gpu[base + t] : 0;
+      q[j] = above && g[j] < 0;
+    }
+  };
   for (int round = 0; round < 64; ++round) {
-    int c = 0;
-#pragma unroll 8
-    for (int t = t0; t < t1; ++t)
-      if (sc[t] > theta && L.host2gpu[base + t] < 0) ++c;
-    block_prefix(FX_THREADS, [&](int) { return c; }, sm.seg_pre);   // f(i) is evaluated by thread i
+    uint32_t c = 0;
+    for (int t0 = w0; t0 < w1; t0 += 128) {
+      bool q[4];
+      int32_t g[4];
+      load4(t0, q, g);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c += __popc(__ballot_sync(0xffffffffu, q[j]));
+    }
+    if (lane == 0) sm.seg_pre[warp] = (int32_t)c;
     if (tid == 0) { sm.n_need = 0; sm.n_free = 0; }
     __syncthreads();
-    uint32_t r = sm.seg_pre[tid];
-    for (int t = t0; t < t1; ++t) {
-      if (!(sc[t] > theta)) continue;
-      const int32_t g = L.host2gpu[base + t];
-      if (g >= 0) continue;                            // resident at scoring time: not a qualifier
-      if (r < (uint32_t)cap && g == -1) {
-        const int i = atomicAdd(&sm.n_need, 1);
-        if (i < FX_LIST) sm.need_t[i] = t;
-      } else if (r >= (uint32_t)cap && g <= -2) {
-        const int i = atomicAdd(&sm.n_free, 1);
-        if (i < FX_LIST) { sm.free_row[i] = -2 - g; sm.free_t[i] = t; }
+    uint32_t r = 0;
+    for (int w = 0; w < warp; ++w) r += (uint32_t)sm.seg_pre[w];
+    for (int t0 = w0; t0 < w1; t0 += 128) {
+      bool q[4];
+      int32_t g[4];
+      load4(t0, q, g);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, q[j]);
+        const uint32_t rk = r + __popc(bal & lanemask_lt());
+        const int t = t0 + 32 * j + lane;
+        if (q[j] && rk < (uint32_t)cap && g[j] == -1) {
+          const int i = atomicAdd(&sm.n_need, 1);
+          if (i < FX_LIST) sm.need_t[i] = t;
+        } else if (q[j] && rk >= (uint32_t)cap && g[j] <= -2) {
+          const int i = atomicAdd(&sm.n_free, 1);
+          if (i < FX_LIST) { sm.free_row[i] = -2 - g[j]; sm.free_t[i] = t; }
+        }
+        r += __popc(bal);
       }
-      ++r;
     }
     __syncthreads();
     const int np = min(min(sm.n_need, sm.n_free), FX_LIST);
