@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&qmap);
+      const uint64_t stream_once = l2_evict_first_policy();   // keys are read once per step
       int it = 0, qn = 0, cur = -1;
       for (int i = blockIdx.x; i < T; i += gridDim.x, ++it) {
         const int b = find_req(S.tile_pre, P.B, i);
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
         const uint32_t ph = (it / IX_STAGES) & 1;
         if (!mbar_wait(&S.empty[s], ph ^ 1)) { set_status(ctr, ECHO_ERR_TIMEOUT); break; }
         mbar_arrive_expect_tx(&S.full[s], IX_KTILE_BYTES);
-        tma_load_2d(kbuf + s * IX_KTILE_BYTES, &kmap, &S.full[s], 0, b * P.Lmax + t0);
+        tma_load_2d_hint(kbuf + s * IX_KTILE_BYTES, &kmap, &S.full[s], 0, b * P.Lmax + t0, stream_once);
       }
     }
   } else if (warp == 1) {
