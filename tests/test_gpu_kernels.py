@@ -129,6 +129,20 @@ def test_topk_all_equal_takes_lowest_indices():
     assert sorted(out[0].tolist()) == list(range(2048)) and kth[0] == 7.0
 
 
+def test_topk_many_rows():
+    # more rows than two per SM (prefill blocks run one row per query): ragged lengths,
+    # ties, rows shorter than k, predictions inside and outside the window
+    rng = np.random.default_rng(4)
+    n_rows = 2 * E.lib().echo_device_sm_count() + 5
+    k = 256
+    lists, thetas = [], []
+    for r in range(n_rows):
+        L = int(rng.integers(0, 4000)) if r % 7 else int(rng.integers(0, 300))
+        lists.append((rng.integers(0, 200, L) / 16.0).astype(np.float32))
+        thetas.append([math.inf, 3.0, 11.5, 0.25][r % 4])
+    check_topk(lists, k, thetas)
+
+
 def test_topk_large_context_k2048():
     rng = np.random.default_rng(1)
     lists = [(rng.integers(0, 2 ** 14, 100_000) / 1024.0).astype(np.float32) for _ in range(3)]
