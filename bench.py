@@ -540,7 +540,7 @@ def run_echo(args, ws, rank, local):
                 "how": "library step replayed as a CUDA Graph; each step's inputs copied from pinned host memory "
                        "and its attention output read back inside the timed region, on a copy stream that "
                        "overlaps the next step's inputs with the current step (two buffer sets)"},
-        "gpu_launches": launches_per_step(prefetch) * layers * args.steps,
+        "gpu_launches": launches_per_step(prefetch, wl.n_gpu) * layers * args.steps,
         "clocks": clocks,
         "stages_us": stages,
         "indexer_gbs": achieved,
@@ -558,11 +558,13 @@ def run_echo(args, ws, rank, local):
 PROBE_STEPS = 3
 
 
-def launches_per_step(prefetch: bool) -> int:
-    """Kernels of one layer step: write-back 1 (cooperative manager), reserve 1,
-    indexer 1, top-k 1 (with the deferred exact prefetch cap), recall 1 (cooperative
-    manager: protect, miss list, evict+bind, copy, translate), MLA 2."""
-    return (1 + 1 + 1 + 1 + 1 + 2) if prefetch else (1 + 1 + 1 + 1 + 2)
+def launches_per_step(prefetch: bool, n_gpu: int) -> int:
+    """Kernels of one layer step (echo_decode_layer_step): write-back with the step's
+    prefetch budget (the single-CTA write-back from the pending victim list on pools of
+    at least 14080 slots, then the cooperative manager), indexer 1, top-k 1 (with the
+    deferred exact prefetch cap when prefetching), recall 1 (cooperative manager:
+    protect, miss list, evict+bind, copy, translate), MLA 2 (split + combine)."""
+    return (2 if n_gpu >= 14080 else 1) + 1 + 1 + 1 + 2
 
 
 def enqueue_index_topk(lib, dl, h, between=None):

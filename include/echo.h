@@ -72,8 +72,9 @@ enum {
   ECHO_CTR_WB_EVICTED = 13, /*   tokens evicted by the write-back                       */
   ECHO_CTR_BOUND = 14,      /*   tokens bound to slots by the recall                    */
   ECHO_CTR_QUALIFIED = 15,  /*   tokens that met the prefetch rule (before the cap)     */
-                            /* 16..31: the manager's own words (grid barrier, cursors);  */
-                            /*   zero between calls, set to zero by echo_cache_reset     */
+                            /* 16..31: the manager's own words (grid barrier, cursors,   */
+                            /*   the pending victim list's count and step); set to zero  */
+                            /*   by echo_cache_reset                                     */
   ECHO_NUM_COUNTERS = 32
 };
 
@@ -88,13 +89,21 @@ enum {
  *   priority[n_gpu]  : step of the slot's last touch (LRU key with the host index)
  *   index_buf[n_gpu] : the manager's scratch (victim-selection histograms, at most
  *                      3 x 2048 words; pools under 6 slots use counter words 24..29);
- *                      zero between calls
+ *                      zero between calls, except, in pools of at least 14080 slots,
+ *                      its last 768 words: the pending victim list that a recall
+ *                      leaves for the next write-back (the recall ranks the B least
+ *                      recently used slots it does not evict; the write-back evicts
+ *                      them in one CTA if every slot still holds its recorded key,
+ *                      and otherwise runs the full selection)
  *   free_map[n_gpu]  : one byte per slot, 1 = free
  * Metadata = 4*n_host + 13*n_gpu bytes (echo_cache_metadata_bytes) plus the fixed
  * 128-byte counters block.  gpu2host, priority and counters must be 16-byte aligned
  * (read as vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
  * The manager calls (write-back, recall, alloc, evict) are cooperative launches over
- * the whole device, one CTA per SM; calls on one layer must not run concurrently.
+ * the whole device, one CTA per SM (a write-back on a pool of at least 14080 slots
+ * first launches one CTA that uses the pending list; the cooperative launch then
+ * returns at once if that CTA did the work); calls on one layer must not run
+ * concurrently, and only the library writes the layer's arrays between calls.
  * A manager call whose grid barrier waited more than ~1 s sets ECHO_ERR_TIMEOUT and
  * leaves the layer undefined until echo_cache_reset.
  */

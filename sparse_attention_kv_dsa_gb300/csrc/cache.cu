@@ -72,10 +72,27 @@ enum { MODE_WRITEBACK = 0, MODE_RECALL = 1, MODE_ALLOC = 2, MODE_EVICT = 3 };
 enum {
   MG_BAR = 16,         // words 16-17: grid barrier arrivals (uint64, a multiple of the grid between barriers)
   MG_ABORT = 18,       // a barrier wait gave up: every CTA leaves
+  MG_FAST = 19,        // the write-back was done by wb_fast_kernel (set by it before every
+                       // cooperative write-back it precedes)
+  MG_PRE_N = 20,       // entries in the pending victim list (0 = none)
+  MG_PRE_STEP = 21,    // step of the recall that wrote the list
   MG_VCUR = 22,        // victim rank cursor
   MG_SCUR = 23,        // free-slot scan cursor
   MG_SMALL_HIST = 24,  // words 24..29: the histograms of pools with fewer than 6 slots
+  MG_PCUR = 30,        // pending-list cursor
 };
+
+// Pending victims.  A write-back evicts the B least recently used slots, and between a
+// recall and the next step's write-back no slot changes: so the recall's LRU selection
+// can also rank the next B victims (a second target rank in the same radix passes)
+// and leave them, with their keys, at the end of index_buf.  The write-back then binds
+// them in one CTA (wb_fast_kernel) after checking that every entry still holds its key,
+// and its cooperative launch returns at once; any other case takes the full path.
+// Pools of at least PRE_POOL slots keep this layout of index_buf in every mode:
+//   [0, 6144)                two sets of three 2048-bin histograms
+//   [6144 * 2, +MAXB)        the recall's miss counters
+//   [n_gpu - 3 PRE_MAX, n_gpu)  pending list: slot, key low word, key high word
+constexpr int PRE_MAX = 256;    // requests per recall that leave a list
 
 struct ManageParams {
   echo_cache_layer_t L;
@@ -115,6 +132,11 @@ struct ManageParams {
   int32_t *rs_cap;
   int32_t *rs_pf_count;
   int rs_cap_max, rs_cap_div;
+  // pending victims (pools of at least PRE_POOL slots)
+  uint32_t *hist2;        // second histogram set (recall), or null
+  int32_t *pend;          // pending list: slot[PRE_MAX], key low[PRE_MAX], key high[PRE_MAX]
+  int pre_n;              // recall: extra victims to rank for the next write-back (0 = none)
+  int fast_checked;       // write-back: wb_fast_kernel ran first; return if it did the work
 };
 
 constexpr int MG_THREADS = 512;
@@ -123,16 +145,22 @@ constexpr int MG_MAXBITS = 11;                  // 2048-bin digits at most
 constexpr int MG_BPT = (1 << MG_MAXBITS) / MG_THREADS;   // bins per thread in the digit search
 constexpr int MAXB = 1024;                      // requests per call handled by the manager
 constexpr size_t MG_KEY_SMEM = 192 * 1024;      // victim keys cached per CTA (bytes)
+constexpr int PRE_POOL = 6 * (1 << MG_MAXBITS) + MAXB + 3 * PRE_MAX;
 
 struct MgShared {
   uint32_t hist[1 << MG_MAXBITS];
   int32_t pre_a[MAXB + 1];             // prefixes of the token lists
   int32_t pre_b[MAXB + 1];
   uint32_t warp_sums[32];
+  uint64_t warp_sums2[32];             // two packed counts per warp (digit searches)
   uint32_t wcnt[MG_WARPS];             // per-warp counts (block reductions, victim ranks)
+  uint32_t wcnt1[MG_WARPS];            // per-warp pending-list counts
   int64_t tok0[MAXB];                  // per request: host index of token 0 (write-back: of the new token)
+  uint32_t hist1[1 << MG_MAXBITS];     // second target's histogram, once its prefix differs
   uint32_t res[2];                     // [0] chosen digit, [1] count above it
+  uint32_t res1[2];                    // the same for the second target
   uint32_t base;                       // this CTA's first rank from a global cursor
+  uint32_t base1;                      // its first pending-list position
 };
 
 __device__ __forceinline__ int bitlen_u64(uint64_t x) { return x ? 64 - __clzll((long long)x) : 0; }
@@ -175,6 +203,33 @@ __device__ __noinline__ bool grid_sync(int32_t *ctr) {
   }
   __syncthreads();
   return gs_ok != 0;
+}
+
+// Inclusive scan over the CTA of two counts packed in 64 bits (the low count's block
+// total stays below 2^32, so nothing carries into the high half).
+__device__ __forceinline__ uint64_t block_incl_scan2(uint64_t v, uint64_t *warp_sums, uint64_t *total) {
+  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= (uint32_t)o) v += n;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    uint64_t w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= (uint32_t)o) w += n;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  if (wid > 0) v += warp_sums[wid - 1];
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return v;
 }
 
 // Sum over the CTA (every thread gets it); ends with a barrier.
@@ -221,6 +276,47 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_s
   return v;
 }
 
+// Write-back of request b's new token by one warp (A1): its host pool row, its GPU slot
+// row if it has a slot (its binding is visible), its indexer key; the prefetch budget
+// of the step when the call carries one; the request's length grows by one.
+__device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int lane, int32_t step) {
+  const echo_cache_layer_t &L = P.L;
+  int32_t *ctr = L.counters;
+  const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
+  const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
+  const int32_t l = P.seq_len[b];
+  const int64_t h = (int64_t)P.host_base[b] + l;
+  const bool bad_h = h < 0 || h >= L.n_host, bad_l = l >= P.Lmax;
+  if (P.rs_cap && lane == 0) {                           // budget from the length after this write-back
+    const int32_t len = (bad_h || bad_l) ? l : l + 1;
+    int c = 0;
+    if (P.rs_cap_max > 0)
+      c = max(P.rs_cap_div > 0 ? min(P.rs_cap_max, (len + P.rs_cap_div - 1) / P.rs_cap_div) : P.rs_cap_max, 0);
+    P.rs_cap[b] = c;
+    P.rs_pf_count[b] = 0;
+  }
+  if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); return; }
+  if (bad_l) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); return; }
+  const int32_t g = __ldcg(L.host2gpu + h);
+  const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + (int64_t)b * KV_W * esz);
+  uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
+  uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz) : nullptr;
+  for (int c = lane; c < chunks; c += 32) {
+    const uint4 v = src[c];
+    hdst[c] = v;
+    if (gdst) gdst[c] = v;
+  }
+  if (g >= 0 && lane == 0) L.priority[g] = step;         // refresh an already resident token
+  if (g < 0 && lane == 0) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
+  const int kesz = P.ik_dtype == ECHO_F32 ? 4 : 1;
+  const char *ks = (const char *)P.new_ik + (int64_t)b * P.D * kesz;
+  char *kd = (char *)P.idx_k + ((int64_t)b * P.Lmax + l) * P.D * kesz;
+  for (int c = lane; c < P.D * kesz / 4; c += 32)
+    reinterpret_cast<uint32_t *>(kd)[c] = reinterpret_cast<const uint32_t *>(ks)[c];
+  __syncwarp();
+  if (lane == 0) P.seq_len[b] = l + 1;
+}
+
 __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constant__ ManageParams P) {
   extern __shared__ __align__(16) unsigned char dsm[];
   MgShared &S = *reinterpret_cast<MgShared *>(dsm);
@@ -231,6 +327,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
   const int64_t gtid = blockIdx.x * (int64_t)MG_THREADS + tid;
   const int64_t gthreads = (int64_t)gridDim.x * MG_THREADS;
   const int64_t gwarp = gtid >> 5, gwarps = gthreads >> 5;
+  // a write-back that wb_fast_kernel completed (the word is set before this launch)
+  if (P.mode == MODE_WRITEBACK && P.fast_checked && ldcg(ctr + MG_FAST) != 0) return;
 
   const int32_t step0 = ldcg(ctr + ECHO_CTR_STEP);
   const int32_t step = P.mode == MODE_WRITEBACK ? step0 + 1 : step0;
@@ -381,6 +479,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
   };
 
   uint32_t m_eff = 0;
+  bool two = false;                                       // a pending list is ranked (uniform)
+  uint64_t prefix1 = 0;                                   // its last key
   if (m_req > 0) {                                        // uniform across the grid
     // keys of the slice (4 slots per thread and iteration)
     if (cached) {
@@ -397,58 +497,88 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     }
     // MSB-first radix select of the m_eff-th largest key (keys are unique) over the
     // bitlen(step) + hbits + 1 bits a key can have.  The first digit's histogram
-    // also counts the evictable slots, which bounds m_eff.
+    // also counts the evictable slots, which bounds m_eff.  A recall that leaves a
+    // pending list selects a second rank, m_eff + pre_n, in the same passes: while
+    // the two prefixes agree one histogram serves both, after that each has its own.
     uint64_t prefix = 0;
-    uint32_t above = 0;
+    uint32_t above = 0, above1 = 0, tgt1 = 0;
     int left = bitlen_u64((uint64_t)max(step, 0)) + hbits + 1, pass = 0;
     const int nb_all = 1 << P.dbits;
     while (left > 0) {
       const int w = min(P.dbits, left), shift = left - w, nbins = 1 << w;
+      const bool split = two && prefix1 != prefix;       // the second target needs its own counts
       uint32_t *gh = P.hist + (pass % 3) * nb_all;
-      for (int i = tid; i < nbins; i += MG_THREADS) S.hist[i] = 0;
+      uint32_t *gh1 = split ? P.hist2 + (pass % 3) * nb_all : gh;
+      for (int i = tid; i < nbins; i += MG_THREADS) {
+        S.hist[i] = 0;
+        if (split) S.hist1[i] = 0;
+      }
       __syncthreads();
       const uint64_t hi_mask = (shift + w >= 64) ? 0ull : (~0ull << (shift + w));
       for (int base = 0; base < nloc; base += MG_THREADS) {   // uniform trip count per warp
         const int i = base + tid;
         const uint64_t kk = i < nloc ? key_at(i) : 0;
-        hist_add_warp(S.hist, kk != 0 && (kk & hi_mask) == (prefix & hi_mask),
-                      (uint32_t)((kk >> shift) & (uint64_t)(nbins - 1)));
+        const uint32_t dg = (uint32_t)((kk >> shift) & (uint64_t)(nbins - 1));
+        hist_add_warp(S.hist, kk != 0 && (kk & hi_mask) == (prefix & hi_mask), dg);
+        if (split) hist_add_warp(S.hist1, kk != 0 && (kk & hi_mask) == (prefix1 & hi_mask), dg);
       }
       __syncthreads();
-      for (int i = tid; i < nbins; i += MG_THREADS)
+      for (int i = tid; i < nbins; i += MG_THREADS) {
         if (S.hist[i]) atomicAdd(gh + i, S.hist[i]);
-      if (!grid_sync(ctr)) return;
-      // the histogram of two passes ago was read by every CTA before this barrier:
-      // clear it for the pass after next
-      {
-        uint32_t *old = P.hist + ((pass + 2) % 3) * nb_all;
-        for (int64_t i = gtid; i < nb_all; i += gthreads) old[i] = 0;
+        if (split && S.hist1[i]) atomicAdd(gh1 + i, S.hist1[i]);
       }
-      // the digit, from the global counts of this thread's MG_BPT consecutive bins
-      uint32_t cb[MG_BPT], mine = 0;
+      if (!grid_sync(ctr)) return;
+      // the histograms of two passes ago were read by every CTA before this barrier:
+      // clear them for the pass after next
+      for (int64_t i = gtid; i < nb_all; i += gthreads) {
+        P.hist[((pass + 2) % 3) * nb_all + i] = 0;
+        if (P.hist2) P.hist2[((pass + 2) % 3) * nb_all + i] = 0;
+      }
+      // the digits from the global counts: this thread's MG_BPT consecutive bins of
+      // each histogram (both loaded before either is used), one block scan of both,
+      // and the bin where the count from the top reaches the target
+      uint32_t cb[MG_BPT], cb1[MG_BPT], mine = 0, mine1 = 0;
 #pragma unroll
       for (int j = 0; j < MG_BPT; ++j) {
         const int d = MG_BPT * tid + j;
         cb[j] = d < nbins ? (uint32_t)__ldcg(reinterpret_cast<const int32_t *>(gh + d)) : 0u;
-        mine += cb[j];
+        cb1[j] = (split && d < nbins) ? (uint32_t)__ldcg(reinterpret_cast<const int32_t *>(gh1 + d)) : 0u;
       }
-      uint32_t tot;
-      const uint32_t incl = block_incl_scan(mine, S.warp_sums, &tot);
+#pragma unroll
+      for (int j = 0; j < MG_BPT; ++j) {
+        mine += cb[j];
+        mine1 += cb1[j];
+      }
+      uint64_t tot2;
+      const uint64_t incl2 = block_incl_scan2(((uint64_t)mine1 << 32) | mine, S.warp_sums2, &tot2);
+      const uint32_t tot = (uint32_t)tot2, incl = (uint32_t)incl2;
       if (pass == 0) {                                   // tot = evictable slots
         m_eff = min((uint32_t)m_req, tot);
         if (blockIdx.x == 0 && tid == 0 && m_eff < (uint32_t)m_req) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
         if (m_eff == 0) break;                           // uniform: every CTA read the same counts
+        two = P.pre_n > 0 && m_eff == (uint32_t)m_req && m_eff + (uint32_t)P.pre_n <= tot;
+        tgt1 = m_eff + (uint32_t)P.pre_n;
       }
-      uint32_t sfx = tot - incl;                         // keys in bins above mine
-      const uint32_t need = m_eff - above;
+      auto search = [&](const uint32_t (&c)[MG_BPT], uint32_t inc, uint32_t tt, uint32_t need, uint32_t *res) {
+        uint32_t sfx = tt - inc;                         // keys in bins above mine
 #pragma unroll
-      for (int j = MG_BPT - 1; j >= 0; --j) {            // my bins, from the top
-        if (sfx < need && need <= sfx + cb[j]) { S.res[0] = MG_BPT * tid + j; S.res[1] = sfx; }
-        sfx += cb[j];
+        for (int j = MG_BPT - 1; j >= 0; --j) {          // my bins, from the top
+          if (sfx < need && need <= sfx + c[j]) { res[0] = MG_BPT * tid + j; res[1] = sfx; }
+          sfx += c[j];
+        }
+      };
+      search(cb, incl, tot, m_eff - above, S.res);
+      if (two) {
+        if (split) search(cb1, (uint32_t)(incl2 >> 32), (uint32_t)(tot2 >> 32), tgt1 - above1, S.res1);
+        else search(cb, incl, tot, tgt1 - above1, S.res1);
       }
       __syncthreads();
       prefix |= (uint64_t)S.res[0] << shift;
       above += S.res[1];
+      if (two) {
+        prefix1 |= (uint64_t)S.res1[0] << shift;
+        above1 += S.res1[1];
+      }
       left = shift;
       ++pass;
       __syncthreads();
@@ -457,27 +587,42 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
       const uint64_t kstar = prefix;
       // evict every key >= kstar (exactly m_eff tokens).  The CTA counts its victims,
       // takes a block of ranks with one atomic, and victim v is rebound at once to
-      // the token of rank n_scan + v, or freed if none is left (evict mode).
-      uint32_t nv = 0;
+      // the token of rank n_scan + v, or freed if none is left (evict mode).  With a
+      // pending list, keys in [prefix1, kstar) (exactly pre_n of them) are listed the
+      // same way.  Each slot's key is read before its own lane changes the slot.
+      uint32_t nv = 0, np = 0;
       for (int base = 0; base < nloc; base += MG_THREADS) {
         const int i = base + tid;
         const uint64_t kk = i < nloc ? key_at(i) : 0;
         nv += __popc(__ballot_sync(0xffffffffu, kk != 0 && kk >= kstar));
+        np += __popc(__ballot_sync(0xffffffffu, two && kk != 0 && kk >= prefix1 && kk < kstar));
       }
-      if (lane == 0) S.wcnt[tid >> 5] = nv;              // per-warp victim counts
+      if (lane == 0) {                                   // per-warp counts
+        S.wcnt[tid >> 5] = nv;
+        S.wcnt1[tid >> 5] = np;
+      }
       __syncthreads();
       if (tid == 0) {
-        uint32_t t = 0;
-        for (int w = 0; w < MG_WARPS; ++w) { const uint32_t x = S.wcnt[w]; S.wcnt[w] = t; t += x; }
+        uint32_t t = 0, t1 = 0;
+        for (int w = 0; w < MG_WARPS; ++w) {
+          const uint32_t x = S.wcnt[w], x1 = S.wcnt1[w];
+          S.wcnt[w] = t;
+          S.wcnt1[w] = t1;
+          t += x;
+          t1 += x1;
+        }
         S.base = t ? atomicAdd(reinterpret_cast<unsigned int *>(ctr + MG_VCUR), t) : 0u;
+        S.base1 = t1 ? atomicAdd(reinterpret_cast<unsigned int *>(ctr + MG_PCUR), t1) : 0u;
       }
       __syncthreads();
-      uint32_t rank = S.base + S.wcnt[tid >> 5];
+      uint32_t rank = S.base + S.wcnt[tid >> 5], pos = S.base1 + S.wcnt1[tid >> 5];
       for (int base = 0; base < nloc; base += MG_THREADS) {
         const int i = base + tid;
         const uint64_t kk = i < nloc ? key_at(i) : 0;
         const bool isv = kk != 0 && kk >= kstar;
+        const bool isp = two && kk != 0 && kk >= prefix1 && kk < kstar;
         const uint32_t bal = __ballot_sync(0xffffffffu, isv);
+        const uint32_t balp = __ballot_sync(0xffffffffu, isp);
         if (isv) {
           const int g = g0 + i;
           const int64_t h_old = cached ? (int64_t)(hmax - ((kk - 1) & hmax)) : (int64_t)ldcg(L.gpu2host + g);
@@ -490,7 +635,16 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
             L.free_map[g] = 1;
           }
         }
+        if (isp) {
+          const uint32_t q = pos + __popc(balp & lanemask_lt());
+          if (q < (uint32_t)P.pre_n) {
+            P.pend[q] = g0 + i;
+            P.pend[PRE_MAX + q] = (int32_t)(uint32_t)kk;
+            P.pend[2 * PRE_MAX + q] = (int32_t)(uint32_t)(kk >> 32);
+          }
+        }
         rank += __popc(bal);
+        pos += __popc(balp);
       }
       __syncthreads();
     }
@@ -531,39 +685,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
   const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
   if (P.mode == MODE_WRITEBACK) {
     // host pool row, GPU slot row and indexer key of each new token; one warp per request
-    for (int64_t b = gwarp; b < P.B; b += gwarps) {
-      const int32_t l = P.seq_len[b];
-      const int64_t h = (int64_t)P.host_base[b] + l;
-      const bool bad_h = h < 0 || h >= L.n_host, bad_l = l >= P.Lmax;
-      if (P.rs_cap && lane == 0) {                       // budget from the length after this write-back
-        const int32_t len = (bad_h || bad_l) ? l : l + 1;
-        int c = 0;
-        if (P.rs_cap_max > 0)
-          c = max(P.rs_cap_div > 0 ? min(P.rs_cap_max, (len + P.rs_cap_div - 1) / P.rs_cap_div) : P.rs_cap_max, 0);
-        P.rs_cap[b] = c;
-        P.rs_pf_count[b] = 0;
-      }
-      if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); continue; }
-      if (bad_l) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); continue; }
-      const int32_t g = ldcg(L.host2gpu + h);
-      const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + b * KV_W * esz);
-      uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
-      uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz) : nullptr;
-      for (int c = lane; c < chunks; c += 32) {
-        const uint4 v = src[c];
-        hdst[c] = v;
-        if (gdst) gdst[c] = v;
-      }
-      if (g >= 0 && lane == 0) L.priority[g] = step;     // refresh an already resident token
-      if (g < 0 && lane == 0) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
-      const int kesz = P.ik_dtype == ECHO_F32 ? 4 : 1;
-      const char *ks = (const char *)P.new_ik + b * P.D * kesz;
-      char *kd = (char *)P.idx_k + (b * P.Lmax + l) * P.D * kesz;
-      for (int c = lane; c < P.D * kesz / 4; c += 32)
-        reinterpret_cast<uint32_t *>(kd)[c] = reinterpret_cast<const uint32_t *>(ks)[c];
-      __syncwarp();
-      if (lane == 0) P.seq_len[b] = l + 1;
-    }
+    for (int64_t b = gwarp; b < P.B; b += gwarps) writeback_row(P, (int)b, lane, step);
   } else if (P.mode == MODE_RECALL) {
     // rows: rank r < nA from staging, else from the host pool (zero-copy reads).
     // Lane j < 4 resolves row r0 + j (list entry, host index, slot) so the four
@@ -614,7 +736,10 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
 
   // ---- counters and the manager's scratch words ---------------------------------
   if (m_req > 0) {                                      // clear the global histograms
-    for (int64_t i = gtid; i < (int64_t)3 << P.dbits; i += gthreads) P.hist[i] = 0;
+    for (int64_t i = gtid; i < (int64_t)3 << P.dbits; i += gthreads) {
+      P.hist[i] = 0;
+      if (P.hist2) P.hist2[i] = 0;
+    }
   }
   if (P.mode == MODE_RECALL && P.miss_cnt)               // and the miss counters
     for (int64_t b = gtid; b < P.B; b += gthreads) P.miss_cnt[b] = 0;
@@ -638,6 +763,104 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     }
     ctr[MG_VCUR] = 0;
     ctr[MG_SCUR] = 0;
+    ctr[MG_PCUR] = 0;
+    ctr[MG_PRE_N] = two ? P.pre_n : 0;                 // every other call drops the list
+    ctr[MG_PRE_STEP] = step;
+  }
+}
+
+// ------------------------------------------------------ write-back, fast --
+// The write-back from the pending list, in one CTA: the new tokens that need a slot
+// (the full path's rule), then, when every condition of the list holds, its m_req
+// largest keys are evicted and bound to them in rank order, the rows are written and
+// the counters updated exactly as the full path would; MG_FAST tells the cooperative
+// launch that follows whether anything is left to do.  Conditions: the list was left
+// by a recall of the current step, no free slot would be used (the full path binds
+// those first), it holds at least m_req entries, and every entry's slot still holds
+// the key recorded for it.  Victims beyond the list's first B ranks cannot be needed:
+// m_req <= B <= pre_n.
+constexpr int WF_THREADS = 512;
+
+__global__ void __launch_bounds__(WF_THREADS, 1) wb_fast_kernel(const __grid_constant__ ManageParams P) {
+  __shared__ int32_t pre_a[MAXB + 1];
+  __shared__ uint64_t pkey[PRE_MAX];
+  __shared__ int fast_s;
+  const echo_cache_layer_t &L = P.L;
+  int32_t *ctr = L.counters;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t step0 = ldcg(ctr + ECHO_CTR_STEP), n_free0 = ldcg(ctr + ECHO_CTR_N_FREE);
+  const int32_t pre_n = ldcg(ctr + MG_PRE_N), pre_step = ldcg(ctr + MG_PRE_STEP);
+  const int32_t step = step0 + 1;
+  // thread i < PRE_MAX reads list entry i and its slot's state now, so these loads
+  // overlap the token list below (entries past pre_n are not used)
+  static_assert(PRE_MAX <= WF_THREADS, "one list entry per thread");
+  int32_t g_i = -1, gh_i = -1, gp_i = 0;
+  uint64_t k_i = 0;
+  if (tid < PRE_MAX) {
+    g_i = ldcg(P.pend + tid);
+    k_i = ((uint64_t)(uint32_t)ldcg(P.pend + 2 * PRE_MAX + tid) << 32) | (uint32_t)ldcg(P.pend + PRE_MAX + tid);
+    if (g_i >= 0 && g_i < L.n_gpu) {
+      gh_i = ldcg(L.gpu2host + g_i);
+      gp_i = ldcg(L.priority + g_i);
+    }
+  }
+  block_prefix(P.B, [&](int b) {
+    const int32_t l = P.seq_len[b];
+    const int64_t h = (int64_t)P.host_base[b] + l;
+    const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
+    return (ok && ldcg(L.host2gpu + h) < 0) ? 1 : 0;
+  }, pre_a);
+  const int n_bind = pre_a[P.B];
+  const int m_req = max(0, n_bind - n_free0);
+  const int n_scan = min(max((int)n_free0, 0), n_bind);
+  bool fast = pre_n > 0 && pre_n <= PRE_MAX && pre_step == step0 && n_scan == 0 && m_req <= pre_n;
+  if (fast) {
+    const int hbits = bitlen_u64((uint64_t)max(L.n_host - 1, 1));
+    const uint64_t hmax = (1ull << hbits) - 1;
+    if (tid == 0) fast_s = 1;
+    __syncthreads();
+    if (tid < pre_n) {
+      const bool ok = g_i >= 0 && g_i < L.n_gpu && k_i != 0 && victim_key(gh_i, gp_i, step0, hbits, hmax) == k_i;
+      if (!ok) fast_s = 0;
+      pkey[tid] = k_i;
+    }
+    __syncthreads();
+    fast = fast_s != 0;
+  }
+  if (!fast) {                                           // uniform: one CTA
+    if (tid == 0) ctr[MG_FAST] = 0;
+    return;
+  }
+  // entry i of rank r (largest key first) is a victim if r < m_req and takes the
+  // token of rank r; keys are unique
+  if (tid < pre_n) {
+    int r = 0;
+    for (int j = 0; j < pre_n; ++j) r += pkey[j] > k_i;
+    if (r < m_req) {
+      int lo = 0, hi = P.B - 1;                          // last b with pre_a[b] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre_a[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      const int32_t g = g_i;
+      const int64_t h = (int64_t)P.host_base[lo] + P.seq_len[lo];
+      L.host2gpu[gh_i] = -1;
+      L.free_map[g] = 0;
+      L.gpu2host[g] = (int32_t)h;
+      L.host2gpu[h] = g;
+      L.priority[g] = step;
+    }
+  }
+  __syncthreads();                                       // bindings visible to the block
+  for (int b = warp; b < P.B; b += WF_THREADS / 32) writeback_row(P, b, lane, step);
+  __syncthreads();
+  if (tid == 0) {
+    ctr[ECHO_CTR_EVICT_M] = m_req;                       // n_free unchanged: every victim is bound
+    ctr[ECHO_CTR_STEP] = step;
+    for (int i = ECHO_CTR_HITS; i <= ECHO_CTR_QUALIFIED; ++i) ctr[i] = 0;
+    ctr[ECHO_CTR_WB_EVICTED] = m_req;
+    ctr[MG_PRE_N] = 0;
+    ctr[MG_FAST] = 1;
   }
 }
 
@@ -665,12 +888,33 @@ static cudaError_t run_manage(ManageParams P, cudaStream_t st) {
   P.cached = (size_t)per * 8 <= MG_KEY_SMEM;
   // the recall's miss counters follow the histograms when the pool leaves room for them
   const int nmc = P.mode == MODE_RECALL ? P.B : 0;
-  P.dbits = digit_bits(P.L.n_gpu, nmc);
-  if ((3 << P.dbits) + nmc > P.L.n_gpu) P.dbits = digit_bits(P.L.n_gpu, 0);
-  const bool in_buf = (3 << P.dbits) <= P.L.n_gpu;
-  P.hist = in_buf ? reinterpret_cast<uint32_t *>(P.L.index_buf)
-                  : reinterpret_cast<uint32_t *>(P.L.counters + MG_SMALL_HIST);
-  P.miss_cnt = (nmc > 0 && (3 << P.dbits) + nmc <= P.L.n_gpu) ? P.L.index_buf + (3 << P.dbits) : nullptr;
+  if (P.L.n_gpu >= PRE_POOL) {
+    // the fixed layout with a pending victim list (see PRE_POOL)
+    constexpr int nb = 1 << MG_MAXBITS;
+    P.dbits = MG_MAXBITS;
+    P.hist = reinterpret_cast<uint32_t *>(P.L.index_buf);
+    P.miss_cnt = nmc > 0 ? P.L.index_buf + 6 * nb : nullptr;
+    P.pend = P.L.index_buf + P.L.n_gpu - 3 * PRE_MAX;
+    if (P.mode == MODE_RECALL && P.B <= PRE_MAX) {
+      P.hist2 = reinterpret_cast<uint32_t *>(P.L.index_buf + 3 * nb);
+      P.pre_n = P.B;
+    }
+  } else {
+    P.dbits = digit_bits(P.L.n_gpu, nmc);
+    if ((3 << P.dbits) + nmc > P.L.n_gpu) P.dbits = digit_bits(P.L.n_gpu, 0);
+    const bool in_buf = (3 << P.dbits) <= P.L.n_gpu;
+    P.hist = in_buf ? reinterpret_cast<uint32_t *>(P.L.index_buf)
+                    : reinterpret_cast<uint32_t *>(P.L.counters + MG_SMALL_HIST);
+    P.miss_cnt = (nmc > 0 && (3 << P.dbits) + nmc <= P.L.n_gpu) ? P.L.index_buf + (3 << P.dbits) : nullptr;
+  }
+  if (P.mode == MODE_WRITEBACK && P.L.n_gpu >= PRE_POOL) {
+    // the write-back from a pending list, when there is one; the cooperative launch
+    // below returns at once if it was done
+    wb_fast_kernel<<<1, WF_THREADS, 0, st>>>(P);
+    const cudaError_t fe = cudaGetLastError();
+    if (fe != cudaSuccess) return fe;
+    P.fast_checked = 1;
+  }
   const size_t smem = ((sizeof(MgShared) + 15) & ~size_t(15)) + (P.cached ? (size_t)per * 8 : 0);
   cudaError_t e = cudaFuncSetAttribute(mgr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -268,6 +268,80 @@ def test_evict_and_alloc_match_oracle_victims():
         assert np.all(t.c.gpu2host.cpu().numpy()[o] == toks)
 
 
+def test_pending_victim_writeback_matches_oracle():
+    # Pools of at least 14080 slots: each recall also ranks the next write-back's B
+    # victims, and the write-back binds them in one CTA.  Residency must equal the
+    # oracle's LRU after every call; manager word 19 tells which path the write-back
+    # took.  Rounds cover: free slots left (full path), a new token made resident by
+    # the recall (fewer victims than listed), a write-back of a subset of the requests,
+    # an eviction between recall and write-back (list dropped), two recalls in a step.
+    from harness import gpu_residency, check_gpu_maps
+    n_gpu, n_host, B, k = 14336, 60000, 6, 1536
+    t = TinyLayer(n_gpu, n_host, B=B, kv32=False)
+    t.idx_k = torch.zeros(B, 9600, 4, device=dev)
+    oc = O.LayerCache(n_gpu, n_host)
+    hb_np = np.arange(B, dtype=np.int64) * 9700
+    hb = torch.tensor(hb_np, dtype=torch.int32, device=dev)
+    seq_np = np.full(B, 9000, dtype=np.int64)
+    rng = np.random.default_rng(11)
+    path = []
+
+    def writeback(reqs):
+        seq_t = torch.tensor(seq_np[reqs], dtype=torch.int32, device=dev)
+        t.writeback(hb[reqs].contiguous(), seq_t)
+        torch.cuda.synchronize()
+        s_sub = seq_np[reqs].copy()
+        oc.writeback(hb_np[reqs], s_sub)
+        seq_np[reqs] = s_sub
+        assert np.array_equal(seq_t.cpu().numpy(), s_sub)
+        path.append(int(t.c.counters[19].item()))
+        assert gpu_residency(t.c) == oc.resident_priority(), "residency after the write-back"
+        check_gpu_maps(t.c)
+        assert t.c.status() == 0
+
+    def recall(extra=None, sel_np=None):
+        if sel_np is None:
+            sel_np = np.stack([rng.choice(int(seq_np[b]), k, replace=False) for b in range(B)]).astype(np.int32)
+        if extra is not None:                                  # request 0's next new token
+            sel_np[0, 0] = extra
+        miss, n_miss, slot = t.recall(torch.tensor(sel_np, device=dev), hb)
+        rec = oc.recall([sel_np[b] for b in range(B)], hb_np, [np.zeros(0, dtype=np.int64)] * B)
+        assert rec.status == 0 and t.c.status() == 0
+        for b in range(B):
+            assert set(miss[b, :n_miss[b]].tolist()) == set(rec.misses[b])
+        assert gpu_residency(t.c) == oc.resident_priority(), "residency after the recall"
+        check_gpu_maps(t.c)
+        return sel_np
+
+    for rnd in range(11):
+        writeback(np.arange(B))
+        sel = recall(extra=int(seq_np[0]) if rnd == 5 else None)
+        if rnd == 7:
+            # a second recall in the same step: the same selection with 60 tokens per
+            # request replaced (the first one's tokens are protected now)
+            for b in range(B):
+                fresh = np.setdiff1d(np.arange(int(seq_np[b])), sel[b])
+                sel[b, :60] = rng.choice(fresh, 60, replace=False)
+            recall(sel_np=sel)
+        if rnd == 8:
+            n = torch.tensor([40], dtype=torch.int32, device=dev)
+            E.cache_evict(t.c, n)
+            torch.cuda.synchronize()
+            oc.evict(oc.lru_victims(40 - oc.n_free()))
+            assert gpu_residency(t.c) == oc.resident_priority()
+        if rnd == 9:
+            writeback(np.array([1, 3, 4]))                     # a subset of the requests
+            recall()
+    # round 0 is cold, round 1 has free slots: full path; once the pool is full the
+    # write-back takes the list, except after the eviction of round 8
+    assert path[0] == 0 and path[1] == 0
+    assert all(p == 1 for p in path[2:9]), path
+    assert path[9] == 0, "the eviction must drop the list"
+    assert path[10] == 1 and path[11] == 1, path
+    # the oracle's victims of a write-back are the list's: the last write-back evicted B
+    assert int(t.c.counters[13].item()) == B
+
+
 # ---------------------------------------------------------- status words ----
 def test_status_host_index_out_of_range():
     t = TinyLayer(8, 16)
