@@ -185,6 +185,7 @@ struct TcShared {
   uint64_t s_full, p_full, o_full, o_empty;
   uint64_t vfull[TC_VST], vempty[TC_VST];
   uint32_t tmem_base;
+  int fail;                                // set when a bounded wait gave up
   int32_t slots[TC_T];
   uint32_t vmask[TC_T / 32];
   float mpart[2][128], lpart[2][128];      // per head: max and sum of each half of the columns
@@ -224,6 +225,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       mbar_init(&S.vfull[i], 128);
       mbar_init(&S.vempty[i], 1);
     }
+    S.fail = 0;
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, 256);
     mbar_init(&S.o_full, 1);
@@ -458,20 +460,23 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       if (tc == NV2 - 1) mma_commit(&S.o_full);
     }
   }
-  if (!ok && tid == 0) {
-    // a bounded wait gave up: poison this split so the combine skips it
-  }
+  if (!ok) S.fail = 1;                                // a bounded wait gave up
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 4) tmem_dealloc(tmem, 256);
+  if (S.fail && tid < 128) {
+    // this split's partial is not valid: the combine skips a split whose max is -inf
+    part.ml[(((int64_t)b * nsplit + s) * 128 + tid) * 2 + 0] = -INFINITY;
+    part.ml[(((int64_t)b * nsplit + s) * 128 + tid) * 2 + 1] = 0.f;
+  }
 }
 
 // Merge the bf16 partials of one (request, head) in split order.  A block of 256
 // threads covers 4 heads; each thread produces 8 consecutive output dims.
 template <int NSMAX>
 __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int nsplit, __nv_bfloat16 *out,
-                                                             float *lse) {
+                                                             float *lse, int drop) {
   // block: two groups of 8 dims (j) x 128 heads; warp w: heads 32 (w & 3) + lane of group
   // j = 2 blockIdx.x + (w >> 2), so every load of a partial is a contiguous 512-byte run
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -524,6 +529,18 @@ __global__ void __launch_bounds__(256) mla_tc_combine_kernel(TcPart part, int ns
   *reinterpret_cast<uint4 *>(out + ((int64_t)b * 128 + h) * V_W + 8 * j) = o;
   // the per-split logits are scaled, so M and lse are in logit units
   if (j == 0) lse[(int64_t)b * 128 + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
+  if (drop) {
+    // The partials are dead once merged: their L2 lines are dropped without being
+    // written back, so the next kernels' streams do not pay for evicting them.  Each
+    // split's chunks of this warp are 512 contiguous bytes (4 lines), read only here;
+    // lane i drops line i & 3 of splits (i >> 2), (i >> 2) + 8, ...
+    __syncwarp();
+    const __nv_bfloat16 *p0 = po - lane * 8;
+    for (int s = lane >> 2; s < nsplit; s += 8) {
+      const __nv_bfloat16 *line = p0 + (int64_t)s * 64 * 128 * 8 + (lane & 3) * 64;
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+    }
+  }
 }
 
 // Q as a 2-D bf16 tensor [rows, 576] with a [128 rows x 64 dims] box, 128-byte swizzle.
@@ -592,7 +609,9 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
     mla_tc_kernel<<<dim3(ns, B), TC_THREADS, TC_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
                                                             scale, tp);
     ECHO_LAUNCH_OK();
-    mla_tc_combine_kernel<8><<<dim3(32, B), 256, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse);
+    // the partials' lines are dropped after the merge when they are whole lines
+    const int drop = (reinterpret_cast<uintptr_t>(workspace) & 127) == 0;
+    mla_tc_combine_kernel<8><<<dim3(32, B), 256, 0, st>>>(tp, ns, (__nv_bfloat16 *)out, lse, drop);
   } else {
     return ECHO_ERR_UNSUPPORTED;
   }
