@@ -380,8 +380,8 @@ def mla(q, kv, idx, scale):
     return out, lse
 
 
-# bf16 k = 2048 / 600 / 300: 8 / 3 / 2 splits merged inside the launch (one cluster per
-# request); k = 2600: 11 splits, merged by the separate combine kernel
+# bf16 k = 2048 / 600 / 300 / 2600: 8 / 3 / 2 / 11 splits of 256 entries (the combine
+# takes its register path up to 8 splits and its loop beyond)
 @pytest.mark.parametrize("dtype,Hq,k", [(torch.bfloat16, 128, 2048), (torch.bfloat16, 128, 300),
                                         (torch.bfloat16, 128, 600), (torch.bfloat16, 128, 2600),
                                         (torch.float32, 16, 256), (torch.float32, 16, 77)])
