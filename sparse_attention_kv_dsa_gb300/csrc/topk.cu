@@ -10,9 +10,10 @@
 // One thread-block cluster (8 CTAs x 512 threads, two CTAs per SM) per request.  Each CTA holds the
 // order-preserving uint32 keys of a contiguous slice of the request's scores in
 // shared memory.  A first pass histograms a window of keys around the key of the EMA
-// threshold (the predicted k-th score); when the k-th key falls inside, one more
-// 11-bit pass finds the k-th largest key K*, otherwise an MSB-first radix select
-// (11 + 11 + 10 bit digits) does.  Each CTA histograms its slice and reads the other
+// threshold (the predicted k-th score) and lists, per warp and in token order, every
+// key from the window up; when the k-th key falls inside, one more 11-bit pass over
+// those lists finds the k-th largest key K* and the output is written from them,
+// otherwise an MSB-first radix select over every key (11 + 11 + 10 bit digits) does.  Each CTA histograms its slice and reads the other
 // CTAs' histograms through distributed shared memory, so every CTA derives the same
 // digit with no broadcast step.  Output: every key > K*, then the tokens equal to
 // K* with the lowest indices (ranks ordered across warps and CTAs), so ties go to
@@ -41,8 +42,10 @@ struct TkShared {
   uint32_t hist[2][TK_BINS];
   uint32_t warp_sums[32];
   uint32_t res[4];
-  uint32_t cta_cnt[2];                  // [0] keys > K* (window pass: above the window), [1] keys == K*
+  uint32_t cta_cnt[2];                  // [0] keys > K* (window pass: above the window, bit 31: a
+                                        // warp's candidate list overflowed), [1] keys == K*
   uint32_t warp_gt[TK_WARPS], warp_eq[TK_WARPS];
+  uint32_t warp_nl[TK_WARPS];           // candidate list lengths
   uint32_t minkey;
 };
 
@@ -80,7 +83,7 @@ __device__ __forceinline__ float ema(float theta, float kth, float alpha) {
 
 __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
-                float *theta, float alpha, const __grid_constant__ PfFix F) {
+                float *theta, float alpha, int lcap, const __grid_constant__ PfFix F) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char dsm[];
@@ -96,7 +99,11 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   const int t0 = min(L, (int)rank * per), t1 = min(L, t0 + per);
   const int n = t1 - t0;
   // keys live in shared memory when the slice for Lmax fits (that is what was allocated)
-  const bool cached = (((Lmax + TK_CL - 1) / TK_CL + 3) & ~3) <= TK_KEYCAP;
+  const int per_max = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
+  const bool cached = per_max <= TK_KEYCAP;
+  // per-warp candidate lists (token, key) after the keys: lcap entries per warp
+  int32_t *list_t = reinterpret_cast<int32_t *>(keys + (cached ? per_max : 0));
+  uint32_t *list_k = reinterpret_cast<uint32_t *>(list_t + TK_WARPS * lcap);
   // the threshold the indexer scored against, read before rank 0 updates it
   const float theta_scored = (F.cap != nullptr && rank == 0) ? theta[b] : 0.f;
 
@@ -143,12 +150,18 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
 
   // ---- window pass around the predicted k-th key ----------------------------
   // The EMA threshold theta[b] predicts this step's k-th score.  One pass counts the
-  // keys above a window of 2^22 key values around it and histograms the window's
-  // keys in 2048 bins of 2048 values.  When the k-th key falls in the window, one
-  // more 11-bit pass finishes the select; otherwise the full radix select runs.
-  // Either way the result is the exact k-th key.
+  // keys above a window of 2^22 key values around it, histograms the window's keys in
+  // 2048 bins of 2048 values, and lists every key from the window up (token, key) per
+  // warp, in token order (warp w owns a contiguous part of the slice).  When the k-th
+  // key falls in the window and no list overflowed, the last 11-bit pass and the
+  // output read only the lists; otherwise the passes read every key.  Either way the
+  // result is the exact k-th key.
+  const int wspan = (n + TK_WARPS - 1) / TK_WARPS;
+  const int s0 = min(n, warp * wspan), s1 = min(n, s0 + wspan);
   uint32_t prefix = 0, above = 0;
   int left = 32, buf = 0;
+  bool use_list = false;
+  uint32_t nl = 0;                                         // this warp's list length
   const float th_pred = theta[b];
   if (isfinite(th_pred)) {                                // uniform across the cluster
     const uint32_t kt = f32_key(th_pred);
@@ -158,23 +171,42 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
     __syncthreads();
     uint32_t nab = 0;
-    for (int base = 0; base < n; base += TK_THREADS) {     // uniform trip count per warp
-      const int i = base + tid;
+    int32_t *lt = list_t + warp * lcap;
+    uint32_t *lk = list_k + warp * lcap;
+    for (int i0 = s0; i0 < s1; i0 += 32) {                // warp-uniform trip count
+      const int i = i0 + lane;
       uint32_t kk = 0;
-      if (i < n) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
-      nab += __popc(__ballot_sync(0xffffffffu, i < n && (uint64_t)kk >= whi));
-      if (i < n && kk >= wlo && (uint64_t)kk < whi) atomicAdd(&h[(kk - wlo) >> 11], 1u);
+      if (i < s1) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+      const bool ab = i < s1 && (uint64_t)kk >= whi;
+      const bool inw = i < s1 && kk >= wlo && (uint64_t)kk < whi;
+      nab += __popc(__ballot_sync(0xffffffffu, ab));
+      if (inw) atomicAdd(&h[(kk - wlo) >> 11], 1u);
+      const uint32_t bal = __ballot_sync(0xffffffffu, ab || inw);
+      if (ab || inw) {
+        const uint32_t pos = nl + __popc(bal & lanemask_lt());
+        if (pos < (uint32_t)lcap) {
+          lt[pos] = t0 + i;
+          lk[pos] = kk;
+        }
+      }
+      nl += __popc(bal);
     }
-    if (lane == 0) S.warp_gt[warp] = nab;
+    if (lane == 0) {
+      S.warp_gt[warp] = nab;
+      S.warp_nl[warp] = nl;
+    }
     __syncthreads();
     if (tid == 0) {
-      uint32_t t = 0;
-      for (int w = 0; w < TK_WARPS; ++w) t += S.warp_gt[w];
-      S.cta_cnt[0] = t;
+      uint32_t t = 0, ovf = 0;
+      for (int w = 0; w < TK_WARPS; ++w) {
+        t += S.warp_gt[w];
+        ovf |= S.warp_nl[w] > (uint32_t)lcap ? 1u : 0u;
+      }
+      S.cta_cnt[0] = t | (ovf << 31);                      // counts stay below 2^31
     }
     __syncthreads();
     cluster_sync();
-    uint32_t tab = 0;                                      // keys above the window
+    uint32_t tab = 0, ovf = 0;                             // keys above the window; any overflow
     uint32_t c[TK_BPT];
 #pragma unroll
     for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
@@ -188,7 +220,8 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       }
 #pragma unroll
       for (uint32_t r = 0; r < TK_CL; ++r) {
-        tab += ab[r];
+        tab += ab[r] & 0x7fffffffu;
+        ovf |= ab[r] >> 31;
         c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w;
       }
     }
@@ -206,9 +239,108 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       prefix = wlo + (S.res[0] << 11);
       above = tab + S.res[1];
       left = 11;
+      use_list = lcap > 0 && ovf == 0;                     // uniform: every CTA read every flag
     }
     buf = 1;                        // other CTAs may still read hist[0]
     __syncthreads();
+  }
+
+  if (use_list) {
+    // ---- last 11-bit pass over the lists: the keys of the chosen window bin ----
+    uint32_t *h = S.hist[buf];
+    for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
+    __syncthreads();
+    const uint32_t *lk = list_k + warp * lcap;
+    const int32_t *lt = list_t + warp * lcap;
+    for (uint32_t j0 = 0; j0 < nl; j0 += 32) {              // warp-uniform trip count
+      const uint32_t j = j0 + lane;
+      const uint32_t kk = j < nl ? lk[j] : 0u;
+      hist_add_warp(h, j < nl && (kk >> 11) == (prefix >> 11), kk & 2047u);   // one bin's keys: ties are common
+    }
+    __syncthreads();
+    cluster_sync();
+    {
+      uint32_t c[TK_BPT];
+#pragma unroll
+      for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
+      uint4 v[TK_CL];
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) { c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w; }
+      uint32_t tot;
+      const uint32_t incl = tk_block_scan(c[0] + c[1] + c[2] + c[3], S.warp_sums, &tot);
+      uint32_t sfx = tot - incl;
+      const uint32_t need = (uint32_t)k - above;
+#pragma unroll
+      for (int j = TK_BPT - 1; j >= 0; --j) {
+        if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
+        sfx += c[j];
+      }
+      __syncthreads();
+      prefix |= S.res[0];
+      above += S.res[1];
+    }
+    const uint32_t kstar = prefix;
+    const uint32_t need_eq = (uint32_t)k - above;
+    // ---- ordered output from the lists (every key >= K* is listed) ----
+    uint32_t gt = 0, eq = 0;
+    for (uint32_t j0 = 0; j0 < nl; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint32_t kk = j < nl ? lk[j] : 0u;
+      gt += __popc(__ballot_sync(0xffffffffu, j < nl && kk > kstar));
+      eq += __popc(__ballot_sync(0xffffffffu, j < nl && kk == kstar));
+    }
+    if (lane == 0) { S.warp_gt[warp] = gt; S.warp_eq[warp] = eq; }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t a = 0, e = 0;
+      for (int w = 0; w < TK_WARPS; ++w) {
+        const uint32_t g = S.warp_gt[w], q = S.warp_eq[w];
+        S.warp_gt[w] = a;
+        S.warp_eq[w] = e;
+        a += g;
+        e += q;
+      }
+      S.cta_cnt[0] = a;
+      S.cta_cnt[1] = e;
+    }
+    __syncthreads();
+    cluster_sync();
+    uint32_t gt_base = 0, eq_base = 0;
+    {
+      uint32_t g[TK_CL], e[TK_CL];
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) {
+        g[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r)) : 0u;
+        e[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r)) : 0u;
+      }
+#pragma unroll
+      for (uint32_t r = 0; r < TK_CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
+    }
+    uint32_t gpos = gt_base + S.warp_gt[warp];
+    uint32_t epos = eq_base + S.warp_eq[warp];
+    for (uint32_t j0 = 0; j0 < nl; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint32_t kk = j < nl ? lk[j] : 0u;
+      const bool isg = j < nl && kk > kstar, ise = j < nl && kk == kstar;
+      const uint32_t bg = __ballot_sync(0xffffffffu, isg), be = __ballot_sync(0xffffffffu, ise);
+      if (isg) out[gpos + __popc(bg & lanemask_lt())] = lt[j];
+      if (ise) {
+        const uint32_t er = epos + __popc(be & lanemask_lt());
+        if (er < need_eq) out[above + er] = lt[j];
+      }
+      gpos += __popc(bg);
+      epos += __popc(be);
+    }
+    if (rank == 0 && tid == 0) {
+      const float kv = key_f32(kstar);
+      kth_out[b] = kv;
+      theta[b] = ema(theta[b], kv, alpha);
+    }
+    cluster_sync();
+    if (F.cap != nullptr && rank == 0) pf_fixup_block(F, b, theta_scored, *reinterpret_cast<PfFixSmem *>(dsm));
+    return;
   }
 
   // ---- radix select of the k-th largest key -----------------------------
@@ -260,8 +392,6 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
 
   // ---- ordered output ---------------------------------------------------
   // warp w of this CTA owns the contiguous sub-range [s0, s1) of the slice
-  const int wspan = (n + TK_WARPS - 1) / TK_WARPS;
-  const int s0 = min(n, warp * wspan), s1 = min(n, s0 + wspan);
   uint32_t gt = 0, eq = 0;
   for (int i0 = s0; i0 < s1; i0 += 32) {
     const int i = i0 + lane;
@@ -323,10 +453,30 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   if (F.cap != nullptr && rank == 0) pf_fixup_block(F, b, theta_scored, *reinterpret_cast<PfFixSmem *>(dsm));
 }
 
-static size_t topk_smem(int Lmax, bool fix) {
+// Entries per warp of the candidate lists: as many as fit (up to 256) while two CTAs
+// still share an SM; 0 (no lists) when fewer than 64 fit.
+static int topk_lcap(int Lmax) {
+  static int per_sm = 0, reserved = 0;
+  if (!per_sm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (per_sm <= 0) per_sm = 1;
+  }
+  const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
+  const long base = (long)((sizeof(TkShared) + 15) & ~size_t(15)) + (per <= TK_KEYCAP ? (long)per * 4 : 0);
+  const long room = (long)per_sm / 2 - reserved - base;
+  if (room <= 0) return 0;
+  const int lc = (int)std::min<long>(256, room / (TK_WARPS * 8)) & ~31;
+  return lc >= 64 ? lc : 0;
+}
+
+static size_t topk_smem(int Lmax, int lcap, bool fix) {
   const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
   size_t s = (sizeof(TkShared) + 15) & ~size_t(15);
   if (per <= TK_KEYCAP) s += (size_t)per * 4;
+  s += (size_t)TK_WARPS * lcap * 8;
   if (fix) s = std::max(s, sizeof(PfFixSmem));
   return s;
 }
@@ -336,10 +486,11 @@ static echo_status_t launch_topk(const float *scores, const int32_t *seq_len, in
                                  echo_stream_t stream) {
   if (!scores || !seq_len || !out_idx || !kth || !theta || B <= 0 || Lmax <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
   if (!(alpha >= 0.f && alpha <= 1.f)) return ECHO_ERR_INVALID_ARG;
-  const size_t smem = topk_smem(Lmax, F.cap != nullptr);
+  const int lcap = topk_lcap(Lmax);
+  const size_t smem = topk_smem(Lmax, lcap, F.cap != nullptr);
   ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   topk_kernel<<<B * TK_CL, TK_THREADS, smem, (cudaStream_t)stream>>>(scores, seq_len, Lmax, k, out_idx, kth, theta,
-                                                                     alpha, F);
+                                                                     alpha, lcap, F);
   ECHO_LAUNCH_OK();
   return ECHO_OK;
 }

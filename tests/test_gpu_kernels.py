@@ -143,6 +143,19 @@ def test_topk_many_rows():
     check_topk(lists, k, thetas)
 
 
+def test_topk_candidate_lists_and_their_fallbacks():
+    # a prediction near the k-th score: the last pass and the output read the per-warp
+    # candidate lists; ties at the k-th key spread over every warp and CTA; a window
+    # that holds nearly every key overflows the lists and falls back to full passes
+    rng = np.random.default_rng(6)
+    L = 100_000
+    a = (rng.integers(0, 2 ** 14, L) / 1024.0).astype(np.float32)          # k-th near 15.7
+    b = rng.choice(np.array([0.0, 1.0, 2.0], np.float32), L, p=[0.6, 0.35, 0.05])   # ~5000 twos
+    c = (2.5 + rng.integers(-8, 8, L) / 4096.0).astype(np.float32)         # all in the window
+    # windows above and below the k-th key: full passes
+    check_topk([a, b, c, a, a], 2048, [15.6, 2.0, 2.5, 60.0, 1.0])
+
+
 def test_topk_large_context_k2048():
     rng = np.random.default_rng(1)
     lists = [(rng.integers(0, 2 ** 14, 100_000) / 1024.0).astype(np.float32) for _ in range(3)]
