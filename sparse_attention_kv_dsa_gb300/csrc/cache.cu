@@ -28,7 +28,10 @@
 //                   then the data: write-back of the new token (A1), or the recall's
 //                   zero-copy host reads and staged rows into slots plus the slot
 //                   translation (A9 + A10).
-//                   Modes: write-back, recall, alloc, evict.
+//                   Modes: write-back, recall, alloc, evict.  A recall also ranks the
+//                   next write-back's victims (the pending list).
+//   wb_fast_kernel  one CTA: the write-back from the pending list, launched before the
+//                   cooperative write-back, which then returns at once if it was done
 
 #include <algorithm>
 
