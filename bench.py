@@ -447,6 +447,10 @@ def run_echo(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # the stream first spins ~1 ms per timed step, so the host has queued every step
+        # before ev0: the events time the device's work, not the host's issue rate
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e6) * args.steps)
         ev0.record(stream)
         run_pipelined(s_idx, args.steps, from_host=False)
         stream.wait_stream(cs)
