@@ -159,30 +159,37 @@ static int mla_splits(int k) { return (k + MS_SPLIT - 1) / MS_SPLIT; }
 //   phase 1  S[128 x 256] = Q . C^T over nine 64-dim chunks: Q chunk by TMA,
 //            gathered C chunk by cp.async into the 128-byte-swizzled K-major
 //            layout; tcgen05.mma kind::f16 M=128 N=256 K=16, f32 in TMEM.
-//   softmax  one thread per head row reads its 256 logits from TMEM, writes bf16
-//            probabilities P[128 x 256] to shared memory (K-major, swizzled).
-//   phase 2  for each half of the 512 value dims: O[128 x 256] = P . V with V
-//            chunks of 32 rows x 256 dims as MN-major operands; the epilogue
-//            writes O / l as bf16 partials, plus (m, l) per head.
-// Warps 0-3 load (cp.async), run the softmax and the epilogues; warp 4 issues the
-// MMAs from one thread.  256 TMEM columns and ~100 KB shared memory per CTA: two
-// CTAs per SM overlap each other's phases.
+//   softmax  one thread per head row and half of the columns reads its logits
+//            from TMEM and writes the bf16 probabilities P back into TMEM over
+//            the logits it has read (tokens 0-127 -> columns 0-63, 128-255 ->
+//            columns 128-191; two per 32-bit column).
+//   phase 2  O = P . V in eight blocks of 64 value dims: the MMA takes P from
+//            TMEM and a 64-token x 64-dim V stage (MN-major) from shared memory,
+//            accumulating into one of two 64-column TMEM buffers (columns 64-127
+//            and 192-255), so block j's epilogue overlaps block j+1's MMAs; the
+//            whole phase-1 region is a 12-stage V ring (96 KB in flight).
+//            The epilogue writes O / l as bf16 partials, plus (m, l) per head.
+// Warps 0-3 load (cp.async), run half of the softmax and the epilogues; warps 5-8
+// the other half of the softmax; warp 4 issues the MMAs from one thread.  256 TMEM
+// columns and ~100 KB shared memory per CTA: two CTAs per SM overlap each other's
+// phases.
 constexpr int TC_T = 256;                 // selected entries per CTA
 constexpr int TC_THREADS = 288;         // warps 0-3 loads/softmax/epilogue, 4 MMA, 5-8 softmax
 constexpr int TC_QCH = 128 * 128;         // Q chunk bytes (128 heads x 64 dims)
 constexpr int TC_KCH = TC_T * 128;        // C chunk bytes (256 rows x 64 dims)
 constexpr int TC_STAGE = TC_QCH + TC_KCH; // 48 KB
-constexpr int TC_VROWS = 16;              // rows per V chunk (one K-step)
-constexpr int TC_VCH = TC_VROWS * 512;    // V chunk bytes (16 rows x 256 dims)
-constexpr int TC_VST = 4;                 // V ring stages
-constexpr int TC_NV = 2 * TC_T / TC_VROWS; // V chunks per CTA (two halves)
-constexpr int TC_P = 128 * TC_T * 2;      // 64 KB
-constexpr int TC_REGION = 2 * TC_STAGE;   // 96 KB, phase 1 ring / (P + V ring)
-static_assert(TC_P + TC_VST * TC_VCH <= TC_REGION, "P and the V ring share the phase-1 region");
+constexpr int TC_VROWS = 64;              // tokens per V stage (four K-steps)
+constexpr int TC_VCH = TC_VROWS * 128;    // V stage bytes (64 tokens x 64 dims)
+constexpr int TC_VST = 12;                // V ring stages
+constexpr int TC_SPB = TC_T / TC_VROWS;   // stages per 64-dim output block (4)
+constexpr int TC_NV = 8 * TC_SPB;         // V stages per CTA (eight blocks)
+constexpr int TC_REGION = 2 * TC_STAGE;   // 96 KB, phase 1 ring / V ring
+static_assert(TC_VST * TC_VCH <= TC_REGION, "the V ring reuses the phase-1 region");
+static_assert(TC_VST - 2 <= 10, "cp_async_wait_upto covers the ring");
 
 struct TcShared {
   uint64_t full[2], empty[2], qfull[2];
-  uint64_t s_full, p_full, o_full, o_empty;
+  uint64_t s_full, p_full, o_full[2], o_empty[2];
   uint64_t vfull[TC_VST], vempty[TC_VST];
   uint32_t tmem_base;
   int fail;                                // set when a bounded wait gave up
@@ -197,6 +204,46 @@ struct TcPart {
   float *ml;          // [B, S, 128, 2]
 };
 
+// TMEM column of the bf16 pair holding tokens t, t+1 of P (t even)
+__device__ __forceinline__ uint32_t p_col(int t) { return (uint32_t)((t >> 1) + (t >= TC_T / 2 ? TC_T / 4 : 0)); }
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// tcgen05.mma kind::f16 with A (M x 16) read from TMEM at a_tmem
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// Wait until at most n (0..10) of this thread's cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    case 8: cp_async_wait<8>(); break;
+    case 9: cp_async_wait<9>(); break;
+    default: cp_async_wait<10>(); break;
+  }
+}
+
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
   // byte offset of 16-byte chunk `chunk16` of row `row` in a 128B-swizzled
   // K-major tile whose rows are 128 bytes apart
@@ -209,8 +256,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   extern __shared__ unsigned char tc_raw[];
   unsigned char *R = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
   TcShared &S = *reinterpret_cast<TcShared *>(R + TC_REGION);
-  unsigned char *P = R;                       // phase 2: probabilities
-  unsigned char *V = R + TC_P;                // phase 2: V ring (2 x 16 KB)
+  unsigned char *V = R;                       // phase 2: V ring (12 x 8 KB)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, b = blockIdx.y, nsplit = gridDim.x;
   const int j0 = s * TC_T;
@@ -228,8 +274,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     S.fail = 0;
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, 256);
-    mbar_init(&S.o_full, 1);
-    mbar_init(&S.o_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.o_full[i], 1);
+      mbar_init(&S.o_empty[i], 128);
+    }
     fence_mbar_init();
   }
   for (int i = tid; i < TC_T; i += TC_THREADS) {
@@ -278,7 +326,8 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
     const float mc = m * c2;
     float l = 0.f;
-    // 32 probabilities -> bf16 -> four 16-byte chunks of P (half an atom column)
+    // 32 probabilities -> 16 bf16 pairs -> 16 TMEM columns of this row, over logits
+    // this thread has already read (p_col(c0) < c0 within its half)
     auto write_p = [&](int c0, const uint32_t (&r)[32], uint32_t vm) {
       uint32_t pk[16];
 #pragma unroll
@@ -289,13 +338,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
         pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
       }
-      unsigned char *pa = P + (c0 >> 6) * (128 * 128);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int ch = ((c0 & 63) >> 3) + q;
-        *reinterpret_cast<uint4 *>(pa + sw128(hr, ch)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                                                                    pk[4 * q + 3]);
-      }
+      tmem_st16(tr + p_col(c0), pk);
     };
     for (int c0 = cb; c0 < ce; c0 += 64) {       // two TMEM loads per wait
       uint32_t r[32], r2[32];
@@ -305,7 +348,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
       write_p(c0, r, vmask[c0 >> 5]);
       write_p(c0 + 32, r2, vmask[(c0 >> 5) + 1]);
     }
-    fence_proxy_async_smem();
+    tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&S.p_full);
     S.lpart[half][hr] = l;
@@ -347,19 +390,17 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     // ------------------------------------------------------ softmax --
     if (!mbar_wait(&S.s_full, 0)) ok = false;
     tc_fence_after();
-    // V loads of the first chunks can start: phase 1 no longer reads smem
-    constexpr int NV2 = TC_NV / 2;                     // chunks per half
-    auto load_v = [&](int vc) {                        // half vc / NV2, rows (vc % NV2) * 16
-      const int st = vc % TC_VST, hf = vc / NV2, r0 = (vc % NV2) * TC_VROWS;
+    // V loads of the first stages can start: phase 1 no longer reads smem
+    auto load_v = [&](int vc) {                        // block vc / TC_SPB, tokens (vc % TC_SPB) * 64
+      const int st = vc % TC_VST, j = vc / TC_SPB, r0 = (vc % TC_SPB) * TC_VROWS;
       unsigned char *vb = V + st * TC_VCH;
 #pragma unroll
-      for (int i = 0; i < TC_VROWS * 32 / 128; ++i) {
-        const int idx = tid + 128 * i;                 // rows x 32 chunks of 16 B
-        const int r = idx >> 5, cc = idx & 31;         // chunk cc: dims hf*256 + cc*8
-        const int ac = cc >> 3, c = cc & 7;
+      for (int i = 0; i < TC_VROWS * 8 / 128; ++i) {
+        const int idx = tid + 128 * i;                 // rows x 8 chunks of 16 B (64 dims)
+        const int r = idx >> 3, c = idx & 7;
         const int32_t g = S.slots[r0 + r];
-        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + hf * 256 + cc * 8;
-        cp_async_16(vb + ac * (TC_VROWS * 128) + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
+        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + j * 64 + c * 8;
+        cp_async_16(vb + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
       }
       cp_async_commit();
     };
@@ -370,54 +411,53 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     softmax_half(0, m, l);
 
     // ------------------------------------------- phase 2 loads + epilogue --
+    // epilogue of 64-dim block j: O / l from its TMEM buffer to bf16 partials, stored
+    // in groups of 8 dims with heads innermost ([b][s][dim/8][head][8]), so the 32
+    // heads of a warp write one contiguous 512-byte run per store
+    auto epilogue = [&](int j) {
+      if (!mbar_wait(&S.o_full[j & 1], (j >> 1) & 1)) ok = false;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + j * 8) * 128 * 8 + (int64_t)h * 8;
+      uint32_t r[32], r2[32];
+      const uint32_t ob = trow + ((j & 1) ? 192u : 64u);
+      tmem_ld32(ob, r);
+      tmem_ld32(ob + 32, r2);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&S.o_empty[j & 1]);                  // the values are in registers
+      auto store_o = [&](int c0, const uint32_t (&v)[32]) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[q]) * inv, __uint_as_float(v[q + 1]) * inv);
+          pk[q >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)                    // dims 64 j + c0 + 8q .. + 7
+          *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      };
+      store_o(0, r);
+      store_o(32, r2);
+    };
     for (int vc = 0; vc < TC_NV; ++vc) {
-      // chunk vc was issued earlier; wait for it (later groups may stay in flight)
-      // groups issued after chunk vc so far: chunks vc+1 .. vc+TC_VST-2 (refills lag one iteration)
-      const int later = max(0, min(TC_VST - 2, TC_NV - 1 - vc));
-      if (later >= 3) cp_async_wait<3>(); else if (later == 2) cp_async_wait<2>();
-      else if (later == 1) cp_async_wait<1>(); else cp_async_wait<0>();
+      // stage vc was issued earlier; wait for it (later groups may stay in flight):
+      // groups issued after stage vc so far: vc+1 .. vc+TC_VST-2 (refills lag one iteration)
+      cp_async_wait_upto(max(0, min(TC_VST - 2, TC_NV - 1 - vc)));
       fence_proxy_async_smem();
       mbar_arrive(&S.vfull[vc % TC_VST]);
-      // refill the buffer of the chunk delivered one iteration ago (likely consumed
+      // refill the buffer of the stage delivered one iteration ago (likely consumed
       // by now), not the one just delivered: the other stages stay in flight
       if (vc >= 1 && vc - 1 + TC_VST < TC_NV) {
         const int pv = vc - 1;
         if (!mbar_wait(&S.vempty[pv % TC_VST], (pv / TC_VST) & 1)) { ok = false; }
         load_v(pv + TC_VST);
       }
-      if ((vc % NV2) == NV2 - 1) {
-        // epilogue of half vc / NV2
-        const int hf = vc / NV2;
-        if (!mbar_wait(&S.o_full, hf & 1)) ok = false;
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        // partials are stored in groups of 8 dims, heads innermost: [b][s][dim/8][head][8], so
-        // the 32 heads of a warp write one contiguous 512-byte run per store
-        __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + hf * 32) * 128 * 8 + (int64_t)h * 8;
-        auto store_o = [&](int c0, const uint32_t (&r)[32]) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-            pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)                      // dims c0 + 8q .. c0 + 8q + 7 of this half
-            *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        };
-        for (int c0 = 0; c0 < 256; c0 += 64) {             // two TMEM loads per wait
-          uint32_t r[32], r2[32];
-          tmem_ld32(trow + c0, r);
-          tmem_ld32(trow + c0 + 32, r2);
-          tmem_wait_ld();
-          store_o(c0, r);
-          store_o(c0 + 32, r2);
-        }
-        tc_fence_before();
-        mbar_arrive(&S.o_empty);
-      }
+      // block j = vc / TC_SPB is delivered: write out the block before it
+      if (vc % TC_SPB == TC_SPB - 1 && vc >= TC_SPB) epilogue(vc / TC_SPB - 1);
     }
+    epilogue(TC_NV / TC_SPB - 1);
     part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
     part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1] = l;
   } else if (warp > 4) {
@@ -429,7 +469,6 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   } else if (lane == 0) {
     // ------------------------------------------------------------- MMA --
     constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, TC_T);
-    constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 256);
     for (int dc = 0; dc < 9 && ok; ++dc) {
       const int st = dc & 1;
       if (!mbar_wait(&S.qfull[st], (dc >> 1) & 1) || !mbar_wait(&S.full[st], (dc >> 1) & 1)) { ok = false; break; }
@@ -443,21 +482,27 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     mma_commit(&S.s_full);
     if (ok && !mbar_wait(&S.p_full, 0)) ok = false;
     tc_fence_after();
-    constexpr int NV2 = TC_NV / 2;
-    for (int vc = 0; vc < TC_NV && ok; ++vc) {
-      const int st = vc % TC_VST, hf = vc / NV2, tc = vc % NV2;
-      if (tc == 0 && hf == 1) {                          // O columns reused: wait for the first epilogue
-        if (!mbar_wait(&S.o_empty, 0)) { ok = false; break; }
+    // block j: O_j[128 x 64] = P[128 x 256] . V[256 x 64 dims of block j]; P from TMEM
+    constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 64);
+    for (int j = 0; j < TC_NV / TC_SPB && ok; ++j) {
+      if (j >= 2) {                                    // this buffer's previous block is written out
+        if (!mbar_wait(&S.o_empty[j & 1], ((j >> 1) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
       }
-      if (!mbar_wait(&S.vfull[st], (vc / TC_VST) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const int t0 = tc * TC_VROWS;                      // token offset in P (one K-step)
-      const uint64_t ad = smem_desc(smem_u32(P + (t0 >> 6) * (128 * 128) + (t0 & 63) * 2), 16, 1024, LAYOUT_SW128);
-      const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH), TC_VROWS * 128, 1024, LAYOUT_SW128);
-      mma_f16(tmem, ad, bd, id2, tc ? 1u : 0u);
-      mma_commit(&S.vempty[st]);
-      if (tc == NV2 - 1) mma_commit(&S.o_full);
+      const uint32_t d = tmem + ((j & 1) ? 192u : 64u);
+      for (int s4 = 0; s4 < TC_SPB && ok; ++s4) {
+        const int vc = j * TC_SPB + s4, st = vc % TC_VST;
+        if (!mbar_wait(&S.vfull[st], (vc / TC_VST) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TC_VROWS / 16; ++kk) {
+          const int t0 = s4 * TC_VROWS + kk * 16;      // tokens of this K-step
+          const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH + kk * 16 * 128), TC_VCH, 1024, LAYOUT_SW128);
+          mma_f16_ts(d, tmem + p_col(t0), bd, id2, (s4 | kk) ? 1u : 0u);
+        }
+        mma_commit(&S.vempty[st]);
+      }
+      mma_commit(&S.o_full[j & 1]);
     }
   }
   if (!ok) S.fail = 1;                                // a bounded wait gave up
