@@ -487,21 +487,48 @@ def run_echo(args, ws, rank, local):
     e2e_value = tokens / (e2e_ms / 1e3)
 
     # ---------------- per-stage times inside the graph (probe replays, untimed) ----------------
-    stages = {}
+    stages, telemetry = {}, None
     if not args.skip_stages and probe is not None:
         names = ["writeback", "reserve", "index_prefetch", "topk", "recall", "mla"]
         per = {n: [] for n in names}
+        tele = {"qualified": [], "staged": [], "useful": [], "final_recall": [], "theta_rel_err": []}
         for _ in range(PROBE_STEPS):
             load_inputs(s_idx, stream)
+            theta_before = [dl.theta.clone() for dl in L]       # the prediction this step scores against
             with torch.cuda.stream(stream):
                 probe.replay()
             s_idx += 1
             stream.synchronize()
             for i, n in enumerate(names):
                 per[n].append(sum(st_ev[l][i].elapsed_time(st_ev[l][i + 1]) for l in range(layers)) * 1e3 / layers)
+            for l, dl in enumerate(L):
+                c = dl.cache.read_counters()
+                tele["qualified"].append(c[E.CTR_QUALIFIED])
+                tele["staged"].append(c[E.CTR_STAGED])
+                tele["useful"].append(c[E.CTR_STAGED_HITS])
+                tele["final_recall"].append(c[E.CTR_MISSES])
+                th, kth = theta_before[l].cpu(), dl.kth.cpu()
+                ok = torch.isfinite(th) & torch.isfinite(kth) & (kth != 0)
+                if bool(ok.any()):
+                    tele["theta_rel_err"].append(float(((th[ok] - kth[ok]).abs() / kth[ok].abs()).median()))
         stages = {n + "_us": round(statistics.median(v), 2) for n, v in per.items()}
         stages["how"] = "CUDA events between the stages inside a graph of the step issued through the separate " \
                         "entry points (reserve as its own launch), median of %d steps, mean over layers" % PROBE_STEPS
+        row_bytes = 576 * (4 if wl.kv_fp32 else 2)
+        mean = lambda v: (sum(v) / len(v)) if v else None
+        telemetry = {
+            "qualified_rows": mean(tele["qualified"]),
+            "prefetched_rows": mean(tele["staged"]),
+            "prefetched_rows_selected": mean(tele["useful"]),
+            "useless_prefetch_bytes": (mean(tele["staged"]) - mean(tele["useful"])) * row_bytes if tele["staged"] else None,
+            "final_recall_rows": mean(tele["final_recall"]),
+            "final_recall_bytes": mean(tele["final_recall"]) * row_bytes if tele["final_recall"] else None,
+            "theta_rel_err_median": statistics.median(tele["theta_rel_err"]) if tele["theta_rel_err"] else None,
+            "how": "per layer and step, mean over %d probe steps x %d layers: rows above the threshold and not "
+                   "resident (before the cap), rows prefetched during scoring, "
+                   "those the exact top-k then selected, the bytes of the rest, rows recalled after the top-k; "
+                   "median over requests of |theta - kth| / |kth| (EMA prediction vs this step's k-th score)"
+                   % (PROBE_STEPS, layers)}
 
     # ---------------- roofline of the dominant kernel (indexer) ----------------
     peaks = measured_peaks()
@@ -547,6 +574,7 @@ def run_echo(args, ws, rank, local):
         "gpu_launches": launches_per_step(prefetch, wl.n_gpu) * layers * args.steps,
         "clocks": clocks,
         "stages_us": stages,
+        "prefetch_telemetry": telemetry,
         "indexer_gbs": achieved,
         "recall_gbs": recall_gbs,
         "host_link": link,

@@ -11,8 +11,8 @@
 //   "Fusing prefetch into the indexer pipeline" -- prefetch overlaps the scoring stream.
 //
 // FP8 kernel (H = 64 heads, D = 128): persistent CTAs, two per SM (two independent
-// pipelines per SM measured 1.5x faster than one CTA with deeper rings), walk the
-// 128-token tiles of every request round-robin.  Warp roles:
+// pipelines per SM measured 1.5x faster than one CTA with deeper rings), each walking
+// a contiguous range of the 128-token tiles of all requests.  Warp roles:
 //   warp 0     TMA producer: 16 KB key tiles (128 tokens x 128 B, 128-byte swizzle)
 //              through a 4-stage mbarrier ring, plus the request's q (64 x 128 B)
 //   warp 1     one thread issues tcgen05.mma kind::f8f6f4, M=128 tokens, N=64 heads,
@@ -20,7 +20,8 @@
 //   warp 2     prefetch: residency check, capped claim, zero-copy copy of the latent
 //              row from pinned host memory into the request's staging rows
 //   warps 3-6  epilogue: tcgen05.ld of a token row (64 head dot products), ReLU,
-//              weighted sum, score store; tokens above the threshold go to a ring
+//              weighted sum (packed fma.rn.f32x2, two heads per instruction), score
+//              store; tokens above the threshold go to a ring
 // On the exact grid the tensor-core sums are exact, so scores equal the definition.
 // The cap is exact: claims are optimistic (any order) and a fix-up restores "the first
 // cap tokens by ascending t" for the rare request whose qualifiers outnumber its cap,
@@ -247,6 +248,10 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const int T = S.tile_pre[P.B];
+  // this CTA's contiguous range of tiles [i0, i1): a CTA meets few requests, so it
+  // rarely reloads a query block or head weights (both stall the pipeline)
+  const int i0 = (int)(((int64_t)T * blockIdx.x) / gridDim.x);
+  const int i1 = (int)(((int64_t)T * (blockIdx.x + 1)) / gridDim.x);
   const uint32_t tmem = S.tmem_base;
   int32_t *ctr = P.L.counters;
 
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
       tma_prefetch_desc(&qmap);
       const uint64_t stream_once = l2_evict_first_policy();   // keys are read once per step
       int it = 0, qn = 0, cur = -1;
-      for (int i = blockIdx.x; i < T; i += gridDim.x, ++it) {
+      for (int i = i0; i < i1; ++i, ++it) {
         const int b = find_req(S.tile_pre, P.B, i);
         const int t0 = (i - S.tile_pre[b]) * IX_TILE;
         if (b != cur) {
@@ -284,10 +289,10 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
       constexpr uint32_t idesc = instr_desc(FMT_E4M3, FMT_E4M3, 0, 0, IX_TILE, IX_H);
       int it = 0, qn = 0, cur = -1, qs = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < T && ok;) {
+      for (int i = i0; i < i1 && ok;) {
         int st[IX_MMA_GROUP], ac[IX_MMA_GROUP], qsl[IX_MMA_GROUP];
         int n = 0, defer = -1;
-        for (; n < IX_MMA_GROUP && i < T; ++n, ++it, i += gridDim.x) {
+        for (; n < IX_MMA_GROUP && i < i1; ++n, ++it, ++i) {
           const int b = find_req(S.tile_pre, P.B, i);
           if (b != cur) {
             if (cur >= 0) {
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
     float theta = 0.f;
     int Lb = 0, cur = -1;
     int it = 0;
-    for (int i = blockIdx.x; i < T; i += gridDim.x, ++it) {
+    for (int i = i0; i < i1; ++i, ++it) {
       if (it % IX_EPI != grp) continue;
       const int b = find_req(S.tile_pre, P.B, i);
       const int t0 = (i - S.tile_pre[b]) * IX_TILE;
@@ -356,16 +361,23 @@ __global__ void __launch_bounds__(IX_THREADS, ECHO_IX_CTAS_PER_SM)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&S.tempty[acc]);
-      // four independent partial sums (every partial sum is exact on the grid)
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      // eight independent partial sums in four packed pairs (every partial sum is exact
+      // on the grid); one fma.rn.f32x2 per pair of heads
+      unsigned long long c[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int h = 0; h < 32; h += 2) {
-        a0 = fmaf(wr[h], fmaxf(__uint_as_float(r0[h]), 0.f), a0);
-        a1 = fmaf(wr[h + 1], fmaxf(__uint_as_float(r0[h + 1]), 0.f), a1);
-        a2 = fmaf(wr[32 + h], fmaxf(__uint_as_float(r1[h]), 0.f), a2);
-        a3 = fmaf(wr[33 + h], fmaxf(__uint_as_float(r1[h + 1]), 0.f), a3);
+      for (int p = 0; p < 32; ++p) {
+        const uint32_t *rr = p < 16 ? r0 : r1;
+        const int hh = 2 * (p & 15);
+        unsigned long long xv, wv;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(fmaxf(__uint_as_float(rr[hh]), 0.f)),
+            "f"(fmaxf(__uint_as_float(rr[hh + 1]), 0.f)));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(wv) : "f"(wr[2 * p]), "f"(wr[2 * p + 1]));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c[p & 3]) : "l"(wv), "l"(xv));
       }
-      const float sc = (a0 + a1) + (a2 + a3);
+      float e[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) asm("mov.b64 {%0, %1}, %2;" : "=f"(e[2 * q]), "=f"(e[2 * q + 1]) : "l"(c[q]));
+      const float sc = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
       const int t = t0 + row;
       if (t < Lb) {
         P.scores[(int64_t)b * P.Lmax + t] = sc;
