@@ -15,7 +15,8 @@
 //                         accumulators in TMEM (two 256-column buffers).  The epilogue
 //                         forms sum_h w_h ReLU(.) per (token, query), stores the causal
 //                         scores and histograms bucket(score - kth_pred) per query.
-//                         Persistent CTAs walk (query quad, range of key tiles) items.
+//                         Persistent CTAs walk contiguous runs of (query quad, range of
+//                         key tiles) items.
 //                         Warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue (two
 //                         warps per TMEM lane quadrant, two queries each).
 //   prefill_cand_kernel   one CTA per query: threshold bucket from the histogram,
@@ -125,6 +126,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  // this CTA's contiguous range of items [i0, i1): consecutive items share a query quad,
+  // so its queries, weights and histograms change rarely
+  const int i0 = (int)(((int64_t)P.nitems * blockIdx.x) / gridDim.x);
+  const int i1 = (int)(((int64_t)P.nitems * (blockIdx.x + 1)) / gridDim.x);
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       tma_prefetch_desc(&qmap);
       int it = 0, qn = 0, cur = -1;
       bool ok = true;
-      for (int i = blockIdx.x; i < P.nitems && ok; i += gridDim.x) {
+      for (int i = i0; i < i1 && ok; ++i) {
         const PfItem w = pf_item(P, i);
         if (w.ja >= w.jb) continue;
         if (w.g != cur) {
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       constexpr uint32_t idesc = instr_desc(FMT_E4M3, FMT_E4M3, 0, 0, PF_TILE, PF_N);
       int it = 0, qn = 0, cur = -1, qs = 0;
       bool ok = true;
-      for (int i = blockIdx.x; i < P.nitems && ok; i += gridDim.x) {
+      for (int i = i0; i < i1 && ok; ++i) {
         const PfItem w = pf_item(P, i);
         if (w.ja >= w.jb) continue;
         if (w.g != cur) {
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     };
     // every epilogue warp walks every item (the named barriers need all four), even
     // after a bounded wait gave up (its tiles are then skipped)
-    for (int i = blockIdx.x; i < P.nitems; i += gridDim.x) {
+    for (int i = i0; i < i1; ++i) {
       const PfItem w = pf_item(P, i);
       if (w.ja >= w.jb) continue;
       if (w.g != cur) {
