@@ -131,7 +131,11 @@ static __device__ __noinline__ void pf_fixup_block(const PfFix &P, int b, float 
       }
       warp_copy_rows4(src, dst, KV_W * esz / 16);
     }
+    // every wrongly staged token gave its row to a missing one, and the lists held them
+    // all: the staged set is the first-cap set, no rescan needed
+    const bool done = sm.n_need == sm.n_free && sm.n_need <= FX_LIST;
     __syncthreads();
+    if (done) break;
   }
   if (tid == 0) P.pf_count[b] = cap;
 }
