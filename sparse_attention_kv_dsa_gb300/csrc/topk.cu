@@ -13,9 +13,11 @@
 // threshold (the predicted k-th score) and lists, per warp and in token order, every
 // key from the window up; when the k-th key falls inside, one more 11-bit pass over
 // those lists finds the k-th largest key K* and the output is written from them,
-// otherwise an MSB-first radix select over every key (11 + 11 + 10 bit digits) does.  Each CTA histograms its slice and reads the other
-// CTAs' histograms through distributed shared memory, so every CTA derives the same
-// digit with no broadcast step.  Output: every key > K*, then the tokens equal to
+// otherwise an MSB-first radix select over every key (11 + 11 + 10 bit digits) does.
+// Each CTA histograms its slice and publishes the sums of its 32-bin groups; every CTA
+// finds a digit from the group sums of all eight, then from the 32 bins of the chosen
+// group, read through distributed shared memory, so every CTA derives the same digit
+// with no broadcast step.  Output: every key > K*, then the tokens equal to
 // K* with the lowest indices (ranks ordered across warps and CTAs), so ties go to
 // the lower token index.  The selection order is ascending t within each class.
 // echo_topk_prefetch also runs the indexer's deferred exact prefetch cap: after the
@@ -46,32 +48,76 @@ struct TkShared {
                                         // warp's candidate list overflowed), [1] keys == K*
   uint32_t warp_gt[TK_WARPS], warp_eq[TK_WARPS];
   uint32_t warp_nl[TK_WARPS];           // candidate list lengths
+  uint32_t coarse[2][TK_BINS / 32];     // sums of 32-bin groups of hist[buf] (read by the cluster)
+  uint32_t tot_s[3];                    // window pass: keys above the window, in it, any overflow
   uint32_t minkey;
 };
+static_assert(TK_BPT == 4 && TK_THREADS == TK_BINS / 4, "eight threads sum one 32-bin group");
 
-__device__ __forceinline__ uint32_t tk_block_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
-  const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= (uint32_t)o) v += n;
-  }
-  if (lane == 31) warp_sums[wid] = v;
+// This CTA's sums of 32-bin groups of its histogram h, for the other CTAs of the
+// cluster.  Every thread calls it after h is complete; ends with a barrier.
+__device__ __forceinline__ void tk_coarse(const uint32_t *h, uint32_t *coarse) {
+  const int tid = threadIdx.x;
+  const uint4 v = reinterpret_cast<const uint4 *>(h)[tid];   // bins 4 tid .. 4 tid + 3
+  uint32_t s = v.x + v.y + v.z + v.w;
+  s += __shfl_down_sync(0xffffffffu, s, 4);
+  s += __shfl_down_sync(0xffffffffu, s, 2);
+  s += __shfl_down_sync(0xffffffffu, s, 1);
+  if ((tid & 7) == 0) coarse[tid >> 3] = s;
   __syncthreads();
-  if (wid == 0) {
-    uint32_t w = lane < nw ? warp_sums[lane] : 0;
+}
+
+// The bin, over the cluster's histograms h (and their group sums), that holds the
+// need-th largest key counted from the top bin: res[0] = the bin, res[1] = keys in the
+// bins above it.  Two small rounds of remote reads by one warp: the 64 group sums of
+// every CTA, then the 32 bins of the chosen group.  Needs 1 <= need <= the keys in the
+// histograms.  Every thread calls it after the cluster barrier that follows tk_coarse;
+// ends with a barrier.
+__device__ __forceinline__ void tk_find(const uint32_t *h, const uint32_t *coarse, uint32_t need, uint32_t *res) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    // lane L holds groups 63 - 2L (the higher) and 62 - 2L
+    uint32_t a[TK_CL], c[TK_CL];
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) {
+      a[r] = ld_dsmem_u32(map_dsmem(coarse + 63 - 2 * lane, r));
+      c[r] = ld_dsmem_u32(map_dsmem(coarse + 62 - 2 * lane, r));
+    }
+    uint32_t hi = 0, lo = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) { hi += a[r]; lo += c[r]; }
+    uint32_t incl = hi + lo;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= (uint32_t)o) w += n;
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
     }
-    warp_sums[lane] = w;
+    const uint32_t ab = incl - hi - lo;                   // keys in the groups above both
+    int g = -1;
+    uint32_t gab = 0;
+    if (ab < need && need <= ab + hi) { g = 63 - 2 * lane; gab = ab; }
+    else if (ab + hi < need && need <= ab + hi + lo) { g = 62 - 2 * lane; gab = ab + hi; }
+    const uint32_t m = __ballot_sync(0xffffffffu, g >= 0);
+    const int src = m ? __ffs(m) - 1 : 0;
+    g = max(__shfl_sync(0xffffffffu, g, src), 0);
+    gab = __shfl_sync(0xffffffffu, gab, src);
+    // lane i: bin 32 g + i
+    uint32_t fv[TK_CL];
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) fv[r] = ld_dsmem_u32(map_dsmem(h + 32 * g + lane, r));
+    uint32_t f = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < TK_CL; ++r) f += fv[r];
+    uint32_t sfx = f;                                      // bins 32 g + lane .. 32 g + 31
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_down_sync(0xffffffffu, sfx, o);
+      if (lane + o < 32) sfx += x;
+    }
+    const uint32_t above = gab + sfx - f;
+    if (above < need && need <= above + f) { res[0] = 32 * g + lane; res[1] = above; }
   }
   __syncthreads();
-  if (wid > 0) v += warp_sums[wid - 1];
-  *total = warp_sums[nw - 1];
-  __syncthreads();
-  return v;
 }
 
 __device__ __forceinline__ float ema(float theta, float kth, float alpha) {
@@ -170,7 +216,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     uint32_t *h = S.hist[0];
     for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
     __syncthreads();
-    uint32_t nab = 0;
+    uint32_t nab = 0, nwin = 0;
     int32_t *lt = list_t + warp * lcap;
     uint32_t *lk = list_k + warp * lcap;
     for (int i0 = s0; i0 < s1; i0 += 32) {                // warp-uniform trip count
@@ -180,6 +226,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       const bool ab = i < s1 && (uint64_t)kk >= whi;
       const bool inw = i < s1 && kk >= wlo && (uint64_t)kk < whi;
       nab += __popc(__ballot_sync(0xffffffffu, ab));
+      nwin += __popc(__ballot_sync(0xffffffffu, inw));
       if (inw) atomicAdd(&h[(kk - wlo) >> 11], 1u);
       const uint32_t bal = __ballot_sync(0xffffffffu, ab || inw);
       if (ab || inw) {
@@ -193,49 +240,35 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     }
     if (lane == 0) {
       S.warp_gt[warp] = nab;
+      S.warp_eq[warp] = nwin;
       S.warp_nl[warp] = nl;
     }
     __syncthreads();
     if (tid == 0) {
-      uint32_t t = 0, ovf = 0;
+      uint32_t t = 0, wn = 0, ovf = 0;
       for (int w = 0; w < TK_WARPS; ++w) {
         t += S.warp_gt[w];
+        wn += S.warp_eq[w];
         ovf |= S.warp_nl[w] > (uint32_t)lcap ? 1u : 0u;
       }
       S.cta_cnt[0] = t | (ovf << 31);                      // counts stay below 2^31
+      S.cta_cnt[1] = wn;
+    }
+    tk_coarse(h, S.coarse[0]);
+    cluster_sync();
+    // cluster totals: keys above the window, keys in it, any list overflow
+    if (tid < 32) {
+      const uint32_t ab = lane < TK_CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], lane)) : 0u;
+      const uint32_t wn = lane < TK_CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], lane)) : 0u;
+      const uint32_t tab_l = __reduce_add_sync(0xffffffffu, ab & 0x7fffffffu);
+      const uint32_t tot_l = __reduce_add_sync(0xffffffffu, wn);
+      const uint32_t ovf_l = __reduce_or_sync(0xffffffffu, ab >> 31);
+      if (lane == 0) { S.tot_s[0] = tab_l; S.tot_s[1] = tot_l; S.tot_s[2] = ovf_l; }
     }
     __syncthreads();
-    cluster_sync();
-    uint32_t tab = 0, ovf = 0;                             // keys above the window; any overflow
-    uint32_t c[TK_BPT];
-#pragma unroll
-    for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
-    {                                                      // all remote loads issued before any use
-      uint4 v[TK_CL];
-      uint32_t ab[TK_CL];
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) {
-        v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
-        ab[r] = ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r));
-      }
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) {
-        tab += ab[r] & 0x7fffffffu;
-        ovf |= ab[r] >> 31;
-        c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w;
-      }
-    }
-    uint32_t tot;
-    const uint32_t incl = tk_block_scan(c[0] + c[1] + c[2] + c[3], S.warp_sums, &tot);
+    const uint32_t tab = S.tot_s[0], tot = S.tot_s[1], ovf = S.tot_s[2];
     if (tab < (uint32_t)k && (uint32_t)k <= tab + tot) {   // the k-th key is in the window
-      uint32_t sfx = tot - incl;
-      const uint32_t need = (uint32_t)k - tab;
-#pragma unroll
-      for (int j = TK_BPT - 1; j >= 0; --j) {
-        if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
-        sfx += c[j];
-      }
-      __syncthreads();
+      tk_find(h, S.coarse[0], (uint32_t)k - tab, S.res);
       prefix = wlo + (S.res[0] << 11);
       above = tab + S.res[1];
       left = 11;
@@ -258,29 +291,11 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       hist_add_warp(h, j < nl && (kk >> 11) == (prefix >> 11), kk & 2047u);   // one bin's keys: ties are common
     }
     __syncthreads();
+    tk_coarse(h, S.coarse[buf]);
     cluster_sync();
-    {
-      uint32_t c[TK_BPT];
-#pragma unroll
-      for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
-      uint4 v[TK_CL];
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) { c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w; }
-      uint32_t tot;
-      const uint32_t incl = tk_block_scan(c[0] + c[1] + c[2] + c[3], S.warp_sums, &tot);
-      uint32_t sfx = tot - incl;
-      const uint32_t need = (uint32_t)k - above;
-#pragma unroll
-      for (int j = TK_BPT - 1; j >= 0; --j) {
-        if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
-        sfx += c[j];
-      }
-      __syncthreads();
-      prefix |= S.res[0];
-      above += S.res[1];
-    }
+    tk_find(h, S.coarse[buf], (uint32_t)k - above, S.res);
+    prefix |= S.res[0];
+    above += S.res[1];
     const uint32_t kstar = prefix;
     const uint32_t need_eq = (uint32_t)k - above;
     // ---- ordered output from the lists (every key >= K* is listed) ----
@@ -357,30 +372,9 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       if (i < n && (kk & hi_mask) == (prefix & hi_mask)) atomicAdd(&h[(kk >> shift) & ((1u << w) - 1)], 1u);
     }
     __syncthreads();
+    tk_coarse(h, S.coarse[buf]);
     cluster_sync();
-    // cluster-wide counts of this thread's TK_BPT consecutive bins (plain loads,
-    // issued together)
-    uint32_t c[TK_BPT];
-#pragma unroll
-    for (int j = 0; j < TK_BPT; ++j) c[j] = 0;
-    {                                                      // all remote loads issued before any use
-      uint4 v[TK_CL];
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) v[r] = ld_dsmem_v4(map_dsmem(h + TK_BPT * tid, r));
-#pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) { c[0] += v[r].x; c[1] += v[r].y; c[2] += v[r].z; c[3] += v[r].w; }
-    }
-    uint32_t tot;
-    const uint32_t mine = c[0] + c[1] + c[2] + c[3];
-    const uint32_t incl = tk_block_scan(mine, S.warp_sums, &tot);
-    uint32_t sfx = tot - incl;                              // keys in bins above mine
-    const uint32_t need = (uint32_t)k - above;
-#pragma unroll
-    for (int j = TK_BPT - 1; j >= 0; --j) {                 // my bins, from the top
-      if (sfx < need && need <= sfx + c[j]) { S.res[0] = TK_BPT * tid + j; S.res[1] = sfx; }
-      sfx += c[j];
-    }
-    __syncthreads();
+    tk_find(h, S.coarse[buf], (uint32_t)k - above, S.res);
     prefix |= S.res[0] << shift;
     above += S.res[1];
     left = shift;
