@@ -593,10 +593,12 @@ PROBE_STEPS = 3
 def launches_per_step(prefetch: bool, n_gpu: int) -> int:
     """Kernels of one layer step (echo_decode_layer_step): write-back with the step's
     prefetch budget (the single-CTA write-back from the pending victim list on pools of
-    at least 14080 slots, then the cooperative manager), indexer 1, top-k 1 (with the
-    deferred exact prefetch cap when prefetching), recall 1 (cooperative manager:
-    protect, miss list, evict+bind, copy, translate), MLA 2 (split + combine)."""
-    return (2 if n_gpu >= 14080 else 1) + 1 + 1 + 1 + 2
+    at least ECHO_PENDING_LIST_MIN_SLOTS slots, then the cooperative manager), indexer 1,
+    top-k 1 (with the deferred exact prefetch cap when prefetching), recall 1
+    (cooperative manager: protect, miss list, evict+bind, copy, translate), MLA 2
+    (split + combine)."""
+    import sparse_attention_kv_dsa_gb300.echo as E
+    return (2 if n_gpu >= E.PENDING_LIST_MIN_SLOTS else 1) + 1 + 1 + 1 + 2
 
 
 def enqueue_index_topk(lib, dl, h, between=None):

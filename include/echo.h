@@ -89,8 +89,9 @@ enum {
  *   priority[n_gpu]  : step of the slot's last touch (LRU key with the host index)
  *   index_buf[n_gpu] : the manager's scratch (victim-selection histograms, at most
  *                      3 x 2048 words; pools under 6 slots use counter words 24..29);
- *                      zero between calls, except, in pools of at least 14080 slots,
- *                      its last 768 words: the pending victim list that a recall
+ *                      zero between calls, except, in pools of at least
+ *                      ECHO_PENDING_LIST_MIN_SLOTS slots, its last 768 words: the
+ *                      pending victim list that a recall
  *                      leaves for the next write-back (the recall ranks the B least
  *                      recently used slots it does not evict; the write-back evicts
  *                      them in one CTA if every slot still holds its recorded key,
@@ -100,13 +101,18 @@ enum {
  * 128-byte counters block.  gpu2host, priority and counters must be 16-byte aligned
  * (read as vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
  * The manager calls (write-back, recall, alloc, evict) are cooperative launches over
- * the whole device, one CTA per SM (a write-back on a pool of at least 14080 slots
+ * the whole device, one CTA per SM (a write-back on a pool of at least
+ * ECHO_PENDING_LIST_MIN_SLOTS slots
  * first launches one CTA that uses the pending list; the cooperative launch then
  * returns at once if that CTA did the work); calls on one layer must not run
  * concurrently, and only the library writes the layer's arrays between calls.
  * A manager call whose grid barrier waited more than ~1 s sets ECHO_ERR_TIMEOUT and
  * leaves the layer undefined until echo_cache_reset.
  */
+/* Pools of at least this many slots keep the pending victim list in index_buf: two
+ * sets of three 2048-word histograms, 1024 miss counters and 3 x 256 list words. */
+#define ECHO_PENDING_LIST_MIN_SLOTS 14080
+
 typedef struct {
   int32_t n_gpu;
   int32_t n_host;

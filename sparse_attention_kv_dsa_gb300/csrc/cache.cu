@@ -149,6 +149,7 @@ constexpr int MG_BPT = (1 << MG_MAXBITS) / MG_THREADS;   // bins per thread in t
 constexpr int MAXB = 1024;                      // requests per call handled by the manager
 constexpr size_t MG_KEY_SMEM = 192 * 1024;      // victim keys cached per CTA (bytes)
 constexpr int PRE_POOL = 6 * (1 << MG_MAXBITS) + MAXB + 3 * PRE_MAX;
+static_assert(PRE_POOL == ECHO_PENDING_LIST_MIN_SLOTS, "index_buf layout and the header agree");
 
 struct MgShared {
   uint32_t hist[1 << MG_MAXBITS];

@@ -24,6 +24,7 @@ KV_WIDTH, V_WIDTH = 576, 512
 CTR_STEP, CTR_N_FREE, CTR_STATUS, CTR_NEED, CTR_CURSOR, CTR_EVICT_M = 0, 1, 2, 3, 4, 5
 CTR_HITS, CTR_STAGED_HITS, CTR_MISSES, CTR_EVICTED, CTR_STAGED, CTR_WB_EVICTED, CTR_BOUND, CTR_QUALIFIED = range(8, 16)
 NUM_COUNTERS = 32
+PENDING_LIST_MIN_SLOTS = 14080  # ECHO_PENDING_LIST_MIN_SLOTS: pools that keep the pending victim list
 
 STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                 ERR_TIMEOUT: "TIMEOUT", ERR_POOL_EXHAUSTED: "POOL_EXHAUSTED", ERR_HOST_INDEX: "HOST_INDEX",

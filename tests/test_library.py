@@ -54,3 +54,18 @@ def test_kernels_target_sm103a():
         pytest.skip("cuobjdump not available")
     out = subprocess.run([tool, "--list-elf", B.LIB], capture_output=True, text=True).stdout
     assert "sm_103a" in out and "sm_90" not in out
+
+
+def test_binding_constants_match_the_header():
+    import sparse_attention_kv_dsa_gb300.echo as E
+    src = open(os.path.join(ROOT, "include", "echo.h")).read()
+
+    def define(name):
+        m = re.search(r"^#define\s+%s\s+(\S+)" % name, src, flags=re.M)
+        assert m, name
+        return int(m.group(1))
+
+    assert define("ECHO_PF_DEFER_CAP") == E.PF_DEFER_CAP
+    assert define("ECHO_PENDING_LIST_MIN_SLOTS") == E.PENDING_LIST_MIN_SLOTS
+    m = re.search(r"ECHO_NUM_COUNTERS\s*=\s*(\d+)", src)
+    assert m and int(m.group(1)) == E.NUM_COUNTERS
