@@ -285,7 +285,7 @@ def test_pending_victim_writeback_matches_oracle():
     # Pools of at least 14080 slots: each recall also ranks the next write-back's B
     # victims, and the write-back binds them in one CTA.  Residency must equal the
     # oracle's LRU after every call; manager word 19 tells which path the write-back
-    # took.  Rounds cover: free slots left (full path), a new token made resident by
+    # took.  The iterations cover: free slots left (full path), a new token made resident by
     # the recall (fewer victims than listed), a write-back of a subset of the requests,
     # an eviction between recall and write-back (list dropped), two recalls in a step.
     from harness import gpu_residency, check_gpu_maps
@@ -326,27 +326,27 @@ def test_pending_victim_writeback_matches_oracle():
         check_gpu_maps(t.c)
         return sel_np
 
-    for rnd in range(11):
+    for it in range(11):
         writeback(np.arange(B))
-        sel = recall(extra=int(seq_np[0]) if rnd == 5 else None)
-        if rnd == 7:
+        sel = recall(extra=int(seq_np[0]) if it == 5 else None)
+        if it == 7:
             # a second recall in the same step: the same selection with 60 tokens per
             # request replaced (the first one's tokens are protected now)
             for b in range(B):
                 fresh = np.setdiff1d(np.arange(int(seq_np[b])), sel[b])
                 sel[b, :60] = rng.choice(fresh, 60, replace=False)
             recall(sel_np=sel)
-        if rnd == 8:
+        if it == 8:
             n = torch.tensor([40], dtype=torch.int32, device=dev)
             E.cache_evict(t.c, n)
             torch.cuda.synchronize()
             oc.evict(oc.lru_victims(40 - oc.n_free()))
             assert gpu_residency(t.c) == oc.resident_priority()
-        if rnd == 9:
+        if it == 9:
             writeback(np.array([1, 3, 4]))                     # a subset of the requests
             recall()
-    # round 0 is cold, round 1 has free slots: full path; once the pool is full the
-    # write-back takes the list, except after the eviction of round 8
+    # iteration 0 is cold, iteration 1 has free slots: full path; once the pool is full
+    # the write-back takes the list, except after the eviction of iteration 8
     assert path[0] == 0 and path[1] == 0
     assert all(p == 1 for p in path[2:9]), path
     assert path[9] == 0, "the eviction must drop the list"
