@@ -475,3 +475,49 @@ def test_token_union_and_block_properties():
     for j in range(Q):
         assert r["hist"][j].sum() == pos0 + j + 1
         assert r["kth"][j] == np.float32(np.sort(r["scores"][j])[::-1][k - 1])
+
+
+def test_writeback_victims_continue_the_recall_lru_order():
+    # After the recall of step s has protected the selection and evicted its m victims
+    # (the m smallest (priority, host) among slots untouched in step s), the write-back
+    # of step s+1 evicts the next B of that same order, as long as enough of them are
+    # left: the GPU manager ranks them during the recall and binds them at the write-back.
+    rng = np.random.default_rng(21)
+    checked = 0
+    for trial in range(25):
+        B = int(rng.integers(1, 7))
+        span, n_gpu = 600, 300
+        oc = O.LayerCache(n_gpu, span * B)
+        host_base = np.arange(B, dtype=np.int64) * span
+        s = 12
+        hosts = rng.choice(np.concatenate([host_base[b] + np.arange(550) for b in range(B)]), n_gpu, replace=False)
+        for g, h in enumerate(hosts):
+            oc.free[g] = False
+            oc.gpu2host[g] = h
+            oc.host2gpu[h] = g
+            oc.priority[g] = int(rng.integers(0, s))
+        oc.step = s
+        sel = [rng.choice(550, int(rng.integers(5, 200 // B + 6)), replace=False) for _ in range(B)]
+        # the order the recall evicts in: protection first, then (priority, host)
+        prio = oc.priority.copy()
+        for b in range(B):
+            for t in sel[b]:
+                g = oc.host2gpu[host_base[b] + t]
+                if g >= 0:
+                    prio[g] = s
+        used = np.nonzero(oc.gpu2host >= 0)[0]
+        elig = used[prio[used] < s]
+        order = oc.gpu2host[elig[np.lexsort((oc.gpu2host[elig], prio[elig]))]]
+        rec = oc.recall(sel, host_base, [np.zeros(0, dtype=np.int64)] * B)
+        assert rec.status == 0
+        m = rec.evicted.size
+        assert set(rec.evicted.tolist()) == set(order[:m].tolist())
+        if m == 0 or order.size < m + B or oc.n_free() != 0:
+            continue
+        before = set(oc.resident_hosts().tolist())
+        seq = np.full(B, 580, dtype=np.int64)                 # new tokens, not resident
+        oc.writeback(host_base, seq)
+        gone = before - set(oc.resident_hosts().tolist())
+        assert gone == set(order[m:m + B].tolist()), f"trial {trial}"
+        checked += 1
+    assert checked >= 10, "too few trials reached the write-back"
