@@ -32,6 +32,10 @@ Sources (cited below by tag and section):
   [DSA]   DeepSeek-V3.2-Exp report, listed among the show notes' sources: the
           lightning indexer score sum_h w_h * ReLU(q_h . k_t).
 
+Parity unpinned: prefill_buckets.  The pages fix a 256-bucket coarse histogram of the
+score minus the predicted k-th score, but no printed example fixes the bucket mapping
+(R19); the candidate rule built on it is pinned by brute force on that mapping only.
+
 Readings taken where the pages are silent (each is listed again in the design doc):
   R1  indexer score: no extra scale; every t < L_b is scored, the token written
       back in this step included.
@@ -482,7 +486,8 @@ def order_key_f32(x) -> np.ndarray:
 
 def prefill_buckets(scores_f32: np.ndarray, kth_pred: float) -> np.ndarray:
     """Bucket 0..255 of each score (R19): top byte of the key of score - kth_pred,
-    the difference taken in float32."""
+    the difference taken in float32.  Parity unpinned: a reading of the pages, which
+    print no example of the mapping."""
     d = np.asarray(scores_f32, dtype=np.float32) - np.float32(kth_pred)   # float32 op
     return (order_key_f32(d) >> 24).astype(np.int64)
 
