@@ -91,21 +91,21 @@ enum {
  *                      3 x 2048 words; pools under 6 slots use counter words 24..29);
  *                      zero between calls, except, in pools of at least
  *                      ECHO_PENDING_LIST_MIN_SLOTS slots, its last 768 words: the
- *                      pending victim list that a recall
- *                      leaves for the next write-back (the recall ranks the B least
- *                      recently used slots it does not evict; the write-back evicts
- *                      them in one CTA if every slot still holds its recorded key,
- *                      and otherwise runs the full selection)
+ *                      pending victim list that a recall leaves for the next
+ *                      write-back (the recall ranks the B least recently used slots
+ *                      it does not evict; the write-back evicts them in one CTA if
+ *                      every slot still holds its recorded key, and otherwise runs
+ *                      the full selection)
  *   free_map[n_gpu]  : one byte per slot, 1 = free
  * Metadata = 4*n_host + 13*n_gpu bytes (echo_cache_metadata_bytes) plus the fixed
  * 128-byte counters block.  gpu2host, priority and counters must be 16-byte aligned
  * (read as vectors); calls reject other layers with ECHO_ERR_INVALID_ARG.
  * The manager calls (write-back, recall, alloc, evict) are cooperative launches over
  * the whole device, one CTA per SM (a write-back on a pool of at least
- * ECHO_PENDING_LIST_MIN_SLOTS slots
- * first launches one CTA that uses the pending list; the cooperative launch then
- * returns at once if that CTA did the work); calls on one layer must not run
- * concurrently, and only the library writes the layer's arrays between calls.
+ * ECHO_PENDING_LIST_MIN_SLOTS slots first launches one CTA that uses the pending
+ * list; the cooperative launch then returns at once if that CTA did the work); calls
+ * on one layer must not run concurrently, and only the library writes the layer's
+ * arrays between calls.
  * A manager call whose grid barrier waited more than ~1 s sets ECHO_ERR_TIMEOUT and
  * leaves the layer undefined until echo_cache_reset.
  */
