@@ -251,12 +251,13 @@ def run_reference(args, ws, rank):
 
 # ---------------------------------------------------------------- echo arm ----
 def run_echo(args, ws, rank, local):
+    import ctypes
     import torch
     import sparse_attention_kv_dsa_gb300.echo as E
     from sparse_attention_kv_dsa_gb300 import synth as S
     from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
 
-    E.lib()
+    lib = E.lib()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = S.workloads()[args.workload]
@@ -265,10 +266,10 @@ def run_echo(args, ws, rank, local):
     layers = wl.layers
     # step inputs: pool fill + warm-up + timed + e2e + stage leg, within the workload's steps
     n_warm = max(args.warmup - 1, 2)                       # after the first (eager) step
-    base_steps = 1 + n_warm + args.steps + args.steps + 1 + PROBE_STEPS
-    fill_max = max(0, min(args.fill_max, wl.steps + 8 - base_steps - 1))
+    base_steps = 1 + n_warm + args.steps + args.steps + PROBE_STEPS
     if base_steps > wl.steps + 8:
         raise SystemExit(f"--steps/--warmup need {base_steps} decode steps; {wl.name} has {wl.steps}")
+    fill_max = max(0, min(args.fill_max, wl.steps + 8 - base_steps))
     total_steps = base_steps + fill_max
     prefetch = not args.no_prefetch
     scratch = SharedScratch(wl, dev, wl.cap_max)
@@ -280,58 +281,67 @@ def run_echo(args, ws, rank, local):
     h_in = {}                      # pinned host copies of the e2e leg's step inputs (made later)
     h_out = [torch.empty(L[l].out.shape, dtype=L[l].out.dtype, pin_memory=True) for l in range(layers)]
 
-    # timing events around the indexer, recorded inside the graph when supported
-    ext_ok = True
-    ix_ev, st_ev = [], []
+    def timing_event(external=False):
+        return torch.cuda.Event(enable_timing=True, external=True) if external else \
+            torch.cuda.Event(enable_timing=True)
+
+    # events recorded inside the captured graphs (around each layer's indexer launch,
+    # and between the stages of the probe graph) need external events
     try:
-        ix_ev = [(torch.cuda.Event(enable_timing=True, external=True),
-                  torch.cuda.Event(enable_timing=True, external=True)) for _ in range(layers)]
-        st_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)] for _ in range(layers)]
+        timing_event(external=True)
+        ext_ok = True
     except TypeError:
         ext_ok = False
 
-    import ctypes
-    lib = E.lib()
+    # Buffer sets: set 0 is each layer's own step-input/output buffers, sets 1.. are
+    # StepIO objects that own theirs.  Each set has its own captured graph of the whole
+    # step and its own indexer events, so a replay's events stay readable until the
+    # same set replays again, NSETS steps later.
+    io = [None] + [[dl.make_io_set() for dl in L] for _ in range(NSETS - 1)]
 
-    def layer_step(l, st, stages=False):
+    def set_args(p, l):
+        return L[l].args if p == 0 else io[p][l].args
+
+    def set_inputs(p, l):
         dl = L[l]
-        if ext_ok:
-            # the step's kernels issued through the separate entry points (the prefetch
-            # budget as its own launch), with events between the stages
-            a = dl.args
-            h = st.cuda_stream
-            mark = (lambda i: st_ev[l][i].record(st)) if stages else (lambda i: None)
-            mark(0)
-            E.check(lib.echo_cache_writeback(dl.cache.ref, a.new_kv, a.new_ik, a.idx_k, a.D, a.Lmax, a.idx_dtype,
-                                             a.host_base, a.seq_len, a.B, h))
-            mark(1)
-            if a.prefetch:
-                E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap,
-                                               a.pf_count, h))
-            mark(2)
-            enqueue_index_topk(lib, dl, h, between=lambda: mark(3))
-            mark(4)
-            E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k,
-                                          a.pf_list if a.prefetch else None, a.pf_count if a.prefetch else None,
-                                          a.cap_max, a.stage_kv, a.miss_list, a.n_miss, a.slot_idx, h))
-            mark(5)
-            E.check(lib.echo_sparse_mla_decode(a.q_mla, dl.cache.struct.gpu_kv, dl.cache.n_gpu,
-                                               dl.cache.struct.kv_dtype, a.slot_idx, a.B, a.Hq, a.k,
-                                               ctypes.c_float(a.scale), a.out, a.lse, a.mla_workspace,
-                                               a.mla_workspace_bytes, h))
-            mark(6)
-        else:
-            dl.step(stream=st)
+        return (dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla) if p == 0 else io[p][l].inputs
 
-    def load_inputs(s, st, from_host=False):
+    def set_out(p, l):
+        return L[l].out if p == 0 else io[p][l].out
+
+    def layer_step(l, st):
+        # the step's kernels issued through the separate entry points (the prefetch
+        # budget as its own launch), with events between the stages
+        dl = L[l]
+        a = dl.args
+        h = st.cuda_stream
+        mark = lambda i: st_ev[l][i].record(st)
+        mark(0)
+        E.check(lib.echo_cache_writeback(dl.cache.ref, a.new_kv, a.new_ik, a.idx_k, a.D, a.Lmax, a.idx_dtype,
+                                         a.host_base, a.seq_len, a.B, h))
+        mark(1)
+        if a.prefetch:
+            E.check(lib.echo_cache_reserve(dl.cache.ref, a.seq_len, a.B, a.cap_max, a.cap_div, a.cap,
+                                           a.pf_count, h))
+        mark(2)
+        enqueue_index_topk(lib, dl, h, between=lambda: mark(3))
+        mark(4)
+        E.check(lib.echo_cache_recall(dl.cache.ref, a.sel, a.host_base, a.B, a.k,
+                                      a.pf_list if a.prefetch else None, a.pf_count if a.prefetch else None,
+                                      a.cap_max, a.stage_kv, a.miss_list, a.n_miss, a.slot_idx, h))
+        mark(5)
+        E.check(lib.echo_sparse_mla_decode(a.q_mla, dl.cache.struct.gpu_kv, dl.cache.n_gpu,
+                                           dl.cache.struct.kv_dtype, a.slot_idx, a.B, a.Hq, a.k,
+                                           ctypes.c_float(a.scale), a.out, a.lse, a.mla_workspace,
+                                           a.mla_workspace_bytes, h))
+        mark(6)
+
+    def load_inputs(s, st):
         with torch.cuda.stream(st):
             for l in range(layers):
-                if from_host:
-                    L[l].load_step_inputs(*h_in[(l, s)], non_blocking=True)
-                else:
-                    L[l].load_step_inputs(inp.q_ik[l][s], inp.new_ik_ik[l][s], inp.new_kv[l][s], inp.q_mla[l][s])
+                L[l].load_step_inputs(inp.q_ik[l][s], inp.new_ik_ik[l][s], inp.new_kv[l][s], inp.q_mla[l][s])
 
-    # first step eagerly (cold cache), then capture one whole step in a graph
+    # first step eagerly (cold cache), then capture one whole step per buffer set
     s_idx = 0
     load_inputs(s_idx, stream)
     with torch.cuda.stream(stream):
@@ -339,79 +349,88 @@ def run_echo(args, ws, rank, local):
             L[l].step(stream=stream)
     s_idx += 1
     stream.synchronize()
-    # the timed graph is the library's own step (echo_decode_layer_step) with its
-    # profiling hook recording events around each layer's indexer launch
+    ix_ev = [[(timing_event(True), timing_event(True)) for _ in range(layers)] for _ in range(NSETS)] \
+        if ext_ok else None
     if ext_ok:
-        for l in range(layers):
-            for j in range(2):
-                ix_ev[l][j].record(stream)                # creates the events
-                L[l].args.index_events[j] = ix_ev[l][j].cuda_event
+        # the timed graphs are the library's own step (echo_decode_layer_step) with its
+        # profiling hook recording events around each layer's indexer launch
+        for p in range(NSETS):
+            for l in range(layers):
+                for j in range(2):
+                    ix_ev[p][l][j].record(stream)            # creates the events
+                    set_args(p, l).index_events[j] = ix_ev[p][l][j].cuda_event
         stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for l in range(layers):
-            L[l].step(stream=stream)
-    # a second set of every layer's step-input and output buffers with the same step
-    # captured on them: the e2e leg copies step i+1's inputs in while step i computes
-    alt_args, alt_in, alt_out = [], [], []
-    for dl in L:
-        keep = (dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla, dl.out, dl.lse, dl.args)
-        dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla = (torch.empty_like(x) for x in keep[:4])
-        dl.out, dl.lse = torch.empty_like(keep[4]), torch.empty_like(keep[5])
-        alt_in.append((dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla))
-        alt_out.append(dl.out)
-        alt_args.append(dl.make_args())
-        dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla, dl.out, dl.lse, dl.args = keep
-    graph_alt = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_alt, stream=stream):
-        for l in range(layers):
-            L[l].step(stream=stream, args=alt_args[l])
-    probe = None                                         # the same step with events between stages
+    graphs = []
+    for p in range(NSETS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(layers):
+                L[l].step(stream=stream, args=set_args(p, l))
+        graphs.append(g)
+    probe, st_ev = None, None                             # the same step with events between stages
     if ext_ok:
+        st_ev = [[timing_event(True) for _ in range(7)] for _ in range(layers)]
         probe = torch.cuda.CUDAGraph()
         with torch.cuda.graph(probe, stream=stream):
             for l in range(layers):
-                layer_step(l, stream, stages=True)
+                layer_step(l, stream)
     torch.cuda.synchronize()
 
-    # Step i of a run uses buffer set i % 2 (the two captured graphs).  A copy stream
-    # stages step i+1's inputs while step i computes and, in the end-to-end leg, reads
-    # step i's attention output back to pinned host memory once it is done.
+    # Step i of a run uses buffer set i % NSETS.  A copy stream stages step i+1's inputs
+    # while step i computes and, in the end-to-end leg, reads step i's attention output
+    # back to pinned host memory once it is done.
     cs = torch.cuda.Stream(dev)
-    in_sets = [[(dl.q_idx, dl.new_ik, dl.new_kv, dl.q_mla) for dl in L], alt_in]
-    out_sets = [[dl.out for dl in L], alt_out]
-    graphs = [graph, graph_alt]
-    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-    ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_in = [torch.cuda.Event() for _ in range(NSETS)]
+    ev_done = [torch.cuda.Event() for _ in range(NSETS)]
 
     def stage_inputs(i, s, from_host):
-        p = i % 2
+        p = i % NSETS
         with torch.cuda.stream(cs):
-            if i >= 2:
-                cs.wait_event(ev_done[p])                    # set p: step i-2 has computed
+            if i >= NSETS:
+                cs.wait_event(ev_done[p])                    # set p: step i-NSETS has computed
             for l in range(layers):
                 src = h_in[(l, s)] if from_host else \
                     (inp.q_ik[l][s], inp.new_ik_ik[l][s], inp.new_kv[l][s], inp.q_mla[l][s])
-                for dst, x in zip(in_sets[p][l], src):
+                for dst, x in zip(set_inputs(p, l), src):
                     dst.copy_(x, non_blocking=True)
             ev_in[p].record(cs)
 
-    def run_pipelined(s0, n, from_host):
+    def run_pipelined(s0, n, from_host, sample_ix=False):
+        """Steps s0 .. s0+n-1 back to back.  Returns the (start, end) events of every
+        replay and, with sample_ix, every replay's per-layer indexer time (ms): the
+        host reads replay i's in-graph events while replays i+1 .. i+NSETS-1 are
+        queued, before replay i+NSETS records them again."""
         cs.wait_stream(stream)
         stage_inputs(0, s0, from_host)
+        evs = [(timing_event(), timing_event()) for _ in range(n)]
+        ix = []
+
+        def read_ix(j):
+            q = j % NSETS
+            evs[j][1].synchronize()
+            ix.append([ix_ev[q][l][0].elapsed_time(ix_ev[q][l][1]) for l in range(layers)])
+
         for i in range(n):
-            p = i % 2
+            p = i % NSETS
             if i + 1 < n:
                 stage_inputs(i + 1, s0 + i + 1, from_host)
             stream.wait_event(ev_in[p])
+            evs[i][0].record(stream)
             with torch.cuda.stream(stream):
                 graphs[p].replay()
+            evs[i][1].record(stream)
             ev_done[p].record(stream)
             if from_host:
                 with torch.cuda.stream(cs):
                     cs.wait_event(ev_done[p])
                     for l in range(layers):
-                        h_out[l].copy_(out_sets[p][l], non_blocking=True)
+                        h_out[l].copy_(set_out(p, l), non_blocking=True)
+            if sample_ix and i >= NSETS - 1:
+                read_ix(i - (NSETS - 1))
+        if sample_ix:
+            for j in range(max(0, n - (NSETS - 1)), n):
+                read_ix(j)
+        return evs, ix
 
     # steady state of the pool: untimed steps until every layer has fewer free slots
     # than its last step bound, so that every timed step evicts (or fill_max steps)
@@ -419,7 +438,7 @@ def run_echo(args, ws, rank, local):
     while fill < fill_max:
         load_inputs(s_idx, stream)
         with torch.cuda.stream(stream):
-            graph.replay()
+            graphs[0].replay()
         s_idx += 1
         fill += 1
         stream.synchronize()
@@ -428,7 +447,7 @@ def run_echo(args, ws, rank, local):
             break
     n_free_at_start = [int(dl.cache.read_counters()[E.CTR_N_FREE]) for dl in L]
 
-    run_pipelined(s_idx, n_warm, from_host=False)         # both graphs, as timed
+    run_pipelined(s_idx, n_warm, from_host=False)         # every graph, as timed
     s_idx += n_warm
     stream.synchronize()
     for dl in L:
@@ -441,18 +460,17 @@ def run_echo(args, ws, rank, local):
                             inp.new_kv[l][s].cpu().pin_memory(), inp.q_mla[l][s].cpu().pin_memory())
 
     # ---------------- timed region: inputs resident in HBM ----------------
-    seq0 = [dl.seq_len.clone() for dl in L]
-    ix_ms = []
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    seq0 = [dl.seq_len.cpu().double() for dl in L]        # context lengths before the first timed step
+    ev0, ev1 = timing_event(), timing_event()
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        # the stream first spins ~1 ms per timed step, so the host has queued every step
-        # before ev0: the events time the device's work, not the host's issue rate
+        # the stream first spins for a few ms so that the host has queued the first
+        # replays before ev0: the events time the device's work, not the host's issue
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(2e6) * args.steps)
+            torch.cuda._sleep(int(2e6) * NSETS)
         ev0.record(stream)
-        run_pipelined(s_idx, args.steps, from_host=False)
+        step_ev, ix_samples = run_pipelined(s_idx, args.steps, from_host=False, sample_ix=ext_ok)
         stream.wait_stream(cs)
         ev1.record(stream)
         stream.synchronize()
@@ -460,10 +478,8 @@ def run_echo(args, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
     t_ms = ev0.elapsed_time(ev1)
-    if ext_ok:
-        # events of the last replay (each replay re-records them)
-        ix_ms = [ix_ev[l][0].elapsed_time(ix_ev[l][1]) for l in range(layers)]
-    ctrs = [dl.cache.read_counters() for dl in L]
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    step_gap_ms = [step_ev[i][1].elapsed_time(step_ev[i + 1][0]) for i in range(len(step_ev) - 1)]
     statuses = [dl.cache.status() for dl in L]
     t_ms_max = max_over_ranks(t_ms, ws)
     tokens = sum_over_ranks(wl.batch * args.steps, ws)
@@ -475,9 +491,9 @@ def run_echo(args, ws, rank, local):
     d2h_bytes = sum(h_out[l].numel() * h_out[l].element_size() for l in range(layers))
     barrier(ws)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = timing_event(), timing_event()
     e0.record(stream)
-    run_pipelined(s_idx, args.steps, from_host=True)
+    e2e_ev, _ = run_pipelined(s_idx, args.steps, from_host=True)
     s_idx += args.steps
     stream.wait_stream(cs)
     e1.record(stream)
@@ -485,9 +501,13 @@ def run_echo(args, ws, rank, local):
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
     e2e_value = tokens / (e2e_ms / 1e3)
+    e2e_step_ms = [a.elapsed_time(b) for a, b in e2e_ev]
 
-    # ---------------- per-stage times inside the graph (probe replays, untimed) ----------------
-    stages, telemetry = {}, None
+    # ------- per-stage times and counters inside the graph (probe replays, untimed) -------
+    stages, telemetry, per_step = {}, None, []
+    row_bytes = 576 * (4 if wl.kv_fp32 else 2)
+    recall_gbs_samples = []
+    ctr_tot = {"hits": 0, "staged_hits": 0, "misses": 0}
     if not args.skip_stages and probe is not None:
         names = ["writeback", "reserve", "index_prefetch", "topk", "recall", "mla"]
         per = {n: [] for n in names}
@@ -499,22 +519,37 @@ def run_echo(args, ws, rank, local):
                 probe.replay()
             s_idx += 1
             stream.synchronize()
-            for i, n in enumerate(names):
-                per[n].append(sum(st_ev[l][i].elapsed_time(st_ev[l][i + 1]) for l in range(layers)) * 1e3 / layers)
+            us = {n: [st_ev[l][i].elapsed_time(st_ev[l][i + 1]) * 1e3 for l in range(layers)]
+                  for i, n in enumerate(names)}
+            for n in names:
+                per[n].append(sum(us[n]) / layers)
+            rec = {"step": None, "hits": [], "staged_hits": [], "misses": [], "qualified": [], "staged": []}
             for l, dl in enumerate(L):
                 c = dl.cache.read_counters()
+                rec["step"] = c[E.CTR_STEP]
+                for key, idx in (("hits", E.CTR_HITS), ("staged_hits", E.CTR_STAGED_HITS),
+                                 ("misses", E.CTR_MISSES), ("qualified", E.CTR_QUALIFIED),
+                                 ("staged", E.CTR_STAGED)):
+                    rec[key].append(int(c[idx]))
+                ctr_tot["hits"] += c[E.CTR_HITS]
+                ctr_tot["staged_hits"] += c[E.CTR_STAGED_HITS]
+                ctr_tot["misses"] += c[E.CTR_MISSES]
                 tele["qualified"].append(c[E.CTR_QUALIFIED])
                 tele["staged"].append(c[E.CTR_STAGED])
                 tele["useful"].append(c[E.CTR_STAGED_HITS])
                 tele["final_recall"].append(c[E.CTR_MISSES])
+                # this layer's host-link rows over this layer's recall time, same step
+                if c[E.CTR_MISSES] > 0 and us["recall"][l] > 0:
+                    recall_gbs_samples.append(c[E.CTR_MISSES] * row_bytes / (us["recall"][l] * 1e-6) / 1e9)
                 th, kth = theta_before[l].cpu(), dl.kth.cpu()
                 ok = torch.isfinite(th) & torch.isfinite(kth) & (kth != 0)
                 if bool(ok.any()):
                     tele["theta_rel_err"].append(float(((th[ok] - kth[ok]).abs() / kth[ok].abs()).median()))
+            rec["recall_us"] = [round(x, 2) for x in us["recall"]]
+            per_step.append(rec)
         stages = {n + "_us": round(statistics.median(v), 2) for n, v in per.items()}
         stages["how"] = "CUDA events between the stages inside a graph of the step issued through the separate " \
                         "entry points (reserve as its own launch), median of %d steps, mean over layers" % PROBE_STEPS
-        row_bytes = 576 * (4 if wl.kv_fp32 else 2)
         mean = lambda v: (sum(v) / len(v)) if v else None
         telemetry = {
             "qualified_rows": mean(tele["qualified"]),
@@ -532,22 +567,24 @@ def run_echo(args, ws, rank, local):
 
     # ---------------- roofline of the dominant kernel (indexer) ----------------
     peaks = measured_peaks()
-    mean_ctx = sum(float(x.float().mean()) for x in seq0) / layers + args.steps / 2.0
+    # a step's write-back appends one token before scoring: the timed steps score
+    # seq0 + 1 .. seq0 + steps tokens per request
+    mean_ctx = sum(float(x.mean()) for x in seq0) / layers + (args.steps + 1) / 2.0
     ix_bytes = wl.batch * mean_ctx * (wl.d_idx + 4)               # keys read + scores written
-    ix_avg_ms = (sum(ix_ms) / len(ix_ms)) if ix_ms else stages.get("index_prefetch_us", 0.0) / 1e3
+    ix_flat = [x for row in ix_samples for x in row]
+    ix_avg_ms = statistics.median(ix_flat) if ix_flat else stages.get("index_prefetch_us", 0.0) / 1e3
     achieved = ix_bytes / (ix_avg_ms / 1e3) / 1e9 if ix_avg_ms else None
     traffic, tnote = kernel_traffic(os.path.join(ROOT, "sparse_attention_kv_dsa_gb300", "csrc", "indexer.cu"),
                                     wl.name)
-    hits = sum(c[8] for c in ctrs)
-    staged_hits = sum(c[9] for c in ctrs)
-    misses = sum(c[10] for c in ctrs)
-    sel_total = hits + staged_hits + misses
-    recall_bytes = misses * 576 * 2          # host-link bytes of the recall (staged rows come from HBM)
+    sel_total = ctr_tot["hits"] + ctr_tot["staged_hits"] + ctr_tot["misses"]
     clocks = clk.summary()
     link = None if args.skip_host_link else host_link(dev)
     if rank != 0:
         return 0
-    recall_gbs = (recall_bytes / (stages["recall_us"] / 1e6) / 1e9) if stages.get("recall_us") else None
+    recall_gbs = statistics.median(recall_gbs_samples) if recall_gbs_samples else None
+    if recall_gbs is not None and link is not None:
+        assert recall_gbs <= 1.05 * link["peak_gbs"], \
+            f"recall GB/s {recall_gbs:.1f} above the measured host link {link['peak_gbs']:.1f}: a counting error"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_ms_max / args.steps, "higher_is_better": True,
@@ -563,31 +600,40 @@ def run_echo(args, ws, rank, local):
                      "kernel": "indexer_fp8_kernel",
                      "algorithmic_bytes_per_launch": ix_bytes,
                      "avg_launch_ms": ix_avg_ms,
-                     "timing": "CUDA events inside the timed graph" if ix_ms else "eager stage leg",
+                     "launch_samples": len(ix_flat),
+                     "timing": ("median over every timed replay and layer of CUDA events recorded around the "
+                                "indexer launch inside the timed graphs") if ix_flat else "eager stage leg",
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic_note": tnote},
         "cpu_baseline": cpu_baseline(wl) if not args.skip_cpu else None,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "step_ms": [round(x, 3) for x in e2e_step_ms],
                 "how": "library step replayed as a CUDA Graph; each step's inputs copied from pinned host memory "
                        "and its attention output read back inside the timed region, on a copy stream that "
-                       "overlaps the next step's inputs with the current step (two buffer sets)"},
+                       "overlaps the next step's inputs with the current step (%d buffer sets)" % NSETS},
+        "step_ms": [round(x, 3) for x in step_ms],
+        "step_gap_ms_max": round(max(step_gap_ms), 3) if step_gap_ms else None,
         "gpu_launches": launches_per_step(prefetch, wl.n_gpu) * layers * args.steps,
         "clocks": clocks,
         "stages_us": stages,
+        "probe_steps": per_step,
         "prefetch_telemetry": telemetry,
         "indexer_gbs": achieved,
         "recall_gbs": recall_gbs,
+        "recall_gbs_how": "per layer and probe step: rows recalled from the host after the top-k x row bytes / "
+                          "that layer's recall time in the same step; median",
         "host_link": link,
         "recall_kernel_frac_of_host_link": (link["zero_copy_recall_gbs"] / link["memcpy_h2d_gbs"]) if link else None,
-        "hit_rate": (hits / sel_total) if sel_total else None,
-        "hit_rate_after_prefetch": ((hits + staged_hits) / sel_total) if sel_total else None,
+        "hit_rate": (ctr_tot["hits"] / sel_total) if sel_total else None,
+        "hit_rate_after_prefetch": ((ctr_tot["hits"] + ctr_tot["staged_hits"]) / sel_total) if sel_total else None,
         "device_status": statuses,
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-PROBE_STEPS = 3
+NSETS = 3
+PROBE_STEPS = 6
 
 
 def launches_per_step(prefetch: bool, n_gpu: int) -> int:

@@ -127,6 +127,13 @@ class DecodeLayer:
         self._args_pf = pf
         return a
 
+    def make_io_set(self) -> "StepIO":
+        """A second set of this layer's per-step input and output buffers, with step
+        arguments that point at them (every other pointer is shared with self.args).
+        The returned object owns the tensors: keep it alive as long as any CUDA Graph
+        captured on its arguments may replay."""
+        return StepIO(self)
+
     def step(self, stream=None, args: E.StepArgsT | None = None):
         E.decode_layer_step(self.cache, args or self.args, stream)
 
@@ -162,6 +169,29 @@ class DecodeLayer:
                 "priority": c.priority.cpu().numpy().copy(), "free_map": c.free_map.cpu().numpy().copy(),
                 "counters": c.counters.cpu().numpy().copy(), "seq_len": self.seq_len.cpu().numpy().copy(),
                 "theta": self.theta.cpu().numpy().copy()}
+
+
+class StepIO:
+    """Per-step input and output buffers of one layer beside the layer's own set
+    (double buffering: a copy stream fills one set while a step computes on the
+    other).  Holds the tensors for as long as the object lives."""
+
+    def __init__(self, dl: DecodeLayer):
+        self.q_idx = torch.empty_like(dl.q_idx)
+        self.new_ik = torch.empty_like(dl.new_ik)
+        self.new_kv = torch.empty_like(dl.new_kv)
+        self.q_mla = torch.empty_like(dl.q_mla)
+        self.out = torch.empty_like(dl.out)
+        self.lse = torch.empty_like(dl.lse)
+        a = dl.make_args()
+        p = E.ptr
+        a.q_idx, a.new_ik, a.new_kv, a.q_mla = p(self.q_idx), p(self.new_ik), p(self.new_kv), p(self.q_mla)
+        a.out, a.lse = p(self.out), p(self.lse)
+        self.args = a
+
+    @property
+    def inputs(self):
+        return (self.q_idx, self.new_ik, self.new_kv, self.q_mla)
 
 
 class StepInputs:
