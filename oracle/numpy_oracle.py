@@ -1,4 +1,8 @@
-"""CPU oracle for the ECHO per-layer decode hot path.
+"""Numpy restatement of the CPU oracle for the ECHO per-layer decode hot path.
+
+The oracle proper is the plain C++ library (oracle/echo_oracle.cpp); this module
+states the same definitions again in numpy, independently, and the tests require
+the two to agree.
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of ``bench.py``
@@ -36,7 +40,7 @@ Parity unpinned: prefill_buckets.  The pages fix a 256-bucket coarse histogram o
 score minus the predicted k-th score, but no printed example fixes the bucket mapping
 (R19); the candidate rule built on it is pinned by brute force on that mapping only.
 
-Readings taken where the pages are silent (each is listed again in the design doc):
+Readings taken where the pages are silent:
   R1  indexer score: no extra scale; every t < L_b is scored, the token written
       back in this step included.
   R2  top-k with L < k selects all L tokens; the rest of the row is -1; kth is the
@@ -79,7 +83,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 KV_WIDTH = 576          # MLA latent width                    [REV] "Problem and motivation"
-V_WIDTH = 512           # value part of the latent (reading R13)
+V_WIDTH = 512           # value part of the latent (reading R13: the first 512 latent dims)
 NOT_RESIDENT = -1
 
 # status codes (same meaning as the library's, defined independently)
