@@ -10,8 +10,11 @@
  * Conventions shared by every call
  *   - Ownership: the caller allocates every buffer (device memory, and pinned host
  *     memory made device-visible with echo_host_device_pointer).  The library
- *     allocates nothing, keeps no global state and never synchronises the stream,
- *     except echo_cache_status / echo_cache_read_counters, which do.
+ *     allocates nothing and never synchronises the stream, except
+ *     echo_cache_status / echo_cache_read_counters, which do.  It keeps no global
+ *     state, with one exception: echo_sparse_mla_decode_noalloc uses a scratch
+ *     array compiled into the library (one per GPU that loads it) and caches that
+ *     array's device address per device.
  *   - Every data-dependent count (misses, prefetched rows, the step number, context
  *     lengths, the EMA threshold) lives in device memory, so a sequence of calls can
  *     be captured into one CUDA Graph and replayed step after step [REV] "In-graph

@@ -92,8 +92,8 @@ enum {
 // them in one CTA (wb_fast_kernel) after checking that every entry still holds its key,
 // and its cooperative launch returns at once; any other case takes the full path.
 // Pools of at least PRE_POOL slots keep this layout of index_buf in every mode:
-//   [0, 6144)                two sets of three 2048-bin histograms
-//   [6144 * 2, +MAXB)        the recall's miss counters
+//   [0, 12288)               two sets of three 2048-bin histograms (6 x 2048 words)
+//   [12288, +MAXB)           the recall's miss counters
 //   [n_gpu - 3 PRE_MAX, n_gpu)  pending list: slot, key low word, key high word
 constexpr int PRE_MAX = 256;    // requests per recall that leave a list
 

@@ -14,6 +14,7 @@
 // attention over any buffer holding the same rows in the same order.
 
 #include <algorithm>
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -672,7 +673,9 @@ namespace {
 static __device__ __align__(256) unsigned char g_mla_noalloc_scratch[ECHO_MLA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+// device address of the array, per device; host threads that make their first call
+// on a device at the same time may both look it up, and both store the same value
+std::atomic<void *> g_scratch_addr[kMaxDevices];
 }  // namespace
 
 extern "C" echo_status_t echo_sparse_mla_decode_noalloc(const void *q, const void *kv, int32_t kv_rows,
@@ -686,13 +689,13 @@ extern "C" echo_status_t echo_sparse_mla_decode_noalloc(const void *q, const voi
   if (need > (size_t)ECHO_MLA_NOALLOC_SCRATCH_BYTES) return ECHO_ERR_SCRATCH_LIMIT;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ECHO_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
+  void *scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!scratch) {
     // host code cannot use the array's name as a device address: look it up once
     // per device, with that device current
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_mla_noalloc_scratch) != cudaSuccess || !p) return ECHO_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    if (cudaGetSymbolAddress(&scratch, g_mla_noalloc_scratch) != cudaSuccess || !scratch) return ECHO_ERR_CUDA;
+    g_scratch_addr[dev].store(scratch, std::memory_order_release);
   }
-  return echo_sparse_mla_decode(q, kv, kv_rows, dtype, slot_idx, B, Hq, k, scale, out, lse, g_scratch_addr[dev],
+  return echo_sparse_mla_decode(q, kv, kv_rows, dtype, slot_idx, B, Hq, k, scale, out, lse, scratch,
                                 (size_t)ECHO_MLA_NOALLOC_SCRATCH_BYTES, stream);
 }

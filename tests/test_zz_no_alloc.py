@@ -38,7 +38,6 @@ def _regular(q, kv, idx, scale):
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype,Hq,k,B", [(torch.bfloat16, 128, 2048, 3), (torch.float32, 16, 300, 2)])
 def test_noalloc_matches_regular_entry_point_twice(dtype, Hq, k, B):
-    tol = 2e-2 if dtype == torch.bfloat16 else 1e-5
     scale = 1 / math.sqrt(576)
     for call, seed in enumerate((101, 202)):               # two calls in a row; the scratch keeps the
         q, kv, idx = _inputs(seed, dtype, B, Hq, k)        # first call's contents when the second starts
@@ -48,8 +47,10 @@ def test_noalloc_matches_regular_entry_point_twice(dtype, Hq, k, B):
         E.sparse_mla_decode_noalloc(q, kv, idx, scale, out, lse)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all(), f"call {call}: non-finite output"
-        assert float((out.float() - ref_out.float()).abs().max()) <= tol, f"call {call}"
-        assert float((lse - ref_lse).abs().max()) <= tol, f"call {call}"
+        # the same kernels on the same inputs, and the split merge runs in a fixed
+        # order: any difference would be a stale or overlapping partial in the scratch
+        assert torch.equal(out, ref_out), f"call {call}: output differs from the regular entry point"
+        assert torch.equal(lse, ref_lse), f"call {call}: lse differs from the regular entry point"
 
 
 @pytest.mark.gpu
