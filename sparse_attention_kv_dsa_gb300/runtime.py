@@ -34,7 +34,7 @@ class DecodeLayer:
     """State and buffers of one layer for a workload."""
 
     def __init__(self, wl: S.Workload, layer: int, device="cuda", *, prefetch=True, cap_max=None,
-                 scratch: SharedScratch | None = None, fill=True, gen_device=None):
+                 scratch: SharedScratch | None = None, fill=True, gen_device=None, adaptive_slack=None):
         dev = torch.device(device)
         self.wl, self.layer, self.device = wl, layer, dev
         B, Lmax = wl.batch, wl.max_ctx
@@ -67,6 +67,8 @@ class DecodeLayer:
         self.new_kv = torch.zeros(B, E.KV_WIDTH, dtype=kvdt, device=dev)
         self.q_mla = torch.zeros(B, wl.h_q, E.KV_WIDTH, dtype=kvdt, device=dev)
         self.cache.reset()
+        if adaptive_slack is not None:                    # the adaptive prefetch cap
+            self.cache.enable_adaptive_cap(B, adaptive_slack)
         if fill:
             self.fill_context(gen_device=gen_device)
         self.args = self.make_args()
@@ -143,6 +145,9 @@ class DecodeLayer:
         the plain top-k; True defers it into the top-k launch, as the fused step does."""
         wl, sc, c = self.wl, self.scratch, self.cache
         pf = self.prefetch
+        if pf and not defer_cap and c.struct.pf_new_rows:
+            raise ValueError("the adaptive cap needs echo_topk_prefetch (defer_cap=True): the plain top-k does "
+                             "not record the prediction error")
         E.cache_writeback(c, self.new_kv, self.new_ik, self.idx_k, self.host_base, self.seq_len, stream)
         if pf:
             E.cache_reserve(c, self.seq_len, self.cap_max, wl.cap_div, self.cap, self.pf_count, stream)
@@ -230,9 +235,12 @@ class PrefillChunk:
                 as soon as it is scored, before its top-k finishes; the exact recall
                 afterwards only fetches what the candidates missed.
     The exact k-th scores of block i are block i+1's predictions (query j for query
-    j); the first block predicts +inf, i.e. it has no candidates."""
+    j); the first block predicts +inf, i.e. it has no candidates.  With attend=True
+    each block's queries then run sparse MLA over their own selections (after the
+    block's union is resident), so a block is done when its attention is."""
 
-    def __init__(self, wl: S.Workload, block: int, device="cuda", layer: int = 0, gen_device=None):
+    def __init__(self, wl: S.Workload, block: int, device="cuda", layer: int = 0, gen_device=None,
+                 record: bool = False, attend: bool = False):
         dev = torch.device(device)
         self.wl, self.block, self.device = wl, int(block), dev
         gd = gen_device or (dev if dev.type == "cuda" else "cpu")
@@ -274,6 +282,27 @@ class PrefillChunk:
         self.status = torch.zeros(1, dtype=i32, device=dev)
         self.s1 = torch.cuda.Stream(dev)
         self.s2 = torch.cuda.Stream(dev)
+        # attend=True: after a block's exact recall, its queries' sparse MLA over their
+        # own selections (slots translated from the selections), written to out / lse
+        self.attend = bool(attend)
+        if attend:
+            self.q_mla = S.prefill_qmla(wl, layer, self.chunk, 0, gd).to(dev).contiguous()
+            self.slot_q = torch.empty(Q, self.k, dtype=i32, device=dev)
+            self.out = torch.empty(self.chunk, wl.h_q, E.V_WIDTH, dtype=torch.bfloat16, device=dev)
+            self.lse = torch.empty(self.chunk, wl.h_q, device=dev)
+            self.mla_ws = torch.empty(E.mla_workspace_bytes(Q, wl.h_q, self.k), dtype=torch.uint8, device=dev)
+        # record=True keeps every block's outputs (copied on the stream that made them,
+        # after the fact) for checks; the two rotating buffers above hold only the last two
+        self.rec = None
+        if record:
+            nb = self.nblocks
+            self.rec = {"kpred": torch.empty(nb, Q, device=dev), "kth": torch.empty(nb, Q, device=dev),
+                        "sel": torch.empty(nb, Q, self.k, dtype=i32, device=dev),
+                        "cand": torch.zeros(nb, Q, dtype=i32, device=dev),
+                        "thr": torch.zeros(nb, Q, dtype=i32, device=dev),
+                        "n_union": torch.zeros(nb, dtype=i32, device=dev),
+                        "n_miss": torch.zeros(nb, dtype=i32, device=dev),
+                        "n_miss_cand": torch.zeros(nb, dtype=i32, device=dev)}
 
     def reset(self):
         self.cache.reset()
@@ -318,13 +347,29 @@ class PrefillChunk:
             with torch.cuda.stream(s1):
                 self.theta[p].copy_(kp)
                 E.topk(self.scores[p], self.seq[i], k, self.sel[p], self.kth[p], self.theta[p], 0.5, s1)
+                if self.rec is not None:
+                    self.rec["kpred"][i].copy_(kp)
+                    self.rec["sel"][i].copy_(self.sel[p])
+                    self.rec["kth"][i].copy_(self.kth[p])
                 ev_topk[i].record(s1)
             with torch.cuda.stream(s2):
                 s2.wait_event(ev_topk[i])
+                if self.rec is not None and mode == "echo":
+                    self.rec["cand"][i].copy_(self.cand[p])
+                    self.rec["thr"][i].copy_(self.thr[p])
+                    self.rec["n_miss_cand"][i].copy_(self.nmiss_c[p][0])
                 E.mark_tokens(self.sel[p], self.bitmap[p], L, s2)
                 E.token_list(self.bitmap[p], L, self.lst[p], self.count[p], s2)
                 E.cache_recall(self.cache, self.lst[p], self.hb, self.miss[p], self.nmiss[p], self.slot[p],
                                stream=s2)
+                if self.rec is not None:
+                    self.rec["n_union"][i].copy_(self.count[p][0])
+                    self.rec["n_miss"][i].copy_(self.nmiss[p][0])
+                if self.attend:
+                    E.translate_slots(self.cache, self.sel[p], self.hb, self.slot_q, s2)
+                    E.sparse_mla_decode(self.q_mla[i * Q:(i + 1) * Q], self.cache.gpu_kv, self.slot_q,
+                                        self.wl.scale, self.out[i * Q:(i + 1) * Q], self.lse[i * Q:(i + 1) * Q],
+                                        self.mla_ws, s2)
                 ev_done[i].record(s2)
         s1.wait_stream(s2)
         end.record(s1)

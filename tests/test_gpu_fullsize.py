@@ -1,9 +1,12 @@
 """Parity at the full sizes of the decode workloads, in the launch configuration the
 benchmark times (one layer of the 64K and of the 80K-100K workloads).
 
-* 64K, batch 8: one steady-state step is checked element by element against the
-  oracle by state hand-off -- the oracle takes the GPU's cache state before the
-  step (residency, priorities, EMA threshold) and recomputes the whole step.
+* 64K, batch 8: three consecutive steady-state steps are checked element by
+  element against the oracle by state hand-off -- the oracle takes the GPU's cache
+  state before each step (residency, priorities, EMA threshold) and recomputes the
+  whole step; every attention head of one request per step.
+* 100K, batch 16, 110K GPU slots (low locality): two steps by state hand-off for
+  every prefetch cap of the sweep {0, 1024, 4096, 16384}.
 * 80K-100K, batch 32: sampled scores, exact top-k of sampled requests (the oracle
   scores those requests itself), sampled attention heads, and invariants over all.
 """
@@ -20,14 +23,14 @@ from sparse_attention_kv_dsa_gb300 import synth as S
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def build(name, steps_before):
+def build(name, steps_before, steps_total=None):
     from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
     wl = S.workloads()[name]
     wl.layers = 1
     dev = torch.device("cuda")
     sc = SharedScratch(wl, dev, wl.cap_max)
     dl = DecodeLayer(wl, 0, dev, scratch=sc, gen_device="cpu")
-    inp = StepInputs(wl, 1, steps_before + 1, dev, gen_device="cpu")
+    inp = StepInputs(wl, 1, steps_total or steps_before + 1, dev, gen_device="cpu")
     for s in range(steps_before):
         dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
         dl.step()
@@ -59,54 +62,141 @@ def handoff_cache(dl, wl):
     return oc
 
 
-def test_decode_b8_ctx64k_full_step_by_state_handoff():
+def generator_keys(wl, layer=0):
+    """Indexer keys of every context token, from the generator (float32, exact)."""
+    return [S.grid_to_float(S.keys_for(wl, layer, b, wl.ctx[b])).numpy() for b in range(wl.batch)]
+
+
+def handoff_step(wl, dl, inp, s, keys, *, full_heads=(), sampled=0, rng=None):
+    """Run step s on the GPU and, from the GPU's state before it (residency,
+    priorities, EMA threshold, context lengths), the oracle's step s; compare every
+    output element by element.  keys holds each request's keys up to the previous
+    step and gains this step's new key.  Attention: every head of the requests in
+    full_heads, 8 random heads of `sampled` other requests."""
     from harness import gpu_residency, check_gpu_maps
-    wl, dl, inp = build("decode-b8-ctx64k", steps_before=3)
-    s = 3
     oc = handoff_cache(dl, wl)
     seq = dl.seq_len.cpu().numpy().astype(np.int64)
     theta = dl.theta.cpu().numpy()
-    # the oracle's own inputs: keys from the generator, plus the appended tokens
-    keys = []
+    nik = S.grid_to_float(S.new_ik_for(wl, 0, s)).numpy()
     for b in range(wl.batch):
-        k0 = S.grid_to_float(S.keys_for(wl, 0, b, wl.ctx[b])).numpy().astype(np.float64)
-        extra = [S.grid_to_float(S.new_ik_for(wl, 0, j)[b:b + 1]).numpy() for j in range(s + 1)]
-        keys.append(np.concatenate([k0] + extra))
+        keys[b] = np.concatenate([keys[b], nik[b:b + 1]])
     dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
     dl.step()
     torch.cuda.synchronize()
+    assert dl.cache.status() == 0
     r = O.decode_layer_step(oc, host_base=wl.host_base, seq_len=seq, keys_of=lambda b, L: keys[b][:L],
                             q_idx=S.grid_to_float(inp.q_int[0][s].cpu()).numpy(), w_idx=dl.w_idx.cpu().numpy(),
-                            theta=theta, k=wl.topk, cap_max=wl.cap_max, cap_div=wl.cap_div, alpha=wl.alpha,
-                            q_mla=None)
+                            theta=theta, k=wl.topk, cap_max=dl.cap_max if dl.prefetch else 0, cap_div=wl.cap_div,
+                            alpha=wl.alpha, q_mla=None, prefetch=dl.prefetch)
+    assert r.recall.status == 0
     scores = dl.scratch.scores.cpu().numpy()
     sel = dl.sel.cpu().numpy()
     pf_list, pf_count = dl.pf_list.cpu().numpy(), dl.pf_count.cpu().numpy()
     miss, n_miss = dl.miss_list.cpu().numpy(), dl.n_miss.cpu().numpy()
-    staged_total = 0
     for b in range(wl.batch):
         L = int(seq[b])
         assert np.array_equal(scores[b, :L], r.scores[b]), f"scores, request {b}"
         assert set(sel[b].tolist()) == set(r.sel[b].tolist()), f"top-k, request {b}"
-        assert set(pf_list[b, :pf_count[b]].tolist()) == set(r.staged[b].tolist()), f"prefetch, request {b}"
+        if dl.prefetch:
+            assert pf_count[b] == len(r.staged[b]), f"prefetch count, request {b}"
+            assert set(pf_list[b, :pf_count[b]].tolist()) == set(r.staged[b].tolist()), f"prefetch, request {b}"
         assert set(miss[b, :n_miss[b]].tolist()) == set(r.recall.misses[b]), f"misses, request {b}"
-        staged_total += len(r.staged[b])
     assert np.array_equal(dl.kth.cpu().numpy(), r.kth) and np.array_equal(dl.theta.cpu().numpy(), r.theta)
     assert gpu_residency(dl.cache) == oc.resident_priority(), "residency / priorities"
     check_gpu_maps(dl.cache)
-    assert staged_total > 0, "steady state should prefetch"
-    # sampled attention heads against the oracle
+    ctr = dl.cache.counters.cpu().numpy()
+    hits = sum(len(x) for x in r.recall.hits)
+    sh = sum(len(x) for x in r.recall.staged_hits)
+    ms = sum(len(x) for x in r.recall.misses)
+    assert (ctr[8], ctr[9], ctr[10]) == (hits, sh, ms), "hit / prefetch-hit / miss counters"
+    # attention against the oracle over the host rows of the oracle's selection
     slot = dl.slot_idx.cpu().numpy()
-    kv = dl.cache.gpu_kv.float().cpu().numpy()
+    kv = dl.cache.gpu_kv
     qm = inp.q_mla[0][s].float().cpu().numpy()
     out = dl.out.float().cpu().numpy()
-    rng = np.random.default_rng(0)
-    for b in rng.choice(wl.batch, 3, replace=False):
+    lse = dl.lse.cpu().numpy()
+    rng = rng or np.random.default_rng(s)
+    others = [b for b in range(wl.batch) if b not in set(full_heads)]
+    for b in list(full_heads) + [int(x) for x in rng.choice(others, min(sampled, len(others)), replace=False)]:
         rows = host_rows(wl, dl, inp, b, r.sel[b])
-        assert np.array_equal(kv[slot[b]], host_rows(wl, dl, inp, b, sel[b])), "recalled rows"
-        heads = rng.choice(wl.h_q, 8, replace=False)
-        o, _ = O.sparse_mla_decode(qm[b, heads], rows, wl.scale)
-        assert np.abs(out[b, heads] - o).max() <= 2e-2
+        got = kv[torch.from_numpy(slot[b]).long().cuda()].float().cpu().numpy()
+        assert np.array_equal(got, host_rows(wl, dl, inp, b, sel[b])), "recalled rows"
+        heads = np.arange(wl.h_q) if b in set(full_heads) else rng.choice(wl.h_q, 8, replace=False)
+        o, l_ = O.sparse_mla_decode(qm[b, heads], rows, wl.scale)
+        assert np.abs(out[b, heads] - o).max() <= 2e-2, f"attention, request {b}"
+        assert np.abs(lse[b, heads] - l_).max() <= 2e-2, f"lse, request {b}"
+    return {"hits": hits, "staged_hits": sh, "misses": ms, "staged": sum(len(x) for x in r.staged)}
+
+
+def test_decode_b8_ctx64k_three_steps_by_state_handoff():
+    wl, dl, inp = build("decode-b8-ctx64k", steps_before=3, steps_total=6)
+    keys = generator_keys(wl)
+    for s in range(3):                                   # the keys appended by the steps already run
+        nik = S.grid_to_float(S.new_ik_for(wl, 0, s)).numpy()
+        for b in range(wl.batch):
+            keys[b] = np.concatenate([keys[b], nik[b:b + 1]])
+    staged = 0
+    for s in (3, 4, 5):
+        st = handoff_step(wl, dl, inp, s, keys, full_heads=(s % wl.batch,), sampled=2)
+        staged += st["staged"]
+    assert staged > 0, "steady state should prefetch"
+
+
+def test_lowlocality_b16_ctx100k_cap_sweep_by_state_handoff():
+    """The low-locality workload (16 requests at 100K, 110K GPU slots, half of each
+    selection new every step) at full size, for every cap of its sweep: two steps
+    each compared with the oracle from the GPU's state.  At cap 1024 about 15K rows
+    qualify per request and the exact cap ("the first cap qualifying tokens by t")
+    does most of the work."""
+    from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
+    wl = S.workloads()["lowlocality-b16-ctx100k"]
+    wl.layers = 1
+    dev = torch.device("cuda")
+    cap_top = max(wl.cap_sweep)
+    sc = SharedScratch(wl, dev, cap_top)
+    dl = DecodeLayer(wl, 0, dev, cap_max=cap_top, scratch=sc, gen_device="cpu")
+    inp = StepInputs(wl, 1, wl.steps, dev, gen_device="cpu")
+    keys = generator_keys(wl)
+    s = 0
+
+    def set_cap(cap):
+        # the prefetch list is [B, cap_max] with a row stride of cap_max
+        dl.cap_max, dl.prefetch = cap, cap > 0
+        dl.pf_list = torch.full((wl.batch, max(cap, 1)), -1, dtype=torch.int32, device=dev)
+        dl.args = dl.make_args()
+
+    def plain_step():
+        nonlocal s
+        nik = S.grid_to_float(S.new_ik_for(wl, 0, s)).numpy()
+        for b in range(wl.batch):
+            keys[b] = np.concatenate([keys[b], nik[b:b + 1]])
+        dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
+        dl.step()
+        s += 1
+
+    set_cap(0)
+    for _ in range(4):                                   # fill the pool (every later step evicts)
+        plain_step()
+    torch.cuda.synchronize()
+    assert int(dl.cache.counters[1].item()) < wl.batch * wl.topk, "pool not yet under pressure"
+    seen = {}
+    for i, cap in enumerate(wl.cap_sweep):
+        set_cap(cap)
+        if i > 0:
+            plain_step()                                  # one step under the new cap before comparing
+        for _ in range(2):
+            st = handoff_step(wl, dl, inp, s, keys, full_heads=(s % wl.batch,) if cap == 1024 else (), sampled=1)
+            s += 1
+            seen.setdefault(cap, []).append(st)
+    assert s <= wl.steps
+    sel_rows = wl.batch * wl.topk
+    for cap, sts in seen.items():
+        for st in sts:
+            assert st["misses"] + st["staged_hits"] > 0.3 * sel_rows, f"cap {cap}: low locality expected"
+            if cap == 0:
+                assert st["staged"] == 0
+            else:
+                assert 0 < st["staged"] <= wl.batch * cap
 
 
 def test_saturated_b32_ctx80k_100k_sampled_and_invariants():
