@@ -848,7 +848,8 @@ def run_compare_prefetch(args, local) -> int:
 
 def run_prefill(args, local) -> int:
     """Prefill chunk indexing of one request (a 2048-token chunk at positions 100K...):
-    the time until every block's exact selection is resident, for the serial
+    the time until every block's exact selection is resident (and, *_attn_us, until
+    every block's queries have attended over their selections), for the serial
     pipeline, the overlapped one, and the overlapped one with the histogram
     candidates recalled early; plus the scoring kernel against the FP8 tensor roof
     (FP8 peak = 2 x the measured bf16 GEMM peak, the nominal dense ratio)."""
@@ -864,25 +865,29 @@ def run_prefill(args, local) -> int:
     out = {"mode": "prefill", "workload": wl.name, "ctx": wl.ctx[0], "chunk": wl.prefill_chunk, "topk": wl.topk,
            "reps": args.steps, "blocks": {}}
     for block in wl.prefill_blocks:
-        pc = PrefillChunk(wl, block, dev)
+        pc = PrefillChunk(wl, block, dev, attend=True)
         res = {}
-        for mode in ("serial", "overlap", "echo"):
-            ts = []
-            for rep in range(args.warmup + args.steps):
-                pc.reset()
-                torch.cuda.synchronize()
-                t0, t1 = pc.run(mode)
-                torch.cuda.synchronize()
-                if rep >= args.warmup:
-                    ts.append(t0.elapsed_time(t1) * 1e3)
-            assert int(pc.status.item()) == 0 and pc.cache.status() == 0
-            res[mode + "_us"] = round(statistics.median(ts), 1)
+        for attend in (False, True):
+            pc.attend = attend                              # with each block's sparse attention
+            for mode in ("serial", "overlap", "echo"):
+                ts = []
+                for rep in range(args.warmup + args.steps):
+                    pc.reset()
+                    torch.cuda.synchronize()
+                    t0, t1 = pc.run(mode)
+                    torch.cuda.synchronize()
+                    if rep >= args.warmup:
+                        ts.append(t0.elapsed_time(t1) * 1e3)
+                assert int(pc.status.item()) == 0 and pc.cache.status() == 0
+                res[mode + ("_attn" if attend else "") + "_us"] = round(statistics.median(ts), 1)
+        pc.attend = False
         # candidate recall vs exact recall of the last block (echo mode state)
         res["last_block_candidates"] = int(pc.cand[(pc.nblocks - 1) % 2].sum().item())
         res["last_block_misses_after_candidates"] = int(pc.nmiss[(pc.nblocks - 1) % 2].item())
         res["last_block_candidate_recall_misses"] = int(pc.nmiss_c[(pc.nblocks - 1) % 2].item())
         res["speedup_echo_vs_serial"] = round(res["serial_us"] / res["echo_us"], 3)
         res["speedup_echo_vs_overlap"] = round(res["overlap_us"] / res["echo_us"], 3)
+        res["speedup_echo_vs_serial_with_attention"] = round(res["serial_attn_us"] / res["echo_attn_us"], 3)
         # the scoring kernel alone: middle block, CUDA events after a device-side delay
         i = pc.nblocks // 2
         pos0 = pc.ctx + i * block

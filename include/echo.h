@@ -51,8 +51,9 @@ enum {
   ECHO_ERR_POOL_EXHAUSTED = 5, /* device: not enough evictable slots for the tokens    */
   ECHO_ERR_HOST_INDEX = 6,     /* device: a host index fell outside [0, n_host)        */
   ECHO_ERR_STAGING = 7,        /* device: a request's prefetch cap exceeds its staging  */
-  ECHO_ERR_SCRATCH_LIMIT = 8   /* host: the call needs more than the library's built-in
+  ECHO_ERR_SCRATCH_LIMIT = 8,  /* host: the call needs more than the library's built-in
                                   scratch (echo_sparse_mla_decode_noalloc only)         */
+  ECHO_ERR_NOT_RESIDENT = 9    /* device: a token to attend over has no GPU slot        */
 };
 
 enum { ECHO_F32 = 0, ECHO_BF16 = 1, ECHO_E4M3 = 2 };
@@ -128,6 +129,22 @@ typedef struct {
   void *gpu_kv;        /* [n_gpu, 576], kv_dtype                                  */
   void *host_kv;       /* [n_host, 576], kv_dtype, pinned host memory (device view) */
   int32_t kv_dtype;    /* ECHO_F32 or ECHO_BF16                                    */
+  /* Adaptive prefetch cap, optional (NULL pf_new_rows: the cap follows the context
+   * alone).  [REV] "Decode: predict the transfer, then recall exactly" (the cap
+   * limits the predicted transfer; the critique asks for its prediction error).
+   * Per request b of the calls on this layer:
+   *   pf_new_rows[b] tokens of its last exact selection that were not resident when
+   *                  that step began (prefetched hits + misses); -1 = no step yet.
+   *                  The step's budget (echo_cache_writeback inside
+   *                  echo_decode_layer_step, or echo_cache_reserve) reads it and sets
+   *                  it to 0; echo_cache_recall adds this step's rows to it.
+   *   pf_pred_err[b] |theta - kth| / |kth| of the last step (float; 0 when either is
+   *                  not finite or kth = 0), written by echo_topk_prefetch.
+   *   cap_b = min(context cap, ceil(min((1 + pf_pred_err[b]) * pf_new_rows[b], 1e9))
+   *               + cap_slack) once pf_new_rows[b] >= 0, the context cap before. */
+  int32_t *pf_new_rows; /* [B] or NULL                                              */
+  float *pf_pred_err;   /* [B] (with pf_new_rows)                                   */
+  int32_t cap_slack;
 } echo_cache_layer_t;
 
 /* Closed form of the per-layer metadata, 4*N_H + 13*N_G bytes
@@ -448,6 +465,23 @@ echo_status_t echo_mark_tokens(const int32_t *tok, int32_t rows, int32_t row_len
  * a one-request echo_cache_recall (the block's union, recalled once). */
 echo_status_t echo_token_list(uint32_t *bitmap, int32_t nbits, int32_t *list, int32_t cap, int32_t *count,
                               echo_stream_t stream);
+
+/*
+ * Prefill sparse attention, slot translation ([REV] "Prefill: overlap recall across
+ * query blocks": once a block's union is resident, each of its queries attends over
+ * its own exact selection; [REV] "Problem and motivation": MLA over the selected
+ * tokens).  For every entry of rows x k token lists:
+ *   out_slot[r, j] = host2gpu[base_r + tok[r, j]]  (tok >= 0), else -1,
+ * with base_r = host_base[r] when per_row_base != 0, host_base[0] otherwise.  The
+ * result is the slot_idx of echo_sparse_mla_decode with one "request" per query row.
+ * A listed token that is not resident gives -1 and sets the layer's sticky status to
+ * ECHO_ERR_NOT_RESIDENT; a host index outside [0, n_host) gives -1 and sets
+ * ECHO_ERR_HOST_INDEX.  Reads the maps only.
+ *   tok, out_slot [rows, k] i32 (device); host_base [rows] or [1] i32 (device).
+ */
+echo_status_t echo_translate_slots(const echo_cache_layer_t *layer, const int32_t *tok, int32_t rows, int32_t k,
+                                   const int32_t *host_base, int32_t per_row_base, int32_t *out_slot,
+                                   echo_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,8 @@ _SIG = {
     "orc_ema_update": (_F, [_F, _F, _F]),
     "orc_prefetch_cap": (_I64, [_I64, _I64, _I64]),
     "orc_prefetch_marks": (_I64, [_P, _I64, _F, _P, _I64, _P]),
+    "orc_prediction_error": (_F, [_F, _F]),
+    "orc_adaptive_cap": (_I64, [_I64, _I64, _I64, _I64, _F, _I64]),
     "orc_sparse_mla_decode": (None, [_P, _I64, _P, _I64, _I64, _D, _I64, _P, _P]),
     "orc_dense_masked_attention": (None, [_P, _I64, _P, _I64, _I64, _P, _D, _I64, _P]),
     "orc_cache_reset": (None, [_P]),
@@ -67,7 +69,7 @@ _SIG = {
     "orc_cache_check_invariants": (_I32, [_P]),
     "orc_decode_layer_step": (_I32, [_P, _I64, _P, _P, _P, ctypes.c_int, _I64, _I64, _P, _P, _P, _P, _I64, _I64,
                                      _I64, _F, ctypes.c_int, _P, _P, _I64, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
-                                     _P, _P, _P, _P]),
+                                     _P, _P, _P, _P, ctypes.c_int, _I64, _P, _P]),
     "orc_order_key_f32": (None, [_P, _I64, _P]),
     "orc_prefill_buckets": (None, [_P, _I64, _F, _P]),
     "orc_prefill_histogram": (None, [_P, _I64, _F, _P]),
@@ -169,6 +171,27 @@ def ema_update(theta, kth, alpha: float = 0.5) -> np.float32:
 
 def prefetch_cap(L: int, cap_max: int, cap_div: int) -> int:
     return int(lib().orc_prefetch_cap(int(L), int(cap_max), int(cap_div)))
+
+
+def prediction_error(theta, kth) -> np.float32:
+    """R23: |theta - kth| / |kth| in float32 (0 when either is not finite or kth = 0)."""
+    return np.float32(lib().orc_prediction_error(float(np.float32(theta)), float(np.float32(kth))))
+
+
+def adaptive_cap(L: int, cap_max: int, cap_div: int, new_rows: int, pred_err, slack: int) -> int:
+    """R23: min(R7's cap, ceil((1 + pred_err) * new_rows) + slack); R7 alone when new_rows < 0."""
+    return int(lib().orc_adaptive_cap(int(L), int(cap_max), int(cap_div), int(new_rows),
+                                      float(np.float32(pred_err)), int(slack)))
+
+
+class AdaptiveCap:
+    """State of the adaptive cap (R23) of one layer: per request the previous step's
+    transfer (new_rows, -1 before any step) and prediction error."""
+
+    def __init__(self, B: int, slack: int):
+        self.new_rows = np.full(B, -1, dtype=np.int64)
+        self.pred_err = np.zeros(B, dtype=np.float32)
+        self.slack = int(slack)
 
 
 def prefetch_marks(scores, theta, resident, cap: int) -> np.ndarray:
@@ -361,10 +384,11 @@ class StepResult:
 def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, w_idx, theta,
                       k: int, cap_max: int, cap_div: int, alpha: float = 0.5,
                       q_mla=None, latent_of=None, scale: float | None = None,
-                      prefetch: bool = True) -> StepResult:
+                      prefetch: bool = True, adaptive: AdaptiveCap | None = None) -> StepResult:
     """One layer's decode step ([REV] "Decode: predict the transfer, then recall
     exactly"): A1..A10 in orc_decode_layer_step, then A11 (orc_sparse_mla_decode)
-    over the rows latent_of(host indices) of each request's selection.
+    over the rows latent_of(host indices) of each request's selection.  With
+    `adaptive` the caps follow R23 and its state moves on to this step's values.
 
     keys_of(b, L) -> [L, D] indexer keys of request b, this step's new key included
     (L = seq_len[b] + 1); seq_len is incremented in place; theta: float32 [B]."""
@@ -384,8 +408,10 @@ def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, 
     th_in = _c(theta, np.float32).reshape(-1)
     kptr = (ctypes.c_void_p * max(B, 1))(*[_p(x) for x in keys])
     Lmax = max(Ls) if B else 1
-    caps = [prefetch_cap(L, cap_max, cap_div) if prefetch else 0 for L in Ls]
+    caps = [prefetch_cap(L, cap_max, cap_div) if prefetch else 0 for L in Ls]   # R23 never exceeds these
     st_stride = max(caps + [1])
+    ad_new = adaptive.new_rows if adaptive is not None else np.zeros(max(B, 1), dtype=np.int64)
+    ad_err = adaptive.pred_err if adaptive is not None else np.zeros(max(B, 1), dtype=np.float32)
     new_h = np.zeros(max(B, 1), dtype=np.int64)
     scores = np.zeros((max(B, 1), Lmax), dtype=np.float32)
     cap_out = np.zeros(max(B, 1), dtype=np.int64)
@@ -403,7 +429,8 @@ def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, 
         cache.ref, B, _p(hb), _p(seq), kptr, kd, H, D, _p(q), _p(w), _p(th_in), _p(th_out), int(k), int(cap_max),
         int(cap_div), float(np.float32(alpha)), int(bool(prefetch)), _p(new_h), _p(scores), Lmax, _p(cap_out),
         _p(staged), _p(staged_n), st_stride, _p(sel), _p(sel_n), _p(kth), _p(cat), _p(sh), _p(ev),
-        ctypes.byref(nev), ctypes.byref(bad_b), ctypes.byref(bad_t)))
+        ctypes.byref(nev), ctypes.byref(bad_b), ctypes.byref(bad_t), int(adaptive is not None),
+        int(adaptive.slack if adaptive is not None else 0), _p(ad_new), _p(ad_err)))
     if not own:
         seq_len[:] = seq
     if st == -1:

@@ -61,6 +61,12 @@
  *       down from bucket 255; candidates = tokens in strictly higher buckets.  A
  *       query with at most k tokens has every token as a candidate.
  *   R21 a block's recall list is the union of its queries' tokens, ascending.
+ *   R23 adaptive cap (optional): with u_b = the tokens of request b's selection in
+ *       the previous step that were not resident when that step began (its
+ *       prefetched hits plus its misses) and e_b = that step's relative prediction
+ *       error |theta - kth| / |kth| (float; 0 when either is not finite or kth = 0),
+ *       cap_b = min(R7's cap, ceil((1 + e_b) * u_b) + slack); before any
+ *       observation (u_b < 0) R7's cap alone.
  */
 
 #include <algorithm>
@@ -193,6 +199,27 @@ int64_t orc_prefetch_cap(int64_t L, int64_t cap_max, int64_t cap_div) {
     return std::min(cap_max, c);
   }
   return cap_max;
+}
+
+/* R23: relative prediction error of one step, in float: |theta - kth| / |kth| ([REV]
+ * "Decode: predict the transfer ...": theta predicts this step's k-th score). */
+float orc_prediction_error(float theta, float kth) {
+  if (!std::isfinite(theta) || !std::isfinite(kth) || kth == 0.0f) return 0.0f;
+  const float d = std::fabs(theta - kth);
+  return d / std::fabs(kth);
+}
+
+/* R23: the adaptive cap -- last step's transfer, grown by the predictor's relative
+ * error, plus a slack; never above the context rule R7.  new_rows < 0: no
+ * observation yet. */
+int64_t orc_adaptive_cap(int64_t L, int64_t cap_max, int64_t cap_div, int64_t new_rows, float pred_err,
+                         int64_t slack) {
+  const int64_t base = orc_prefetch_cap(L, cap_max, cap_div);
+  if (new_rows < 0 || base <= 0) return base;
+  const float grow = 1.0f + pred_err;
+  const float want = std::min(grow * (float)new_rows, 1.0e9f);   /* a huge error: no limit but R7's */
+  const int64_t c = (int64_t)std::ceil(want) + slack;
+  return std::min(base, std::max<int64_t>(c, 0));
 }
 
 /* Tokens prefetched while scoring ([REV] "Decode: predict the transfer ..."): score
@@ -480,7 +507,9 @@ int32_t orc_cache_check_invariants(const orc_cache_t *c) {
  * Outputs: new_h [B]; scores [B, s_stride] float; caps [B]; staged [B, st_stride]
  * with counts staged_n [B]; sel [B, k] with counts sel_n [B]; kth [B]; theta_out [B];
  * per selected entry (row b at b * k) cat and slot_host; evicted [n_gpu] with count
- * n_evicted.  seq_len is incremented in place.
+ * n_evicted.  seq_len is incremented in place.  adaptive != 0 takes the caps from
+ * R23 with ad_new_rows / ad_pred_err [B] (the previous step's, in) and leaves this
+ * step's in them (out).
  * Returns the recall's status, or -1 when a score is not exact in float
  * (bad_req, bad_tok say where; nothing after the scoring has run). */
 int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_base, int64_t *seq_len,
@@ -490,7 +519,8 @@ int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_bas
                               float *scores, int64_t s_stride, int64_t *caps, int64_t *staged, int64_t *staged_n,
                               int64_t st_stride, int64_t *sel, int64_t *sel_n, float *kth, int8_t *cat,
                               int64_t *slot_host, int64_t *evicted, int64_t *n_evicted, int64_t *bad_req,
-                              int64_t *bad_tok) {
+                              int64_t *bad_tok, int adaptive, int64_t slack, int64_t *ad_new_rows,
+                              float *ad_pred_err) {
   /* A1 */
   orc_cache_writeback(c, host_base, seq_len, B, new_h);
   /* A3 + A4: scores, then the prefetch marks against the threshold before this step */
@@ -507,7 +537,9 @@ int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_bas
       *bad_tok = bad;
       return -1;
     }
-    caps[b] = prefetch ? orc_prefetch_cap(L, cap_max, cap_div) : 0;
+    caps[b] = !prefetch ? 0
+              : adaptive ? orc_adaptive_cap(L, cap_max, cap_div, ad_new_rows[b], ad_pred_err[b], slack)
+                         : orc_prefetch_cap(L, cap_max, cap_div);
     resident.assign(L, 0);
     for (int64_t t = 0; t < L; ++t) {
       const int64_t h = host_base[b] + t;
@@ -526,6 +558,7 @@ int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_bas
     sel_n[b] = orc_topk_select(sd.data(), L, k, sel + b * k, &kv);
     kth[b] = (float)kv;
     theta_out[b] = orc_ema_update(theta_in[b], (float)kv, alpha);
+    if (adaptive) ad_pred_err[b] = orc_prediction_error(theta_in[b], (float)kv);
     sel_off[b + 1] = sel_off[b] + sel_n[b];
     st_off[b + 1] = st_off[b] + staged_n[b];
     for (int64_t j = 0; j < sel_n[b]; ++j) sel_flat.push_back(sel[b * k + j]);
@@ -536,11 +569,15 @@ int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_bas
   std::vector<int64_t> sh_flat(sel_flat.size());
   const int32_t st = orc_cache_recall(c, B, host_base, sel_flat.data(), sel_off.data(), st_flat.data(),
                                       st_off.data(), cat_flat.data(), sh_flat.data(), evicted, n_evicted);
-  for (int64_t b = 0; b < B; ++b)
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t fresh = 0;
     for (int64_t j = 0; j < sel_n[b]; ++j) {
       cat[b * k + j] = cat_flat[sel_off[b] + j];
       slot_host[b * k + j] = sh_flat[sel_off[b] + j];
+      fresh += cat[b * k + j] != 0 ? 1 : 0;       /* prefetched hit or miss */
     }
+    if (adaptive) ad_new_rows[b] = fresh;
+  }
   return st;
 }
 

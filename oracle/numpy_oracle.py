@@ -173,6 +173,35 @@ def prefetch_cap(L: int, cap_max: int, cap_div: int) -> int:
     return int(cap_max)
 
 
+def prediction_error(theta, kth) -> np.float32:
+    """R23: relative error of the threshold as a prediction of the k-th score, float32."""
+    th, kv = np.float32(theta), np.float32(kth)
+    if not (math.isfinite(float(th)) and math.isfinite(float(kv))) or float(kv) == 0.0:
+        return np.float32(0.0)
+    return np.float32(np.float32(abs(np.float32(th - kv))) / np.float32(abs(kv)))
+
+
+def adaptive_cap(L: int, cap_max: int, cap_div: int, new_rows: int, pred_err, slack: int) -> int:
+    """R23: last step's transfer grown by the prediction error, plus slack, at most R7's cap."""
+    base = prefetch_cap(L, cap_max, cap_div)
+    if new_rows < 0 or base <= 0:
+        return base
+    want = np.float32(np.float32(np.float32(1.0) + np.float32(pred_err)) * np.float32(new_rows))
+    want = min(want, np.float32(1.0e9))
+    return min(base, max(int(math.ceil(float(want))) + int(slack), 0))
+
+
+@dataclass
+class AdaptiveCap:
+    """Per request: the previous step's transfer (-1 before any step) and prediction error."""
+    B: int
+    slack: int
+
+    def __post_init__(self):
+        self.new_rows = np.full(self.B, -1, dtype=np.int64)
+        self.pred_err = np.zeros(self.B, dtype=np.float32)
+
+
 def prefetch_marks(scores: np.ndarray, theta: float, resident: np.ndarray, cap: int) -> np.ndarray:
     """Tokens prefetched while scoring ([REV] "Decode: predict the transfer ..."):
     score above the EMA threshold (strictly, R5), not resident, and among the
@@ -419,7 +448,7 @@ class StepResult:
 def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, w_idx, theta,
                       k: int, cap_max: int, cap_div: int, alpha: float = 0.5,
                       q_mla=None, latent_of=None, scale: float | None = None,
-                      prefetch: bool = True) -> StepResult:
+                      prefetch: bool = True, adaptive: AdaptiveCap | None = None) -> StepResult:
     """Run one layer's decode step in the pages' order ([REV] "Decode: predict the
     transfer, then recall exactly"): write-back, score every past token, mark
     above-threshold non-resident tokens for prefetch, exact top-k + EMA, recall,
@@ -438,7 +467,12 @@ def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, 
         L = int(seq_len[b])
         s = to_f32_exact(indexer_scores(q_idx[b], w_idx[b], keys_of(b, L)))
         scores.append(s)
-        cap = prefetch_cap(L, cap_max, cap_div) if prefetch else 0
+        if not prefetch:
+            cap = 0
+        elif adaptive is not None:
+            cap = adaptive_cap(L, cap_max, cap_div, int(adaptive.new_rows[b]), adaptive.pred_err[b], adaptive.slack)
+        else:
+            cap = prefetch_cap(L, cap_max, cap_div)
         caps.append(cap)
         hosts = int(host_base[b]) + np.arange(L)
         resident = cache.host2gpu[hosts] >= 0
@@ -447,8 +481,13 @@ def decode_layer_step(cache: LayerCache, *, host_base, seq_len, keys_of, q_idx, 
         sel, kv = topk_select(scores[b], k)
         sels.append(sel)
         kth[b] = np.float32(kv)
+        if adaptive is not None:
+            adaptive.pred_err[b] = prediction_error(theta_new[b], kv)
         theta_new[b] = ema_update(theta_new[b], kv, alpha)
     rec = cache.recall(sels, host_base, staged)
+    if adaptive is not None:
+        for b in range(B):
+            adaptive.new_rows[b] = len(rec.staged_hits[b]) + len(rec.misses[b])
     out = lse = None
     if q_mla is not None:
         Hq = q_mla.shape[1]

@@ -53,16 +53,31 @@ __global__ void reset_kernel(echo_cache_layer_t L) {
 }
 
 // ---------------------------------------------------------------- reserve --
+// Prefetch budget of request b for a step whose context length is len: the context
+// rule min(cap_max, ceil(len / cap_div)), or cap_max when cap_div is 0; with the
+// adaptive state, at most the last step's transfer grown by the prediction error
+// plus the slack.  Clears the transfer count for this step's recall to fill; call it
+// once per request and step.
+__device__ __forceinline__ int budget_cap(const echo_cache_layer_t &L, int b, int32_t len, int cap_max,
+                                          int cap_div) {
+  int c = 0;
+  if (cap_max > 0) c = max(cap_div > 0 ? min(cap_max, (len + cap_div - 1) / cap_div) : cap_max, 0);
+  if (L.pf_new_rows) {
+    const int32_t u = L.pf_new_rows[b];
+    if (u >= 0 && c > 0) {
+      const float grow = __fadd_rn(1.0f, L.pf_pred_err[b]);
+      const float want = fminf(__fmul_rn(grow, (float)u), 1.0e9f);
+      c = min(c, max((int)ceilf(want) + L.cap_slack, 0));
+    }
+    L.pf_new_rows[b] = 0;
+  }
+  return c;
+}
+
 __global__ void reserve_kernel(echo_cache_layer_t L, const int32_t *seq_len, int B, int cap_max, int cap_div,
                                int32_t *cap, int32_t *pf_count) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    int c = 0;
-    if (cap_max > 0) {
-      const int l = seq_len[b];
-      c = cap_div > 0 ? min(cap_max, (l + cap_div - 1) / cap_div) : cap_max;
-      c = max(c, 0);
-    }
-    cap[b] = c;
+    cap[b] = budget_cap(L, b, seq_len[b], cap_max, cap_div);
     pf_count[b] = 0;
   }
 }
@@ -293,10 +308,7 @@ __device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int 
   const bool bad_h = h < 0 || h >= L.n_host, bad_l = l >= P.Lmax;
   if (P.rs_cap && lane == 0) {                           // budget from the length after this write-back
     const int32_t len = (bad_h || bad_l) ? l : l + 1;
-    int c = 0;
-    if (P.rs_cap_max > 0)
-      c = max(P.rs_cap_div > 0 ? min(P.rs_cap_max, (len + P.rs_cap_div - 1) / P.rs_cap_div) : P.rs_cap_max, 0);
-    P.rs_cap[b] = c;
+    P.rs_cap[b] = budget_cap(L, b, len, P.rs_cap_max, P.rs_cap_div);
     P.rs_pf_count[b] = 0;
   }
   if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); return; }
@@ -365,10 +377,12 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
         ++hit;
       } else if (g <= -2) {
         ++staged;
+        if (L.pf_new_rows) atomicAdd(L.pf_new_rows + b, 1);   // this step's transfer (adaptive cap)
       } else {
         const int32_t pos = atomicAdd(mcnt + b, 1);
         P.miss_list[(int64_t)b * P.k + pos] = t;
         ++miss;
+        if (L.pf_new_rows) atomicAdd(L.pf_new_rows + b, 1);
       }
     }
     hit = block_sum(hit, S.wcnt);

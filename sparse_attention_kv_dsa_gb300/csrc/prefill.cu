@@ -351,6 +351,28 @@ __global__ void __launch_bounds__(TL_THREADS)
   if (tid == 0) *count = total;
 }
 
+// Slot of every listed token (prefill attention): one thread per entry.
+__global__ void translate_kernel(echo_cache_layer_t L, const int32_t *tok, int64_t n, int k,
+                                 const int32_t *host_base, int per_row, int32_t *out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t t = tok[i];
+    int32_t g = -1;
+    if (t >= 0) {
+      const int64_t h = (int64_t)host_base[per_row ? i / k : 0] + t;
+      if (h < 0 || h >= L.n_host) {
+        set_status(L.counters, ECHO_ERR_HOST_INDEX);
+      } else {
+        g = L.host2gpu[h];
+        if (g < 0) {                                 // not resident (or staged in a step)
+          set_status(L.counters, ECHO_ERR_NOT_RESIDENT);
+          g = -1;
+        }
+      }
+    }
+    out[i] = g;
+  }
+}
+
 }  // namespace echo
 
 using namespace echo;
@@ -412,6 +434,19 @@ extern "C" echo_status_t echo_token_list(uint32_t *bitmap, int32_t nbits, int32_
                                          int32_t *count, echo_stream_t stream) {
   if (!bitmap || !list || !count || nbits <= 0 || cap <= 0) return ECHO_ERR_INVALID_ARG;
   token_list_kernel<<<1, TL_THREADS, 0, (cudaStream_t)stream>>>(bitmap, nbits, list, cap, count);
+  ECHO_LAUNCH_OK();
+  return ECHO_OK;
+}
+
+extern "C" echo_status_t echo_translate_slots(const echo_cache_layer_t *layer, const int32_t *tok, int32_t rows,
+                                              int32_t k, const int32_t *host_base, int32_t per_row_base,
+                                              int32_t *out_slot, echo_stream_t stream) {
+  if (!layer || !tok || !host_base || !out_slot || rows <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
+  if (!layer->host2gpu || !layer->counters || layer->n_host <= 0) return ECHO_ERR_INVALID_ARG;
+  const int64_t n = (int64_t)rows * k;
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+  translate_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(*layer, tok, n, k, host_base, per_row_base != 0,
+                                                           out_slot);
   ECHO_LAUNCH_OK();
   return ECHO_OK;
 }

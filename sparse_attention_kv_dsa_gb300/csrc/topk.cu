@@ -127,6 +127,15 @@ __device__ __forceinline__ float ema(float theta, float kth, float alpha) {
   return __fadd_rn(__fmul_rn(a, kth), __fmul_rn(b, theta));  // each op rounded, no FMA
 }
 
+// Relative error of the threshold as this step's prediction of the k-th score, for
+// the adaptive prefetch cap: |theta - kth| / |kth|, 0 when either is not finite or
+// kth = 0; written by the EMA's thread before it replaces theta.
+__device__ __forceinline__ void record_pred_err(const PfFix &F, int b, float theta, float kth) {
+  if (F.cap == nullptr || F.L.pf_pred_err == nullptr) return;
+  const bool ok = isfinite(theta) && isfinite(kth) && kth != 0.f;
+  F.L.pf_pred_err[b] = ok ? __fdiv_rn(fabsf(__fsub_rn(theta, kth)), fabsf(kth)) : 0.f;
+}
+
 __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
                 float *theta, float alpha, int lcap, const __grid_constant__ PfFix F) {
@@ -172,6 +181,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       for (uint32_t r = 0; r < TK_CL; ++r) m = min(m, *cluster.map_shared_rank(&S.minkey, r));
       const float kv = L > 0 ? key_f32(m) : -INFINITY;
       kth_out[b] = kv;
+      record_pred_err(F, b, theta[b], kv);
       theta[b] = ema(theta[b], kv, alpha);
     }
     cluster_sync();
@@ -351,6 +361,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     if (rank == 0 && tid == 0) {
       const float kv = key_f32(kstar);
       kth_out[b] = kv;
+      record_pred_err(F, b, theta[b], kv);
       theta[b] = ema(theta[b], kv, alpha);
     }
     cluster_sync();
@@ -440,6 +451,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   if (rank == 0 && tid == 0) {
     const float kv = key_f32(kstar);
     kth_out[b] = kv;
+    record_pred_err(F, b, theta[b], kv);
     theta[b] = ema(theta[b], kv, alpha);
   }
   cluster_sync();

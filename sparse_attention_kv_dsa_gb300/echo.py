@@ -17,6 +17,7 @@ from . import build as _build
 # ---------------------------------------------------------------- constants --
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_POOL_EXHAUSTED, ERR_HOST_INDEX, ERR_STAGING = range(8)
 ERR_SCRATCH_LIMIT = 8
+ERR_NOT_RESIDENT = 9
 MLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 PF_DEFER_CAP = 1            # echo_index_prefetch flag: exact cap restored by echo_topk_prefetch
 F32, BF16, E4M3 = 0, 1, 2
@@ -28,7 +29,7 @@ PENDING_LIST_MIN_SLOTS = 14080  # ECHO_PENDING_LIST_MIN_SLOTS: pools that keep t
 
 STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                 ERR_TIMEOUT: "TIMEOUT", ERR_POOL_EXHAUSTED: "POOL_EXHAUSTED", ERR_HOST_INDEX: "HOST_INDEX",
-                ERR_STAGING: "STAGING", ERR_SCRATCH_LIMIT: "SCRATCH_LIMIT"}
+                ERR_STAGING: "STAGING", ERR_SCRATCH_LIMIT: "SCRATCH_LIMIT", ERR_NOT_RESIDENT: "NOT_RESIDENT"}
 
 
 class EchoError(RuntimeError):
@@ -41,7 +42,8 @@ class CacheLayerT(ctypes.Structure):
     _fields_ = [("n_gpu", ctypes.c_int32), ("n_host", ctypes.c_int32),
                 ("host2gpu", ctypes.c_void_p), ("gpu2host", ctypes.c_void_p), ("priority", ctypes.c_void_p),
                 ("index_buf", ctypes.c_void_p), ("free_map", ctypes.c_void_p), ("counters", ctypes.c_void_p),
-                ("gpu_kv", ctypes.c_void_p), ("host_kv", ctypes.c_void_p), ("kv_dtype", ctypes.c_int32)]
+                ("gpu_kv", ctypes.c_void_p), ("host_kv", ctypes.c_void_p), ("kv_dtype", ctypes.c_int32),
+                ("pf_new_rows", ctypes.c_void_p), ("pf_pred_err", ctypes.c_void_p), ("cap_slack", ctypes.c_int32)]
 
 
 class StepArgsT(ctypes.Structure):
@@ -82,6 +84,7 @@ SIGNATURES = {
     "echo_prefill_candidates": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "echo_mark_tokens": (_I, [_P, _I, _I, _P, _I, _P]),
     "echo_token_list": (_I, [_P, _I, _P, _I, _P, _P]),
+    "echo_translate_slots": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
     "echo_cache_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "echo_cache_read_counters": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
 }
@@ -183,6 +186,14 @@ class LayerCache:
         arr = (ctypes.c_int32 * NUM_COUNTERS)()
         check(lib().echo_cache_read_counters(self.ref, arr), "read_counters")
         return list(arr)
+
+    def enable_adaptive_cap(self, B: int, slack: int) -> None:
+        """Per-request state of the adaptive prefetch cap (no observation yet)."""
+        dev = self.host2gpu.device
+        self.pf_new_rows = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        self.pf_pred_err = torch.zeros(B, dtype=torch.float32, device=dev)
+        self.struct.pf_new_rows, self.struct.pf_pred_err = ptr(self.pf_new_rows), ptr(self.pf_pred_err)
+        self.struct.cap_slack = int(slack)
 
     def metadata_tensors(self):
         return (self.host2gpu, self.gpu2host, self.priority, self.index_buf, self.free_map)
@@ -295,3 +306,12 @@ def mark_tokens(tok, bitmap, nbits: int, stream=None):
 def token_list(bitmap, nbits: int, out_list, count, stream=None):
     check(lib().echo_token_list(ptr(bitmap), nbits, ptr(out_list), out_list.numel(), ptr(count),
                                 stream_handle(stream)), "token_list")
+
+
+def translate_slots(layer: LayerCache, tok, host_base, out_slot, stream=None):
+    """Slot of every listed token (tok [rows, k], -1 = none); host_base [rows] gives one
+    base per row, [1] one base for all rows."""
+    rows, k = tok.shape
+    per_row = int(host_base.numel() == rows)
+    check(lib().echo_translate_slots(layer.ref, ptr(tok), rows, k, ptr(host_base), per_row, ptr(out_slot),
+                                     stream_handle(stream)), "translate_slots")

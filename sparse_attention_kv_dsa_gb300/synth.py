@@ -182,7 +182,7 @@ def grid_to_fp8(x_int: torch.Tensor) -> torch.Tensor:
 
 
 # ---------------------------------------------------- per-purpose streams ----
-P_KEYS, P_QIDX, P_W, P_DRIFT, P_LAT, P_QMLA, P_NEWKV, P_NEWIK, P_PFQ, P_PFW = range(1, 11)
+P_KEYS, P_QIDX, P_W, P_DRIFT, P_LAT, P_QMLA, P_NEWKV, P_NEWIK, P_PFQ, P_PFW, P_PFQMLA = range(1, 12)
 
 
 def keys_for(wl: Workload, layer: int, b: int, L: int, device="cpu") -> torch.Tensor:
@@ -234,3 +234,9 @@ def prefill_queries(wl: Workload, layer: int, n: int, device="cpu") -> torch.Ten
 def prefill_weights(wl: Workload, layer: int, n: int, device="cpu") -> torch.Tensor:
     """Indexer head weights of n prefill positions [n, H]."""
     return choice(mix_seed(wl.seed, P_PFW, layer), (n, wl.h_idx), wl.w_values, device)
+
+
+def prefill_qmla(wl: Workload, layer: int, n: int, row0: int = 0, device="cpu") -> torch.Tensor:
+    """MLA queries of n prefill positions starting at chunk row row0 [n, Hq, 576]."""
+    dt = torch.float32 if wl.kv_fp32 else torch.bfloat16
+    return normal(mix_seed(wl.seed, P_PFQMLA, layer, row0), (n, wl.h_q, 576), dt, device)

@@ -40,10 +40,12 @@ def check_gpu_maps(cache) -> None:
 class Lockstep:
     """One layer of a workload run on the GPU (DecodeLayer) and in the oracle."""
 
-    def __init__(self, wl: S.Workload, *, prefetch=True, cap_max=None, layer=0):
+    def __init__(self, wl: S.Workload, *, prefetch=True, cap_max=None, layer=0, adaptive_slack=None):
         from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, StepInputs
         self.wl = wl
-        self.dl = DecodeLayer(wl, layer, "cuda", prefetch=prefetch, cap_max=cap_max, gen_device="cpu")
+        self.dl = DecodeLayer(wl, layer, "cuda", prefetch=prefetch, cap_max=cap_max, gen_device="cpu",
+                              adaptive_slack=adaptive_slack)
+        self.adaptive = O.AdaptiveCap(wl.batch, adaptive_slack) if adaptive_slack is not None else None
         self.inp = StepInputs(wl, layer + 1, wl.steps, "cuda", gen_device="cpu")
         self.layer = layer
         self.oc = O.LayerCache(wl.n_gpu, wl.n_host)
@@ -79,7 +81,7 @@ class Lockstep:
                                 theta=self.theta, k=wl.topk, cap_max=self.cap_max if self.prefetch else 0,
                                 cap_div=wl.cap_div, alpha=wl.alpha,
                                 q_mla=self.inp.q_mla[l][s].float().cpu().numpy(),
-                                latent_of=lambda h: self.lat[h], scale=wl.scale)
+                                latent_of=lambda h: self.lat[h], scale=wl.scale, adaptive=self.adaptive)
         self.theta = r.theta
         self.s += 1
         return r
@@ -114,6 +116,11 @@ class Lockstep:
             hb = wl.host_base[b]
             for j in range(n):
                 assert g2h[slot[b, j]] == hb + sel[b, j], "slot_idx"
+        if self.prefetch:
+            assert dl.cap.cpu().tolist() == r.cap, "per-request prefetch caps"
+        if self.adaptive is not None:
+            assert dl.cache.pf_new_rows.cpu().tolist() == self.adaptive.new_rows.tolist(), "adaptive: transfer"
+            assert np.array_equal(dl.cache.pf_pred_err.cpu().numpy(), self.adaptive.pred_err), "adaptive: error"
         assert np.array_equal(dl.kth.cpu().numpy(), r.kth), "kth"
         assert np.array_equal(dl.theta.cpu().numpy(), r.theta), "EMA threshold"
         assert gpu_residency(dl.cache) == self.oc.resident_priority(), "residency / priorities"

@@ -58,6 +58,24 @@ def test_fp8_cap_binds_through_separate_entry_points(defer_cap):
     assert ctr[15] > ctr[12], "qualifying tokens did not exceed the cap"
 
 
+@pytest.mark.parametrize("slack", [4, 300])
+def test_fp8_adaptive_cap(slack):
+    # the cap follows the last step's transfer and prediction error (small slack: it
+    # binds and the exact "first cap by t" rule runs; large slack: the context rule)
+    wl = S.small_workload("fp8-adaptive", ctx=(1800, 2500, 700), topk=256, n_gpu=4096, steps=5, cap_max=1024,
+                          cap_div=4, rho=0.6)
+    ls, st = run(wl, adaptive_slack=slack)
+    assert ls.dl.cache.pf_new_rows.min().item() >= 0
+
+
+def test_fp8_adaptive_cap_through_separate_entry_points():
+    # echo_cache_writeback + echo_cache_reserve + echo_index_prefetch + echo_topk_prefetch
+    # (which records the prediction error) + echo_cache_recall
+    wl = S.small_workload("fp8-adaptive-ops", ctx=(1800, 2500), topk=256, n_gpu=4096, steps=4, cap_max=1024,
+                          cap_div=4, rho=0.6)
+    run(wl, ops={"defer_cap": True}, adaptive_slack=4)
+
+
 def test_fp8_cap_grows_with_context():
     wl = S.small_workload("fp8-capdiv", ctx=(3000, 640), topk=128, n_gpu=2048, steps=3, cap_max=4096, cap_div=32,
                           rho=0.6)

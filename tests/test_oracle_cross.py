@@ -206,3 +206,27 @@ def test_bucket_depends_on_score_minus_prediction(shift):
     d = (rng.integers(-4000, 4001, 500) * 0.125).astype(np.float32)
     s = (d + np.float32(shift)).astype(np.float32)
     assert np.array_equal(O.prefill_buckets(s, shift), _bk(d))
+
+
+def test_adaptive_cap_steps_agree():
+    wl = S.small_workload(ctx=(300, 520, 129), topk=64, n_gpu=400, cap_max=60, cap_div=6, steps=4)
+    B = wl.batch
+    keys = [S.grid_to_float(S.keys_for(wl, 0, b, wl.max_ctx)).numpy() for b in range(B)]
+    a, b_ = O.LayerCache(wl.n_gpu, wl.n_host), N.LayerCache(wl.n_gpu, wl.n_host)
+    ada, adb = O.AdaptiveCap(B, 7), N.AdaptiveCap(B, 7)
+    seq_a, seq_b = np.array(wl.ctx, dtype=np.int64), np.array(wl.ctx, dtype=np.int64)
+    th_a = th_b = np.full(B, np.inf, dtype=np.float32)
+    qi = S.qidx_initial(wl, 0)
+    w = S.weights_for(wl, 0).numpy()
+    for s in range(wl.steps):
+        kw = dict(keys_of=lambda r, L: keys[r][:L], q_idx=S.grid_to_float(qi).numpy(), w_idx=w, k=wl.topk,
+                  cap_max=wl.cap_max, cap_div=wl.cap_div)
+        ra = O.decode_layer_step(a, host_base=wl.host_base, seq_len=seq_a, theta=th_a, adaptive=ada, **kw)
+        rb = N.decode_layer_step(b_, host_base=wl.host_base, seq_len=seq_b, theta=th_b, adaptive=adb, **kw)
+        assert ra.cap == rb.cap
+        assert np.array_equal(ada.new_rows, adb.new_rows) and np.array_equal(ada.pred_err, adb.pred_err)
+        for r in range(B):
+            assert ra.staged[r].tolist() == rb.staged[r].tolist()
+        _same_cache(a, b_)
+        th_a, th_b = ra.theta, rb.theta
+        qi = S.qidx_next(wl, 0, s, qi)

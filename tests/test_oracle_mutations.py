@@ -53,6 +53,13 @@ MUTATIONS = [
     ("bucket from the score, not score - prediction", "const float d = s[i] - kth_pred;", "const float d = s[i];"),
     ("threshold bucket included", "if (bk[t] > thr) cand[n++] = t;", "if (bk[t] >= thr) cand[n++] = t;"),
     ("prefill causal range short by one", "const int64_t L = pos0 + j + 1;", "const int64_t L = pos0 + j;"),
+    ("adaptive cap ignores the error", "const float grow = 1.0f + pred_err;", "const float grow = 1.0f;"),
+    ("adaptive cap without slack", "const int64_t c = (int64_t)std::ceil(want) + slack;",
+     "const int64_t c = (int64_t)std::ceil(want);"),
+    ("adaptive cap above the context rule", "return std::min(base, std::max<int64_t>(c, 0));",
+     "return std::max<int64_t>(c, 0);"),
+    ("prediction error relative to theta", "return d / std::fabs(kth);", "return d / std::fabs(theta);"),
+    ("transfer counts the hits", "fresh += cat[b * k + j] != 0 ? 1 : 0;", "fresh += 1;"),
 ]
 
 

@@ -521,3 +521,66 @@ def test_writeback_victims_continue_the_recall_lru_order():
         assert gone == set(order[m:m + B].tolist()), f"trial {trial}"
         checked += 1
     assert checked >= 10, "too few trials reached the write-back"
+
+
+# ------------------------------------------------------- adaptive cap (R23) --
+def test_prediction_error_hand_values():
+    # |theta - kth| / |kth| in float32: 0.25 / 0.75 rounds to the float nearest 1/3
+    assert O.prediction_error(1.0, 0.75) == np.float32(1.0 / 3.0)
+    assert O.prediction_error(0.5, 1.0) == np.float32(0.5)
+    assert O.prediction_error(-2.0, -4.0) == np.float32(0.5)      # relative to |kth|, not to theta
+    assert O.prediction_error(np.inf, 3.0) == 0.0                  # before the first observation
+    assert O.prediction_error(3.0, 0.0) == 0.0 and O.prediction_error(3.0, -np.inf) == 0.0
+
+
+def test_adaptive_cap_hand_values():
+    # R7 at 64K with cap_div 32 is 2048
+    assert O.adaptive_cap(65536, 4096, 32, -1, 0.0, 256) == 2048     # no observation: R7
+    assert O.adaptive_cap(65536, 4096, 32, 100, 0.5, 256) == 150 + 256
+    assert O.adaptive_cap(65536, 4096, 32, 100, 0.0, 256) == 356
+    assert O.adaptive_cap(65536, 4096, 32, 101, 0.5, 0) == 152      # ceil(151.5)
+    assert O.adaptive_cap(65536, 4096, 32, 5000, 0.0, 256) == 2048   # never above R7
+    assert O.adaptive_cap(65536, 0, 32, 100, 0.0, 256) == 0          # prefetch off
+    assert O.adaptive_cap(1000, 512, 0, 10, 0.0, 3) == 13            # constant cap rule below
+
+
+def test_adaptive_cap_properties():
+    rng = np.random.default_rng(31)
+    for _ in range(300):
+        L, cm, cd = int(rng.integers(1, 200000)), int(rng.integers(0, 20000)), int(rng.choice([0, 16, 32]))
+        u, e, sl = int(rng.integers(0, 5000)), np.float32(rng.random() * 2), int(rng.integers(0, 500))
+        c = O.adaptive_cap(L, cm, cd, u, e, sl)
+        base = O.prefetch_cap(L, cm, cd)
+        assert 0 <= c <= base
+        # exact predictor (e = 0) and no slack: the cap is last step's transfer
+        assert O.adaptive_cap(L, cm, cd, u, 0.0, 0) == min(base, u)
+        # a worse prediction or a larger transfer never lowers the cap
+        assert O.adaptive_cap(L, cm, cd, u, e + np.float32(0.25), sl) >= c
+        assert O.adaptive_cap(L, cm, cd, u + 7, e, sl) >= c
+
+
+def test_adaptive_state_follows_the_steps():
+    # the state after a step is its transfer (prefetched hits + misses) and its error
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    wl = S.small_workload(ctx=(300, 520), topk=64, n_gpu=400, cap_max=40, cap_div=8, steps=3)
+    B = wl.batch
+    keys = [S.grid_to_float(S.keys_for(wl, 0, b, wl.max_ctx)).numpy() for b in range(B)]
+    c = O.LayerCache(wl.n_gpu, wl.n_host)
+    ad = O.AdaptiveCap(B, 5)
+    seq = np.array(wl.ctx, dtype=np.int64)
+    theta = np.full(B, np.inf, dtype=np.float32)
+    qi = S.qidx_initial(wl, 0)
+    w = S.weights_for(wl, 0).numpy()
+    for s in range(wl.steps):
+        prev_new, prev_err = ad.new_rows.copy(), ad.pred_err.copy()
+        r = O.decode_layer_step(c, host_base=wl.host_base, seq_len=seq, keys_of=lambda b, L: keys[b][:L],
+                                q_idx=S.grid_to_float(qi).numpy(), w_idx=w, theta=theta, k=wl.topk,
+                                cap_max=wl.cap_max, cap_div=wl.cap_div, adaptive=ad)
+        for b in range(B):
+            assert r.cap[b] == O.adaptive_cap(int(seq[b]), wl.cap_max, wl.cap_div, int(prev_new[b]), prev_err[b], 5)
+            assert ad.new_rows[b] == len(r.recall.staged_hits[b]) + len(r.recall.misses[b])
+            assert ad.pred_err[b] == O.prediction_error(theta[b], r.kth[b])
+        if s == 0:
+            assert r.cap == [O.prefetch_cap(int(L), wl.cap_max, wl.cap_div) for L in seq]
+        theta = r.theta
+        qi = S.qidx_next(wl, 0, s, qi)
