@@ -6,12 +6,13 @@
 // the values).  Per request b and head h:
 //   logit_j = scale * q[b,h,:] . c_j ;  out = softmax(logit) . c[:, :512] ;  lse.
 //
-// Split over the selected list: each CTA takes 256 consecutive entries of one
-// request and 16 heads, streams the gathered rows through shared memory 32 at a
-// time with an online softmax, and writes (o, m, l) partials; a combine kernel
-// merges the splits in a fixed order.  The result depends only on the rows and
-// their order in slot_idx, so attention over the cache is bitwise identical to
-// attention over any buffer holding the same rows in the same order.
+// Split over the selected list: bf16 (tensor cores) takes 512 consecutive entries of
+// one request per CTA with all 128 heads; float32 (SIMT) takes 256 entries and 16
+// heads per CTA, streaming the gathered rows through shared memory 32 at a time with
+// an online softmax.  Both write (o, m, l) partials, and a combine kernel merges the
+// splits in a fixed order.  The result depends only on the rows and their order in
+// slot_idx, so attention over the cache is bitwise identical to attention over any
+// buffer holding the same rows in the same order.
 
 #include <algorithm>
 #include <atomic>
@@ -156,57 +157,10 @@ __global__ void mla_combine_kernel(MlaPart part, int S, int Hq, T *out, float *l
 static int mla_splits(int k) { return (k + MS_SPLIT - 1) / MS_SPLIT; }
 
 // ===================================================== bf16 tensor-core path ==
-// CTA = (request b, split s of 256 selected entries), all 128 heads.
-//   phase 1  S[128 x 256] = Q . C^T over nine 64-dim chunks: Q chunk by TMA,
-//            gathered C chunk by cp.async into the 128-byte-swizzled K-major
-//            layout; tcgen05.mma kind::f16 M=128 N=256 K=16, f32 in TMEM.
-//   softmax  one thread per head row and half of the columns reads its logits
-//            from TMEM and writes the bf16 probabilities P back into TMEM over
-//            the logits it has read (tokens 0-127 -> columns 0-63, 128-255 ->
-//            columns 128-191; two per 32-bit column).
-//   phase 2  O = P . V in eight blocks of 64 value dims: the MMA takes P from
-//            TMEM and a 64-token x 64-dim V stage (MN-major) from shared memory,
-//            accumulating into one of two 64-column TMEM buffers (columns 64-127
-//            and 192-255), so block j's epilogue overlaps block j+1's MMAs; the
-//            whole phase-1 region is a 12-stage V ring (96 KB in flight).
-//            The epilogue writes O / l as bf16 partials, plus (m, l) per head.
-// Warps 0-3 load (cp.async), run half of the softmax and the epilogues; warps 5-8
-// the other half of the softmax; warp 4 issues the MMAs from one thread.  256 TMEM
-// columns and ~100 KB shared memory per CTA: two CTAs per SM overlap each other's
-// phases.
-constexpr int TC_T = 256;                 // selected entries per CTA
-constexpr int TC_THREADS = 288;         // warps 0-3 loads/softmax/epilogue, 4 MMA, 5-8 softmax
-constexpr int TC_QCH = 128 * 128;         // Q chunk bytes (128 heads x 64 dims)
-constexpr int TC_KCH = TC_T * 128;        // C chunk bytes (256 rows x 64 dims)
-constexpr int TC_STAGE = TC_QCH + TC_KCH; // 48 KB
-constexpr int TC_VROWS = 64;              // tokens per V stage (four K-steps)
-constexpr int TC_VCH = TC_VROWS * 128;    // V stage bytes (64 tokens x 64 dims)
-constexpr int TC_VST = 12;                // V ring stages
-constexpr int TC_SPB = TC_T / TC_VROWS;   // stages per 64-dim output block (4)
-constexpr int TC_NV = 8 * TC_SPB;         // V stages per CTA (eight blocks)
-constexpr int TC_REGION = 2 * TC_STAGE;   // 96 KB, phase 1 ring / V ring
-static_assert(TC_VST * TC_VCH <= TC_REGION, "the V ring reuses the phase-1 region");
-static_assert(TC_VST - 2 <= 10, "cp_async_wait_upto covers the ring");
-
-struct TcShared {
-  uint64_t full[2], empty[2], qfull[2];
-  uint64_t s_full, p_full, o_full[2], o_empty[2];
-  uint64_t vfull[TC_VST], vempty[TC_VST];
-  uint32_t tmem_base;
-  int fail;                                // set when a bounded wait gave up
-  int32_t slots[TC_T];
-  uint32_t vmask[TC_T / 32];
-  float mpart[2][128], lpart[2][128];      // per head: max and sum of each half of the columns
-};
-constexpr size_t TC_SMEM = 1024 + TC_REGION + sizeof(TcShared);
-
 struct TcPart {
   __nv_bfloat16 *o;   // [B, S, 128, 512] normalised partial outputs
   float *ml;          // [B, S, 128, 2]
 };
-
-// TMEM column of the bf16 pair holding tokens t, t+1 of P (t even)
-__device__ __forceinline__ uint32_t p_col(int t) { return (uint32_t)((t >> 1) + (t >= TC_T / 2 ? TC_T / 4 : 0)); }
 
 // 16 consecutive 32-bit TMEM columns of this thread's lane
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -228,69 +182,97 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
-// Wait until at most n (0..10) of this thread's cp.async groups are pending.
-__device__ __forceinline__ void cp_async_wait_upto(int n) {
-  switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    case 7: cp_async_wait<7>(); break;
-    case 8: cp_async_wait<8>(); break;
-    case 9: cp_async_wait<9>(); break;
-    default: cp_async_wait<10>(); break;
-  }
+// CTA = (request b, split s of 512 selected entries), all 128 heads, one CTA per SM
+// (512 TMEM columns).  The 512 entries are two regions of 256 TMEM columns.
+//   phase 1  S[128 x 512] = Q . C^T over nine 64-dim chunks x two token halves:
+//            Q chunk by TMA (once per chunk), the gathered rows of one half by
+//            cp.async into the 128-byte-swizzled layout; tcgen05.mma kind::f16
+//            M=128 N=256 K=16 into region 0 (tokens 0-255) or 1 (256-511).
+//   softmax  over all 512 entries at once: warps 0-3 read region 0, warps 4-7 region
+//            1 (one head row per thread), the row max and sum are exchanged through
+//            shared memory, and bf16 P goes back into TMEM over logits already read
+//            (tokens 128 r + c of a region to column 64 r + c / 2 of its 0-63 or
+//            128-191 band).
+//   phase 2  O = P . V in eight 64-dim blocks, each over the two token halves; A = P
+//            from TMEM, B = 64-token x 64-dim pieces (MN-major) of a stage; four O
+//            buffers (columns 64-127, 192-255, 320-383, 448-511) so the epilogue of
+//            block j overlaps the MMAs of blocks j+1 .. j+3.  The epilogue writes O / l
+//            as bf16 partials plus (m, l) per head, in the layout the combine reads.
+// Every load stage is 256 rows x 64 dims (32 KB; row r at 128 r, its 16-byte chunk c
+// at (c ^ (r & 7)) * 16): a K stage of phase 1 and a V stage of phase 2 differ only in
+// the dims and in how the MMA reads it, so both go through one ring of five slots
+// (160 KB in flight), and the V rows start loading as soon as phase 1 frees slots.
+// Roles: warps 0-3 softmax of region 0 and the epilogues, warps 4-7 softmax of
+// region 1, warp 8 issues the MMAs from lane 0 and the Q chunks' TMA from lane 1
+// (three chunks ahead, apart from the row loads), warps 9-16 only load rows.  Each
+// loader thread ends a stage with cp.async.mbarrier.arrive.noinc on the slot's
+// barrier (256 arrivals), which fires once its copies have landed: the loaders never
+// wait for their own copies; the MMA thread fences them for the tensor cores.
+constexpr int T2_T = 512;                     // selected entries per CTA
+constexpr int T2_LOADERS = 256;               // loader threads (warps 9-16)
+constexpr int T2_THREADS = 9 * 32 + T2_LOADERS;
+constexpr int T2_QST = 3, T2_SLOTS = 5;
+constexpr int T2_QCH = 128 * 128;             // Q chunk bytes
+constexpr int T2_SCH = 256 * 128;             // stage: 256 rows x 64 dims
+constexpr int T2_NK = 18;                     // phase-1 stages: 9 chunks x 2 halves
+constexpr int T2_NS = T2_NK + 16;             // + phase-2 stages: 8 blocks x 2 halves
+constexpr int T2_SOFF = T2_QST * T2_QCH;
+constexpr int T2_REGION = T2_SOFF + T2_SLOTS * T2_SCH;     // 192 KB
+
+struct T2Shared {
+  uint64_t qfull[T2_QST], qempty[T2_QST], full[T2_SLOTS], empty[T2_SLOTS];
+  uint64_t s_full, p_full, o_full[4], o_empty[4];
+  uint32_t tmem_base;
+  int fail;
+  int32_t slots[T2_T];
+  uint32_t vmask[T2_T / 32];
+  float mpart[2][128], lpart[2][128];
+};
+constexpr size_t T2_SMEM = 1024 + T2_REGION + sizeof(T2Shared);
+static_assert(T2_SMEM <= 227 * 1024, "one CTA per SM");
+
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk16) {
-  // byte offset of 16-byte chunk `chunk16` of row `row` in a 128B-swizzled
-  // K-major tile whose rows are 128 bytes apart
-  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4);
+// TMEM column of the bf16 pair holding tokens t, t+1 (t even) of the 512 entries
+__device__ __forceinline__ uint32_t p2_col(int t) {
+  const int c = t & 255;
+  return (uint32_t)(256 * (t >> 8) + (c >> 1) + (c >= 128 ? 64 : 0));
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 2)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __nv_bfloat16 *kv, int kv_rows,
-                  const int32_t *slot_idx, int k, float scale, TcPart part) {
-  extern __shared__ unsigned char tc_raw[];
-  unsigned char *R = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-  TcShared &S = *reinterpret_cast<TcShared *>(R + TC_REGION);
-  unsigned char *V = R;                       // phase 2: V ring (12 x 8 KB)
+__global__ void __launch_bounds__(T2_THREADS, 1)
+    mla_tc2_kernel(const __grid_constant__ CUtensorMap qmap, const __nv_bfloat16 *kv, int kv_rows,
+                   const int32_t *slot_idx, int k, float scale, TcPart part) {
+  extern __shared__ unsigned char t2_raw[];
+  unsigned char *R = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(t2_raw) + 1023) & ~uintptr_t(1023));
+  T2Shared &S = *reinterpret_cast<T2Shared *>(R + T2_REGION);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, b = blockIdx.y, nsplit = gridDim.x;
-  const int j0 = s * TC_T;
+  const int j0 = s * T2_T;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.full[i], 128);
-      mbar_init(&S.empty[i], 1);
-      mbar_init(&S.qfull[i], 1);
-    }
-    for (int i = 0; i < TC_VST; ++i) {
-      mbar_init(&S.vfull[i], 128);
-      mbar_init(&S.vempty[i], 1);
-    }
-    S.fail = 0;
+    for (int i = 0; i < T2_QST; ++i) { mbar_init(&S.qfull[i], 1); mbar_init(&S.qempty[i], 1); }
+    for (int i = 0; i < T2_SLOTS; ++i) { mbar_init(&S.full[i], T2_LOADERS); mbar_init(&S.empty[i], 1); }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, 256);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.o_full[i], 1);
-      mbar_init(&S.o_empty[i], 128);
-    }
+    for (int i = 0; i < 4; ++i) { mbar_init(&S.o_full[i], 1); mbar_init(&S.o_empty[i], 128); }
+    S.fail = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < TC_T; i += TC_THREADS) {
+  for (int i = tid; i < T2_T; i += T2_THREADS) {
     const int j = j0 + i;
     int32_t g = j < k ? slot_idx[(int64_t)b * k + j] : -1;
     g = (g >= 0 && g < kv_rows) ? g : -1;
     S.slots[i] = g;
-    const uint32_t bal = __ballot_sync(0xffffffffu, g >= 0);   // whole warps: 160 and 256 are multiples of 32
-    if (lane == 0) S.vmask[i >> 5] = bal;
   }
-  if (warp == 4) {
-    tmem_alloc(&S.tmem_base, 256);
+  __syncthreads();
+  for (int w = warp; w < T2_T / 32; w += T2_THREADS / 32) {   // 16 mask words over 13 warps
+    const uint32_t bal = __ballot_sync(0xffffffffu, S.slots[w * 32 + lane] >= 0);
+    if (lane == 0) S.vmask[w] = bal;
+  }
+  if (warp == 8) {
+    tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -299,218 +281,194 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
   const uint32_t tmem = S.tmem_base;
   bool ok = true;
 
-  // Softmax of one half of the 256 columns (half 0: warps 0-3, half 1: warps 5-8) for
-  // head row (warp & 3) * 32 + lane: row max and sum exchanged between the halves
-  // through shared memory (named barriers 1 and 2 of the 256 softmax threads); writes
-  // bf16 P for its columns and arrives on p_full.  Returns the row's max and sum.
-  auto softmax_half = [&](int half, float &m_out, float &l_out) {
-    const int hr = (warp & 3) * 32 + lane;
-    const uint32_t tr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t *vmask = S.vmask;             // validity of the 256 entries (set before the first barrier)
-    const int cb = half * (TC_T / 2), ce = cb + TC_T / 2;
+  if (warp >= 9) {
+    // ------------------------------------------------------------ loads --
+    // thread lt copies chunk c = lt & 7 of rows (lt >> 3) + 32 i of each stage: the
+    // same rows in every stage of a half, so their slots are read once into registers
+    constexpr int RPT = 256 * 8 / T2_LOADERS;          // rows per thread and stage (8)
+    const int lt = tid - 9 * 32, c = lt & 7, r0 = lt >> 3;
+    int32_t rows[2][RPT];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) rows[h][i] = S.slots[h * 256 + r0 + 32 * i];
+    for (int g = 0; g < T2_NS && ok; ++g) {
+      const int gg = g < T2_NK ? g : g - T2_NK;
+      const int dc = gg >> 1, half = gg & 1;           // dims 64 dc .., tokens 256 half ..
+      const int sl = g % T2_SLOTS;
+      if (!mbar_wait(&S.empty[sl], ((g / T2_SLOTS) & 1) ^ 1)) { ok = false; break; }
+      unsigned char *sb = R + T2_SOFF + sl * T2_SCH;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = r0 + 32 * i;
+        const int32_t row = half ? rows[1][i] : rows[0][i];
+        const __nv_bfloat16 *src = kv + (int64_t)(row >= 0 ? row : 0) * KV_W + dc * 64 + c * 8;
+        cp_async_16(sb + r * 128 + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16u : 0u);
+      }
+      cp_async_arrive(&S.full[sl]);
+    }
+    cp_async_wait_all();                               // nothing of ours stays in flight at the end
+  } else if (warp == 8) {
+    if (lane == 1) {
+      // ------------------------------------------------- Q chunks (TMA) --
+      int issued = 0;
+      for (int dc = 0; dc < 9; ++dc) {
+        const int qs = dc % T2_QST;
+        if (!mbar_wait(&S.qempty[qs], ((dc / T2_QST) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&S.qfull[qs], T2_QCH);
+        tma_load_2d(R + qs * T2_QCH, &qmap, &S.qfull[qs], dc * 64, b * 128);
+        issued = dc + 1;
+      }
+      // on a failure, the chunks in flight land before the CTA ends (bounded waits)
+      for (int dc = ok ? issued : max(0, issued - T2_QST); !ok && dc < issued; ++dc)
+        mbar_wait(&S.qfull[dc % T2_QST], (dc / T2_QST) & 1);
+    }
+    if (lane == 0) {
+      // --------------------------------------------------------------- MMA --
+      constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, 256);
+      constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 64);
+      for (int g = 0; g < T2_NS && ok; ++g) {
+        const int sl = g % T2_SLOTS;
+        const uint32_t sa = smem_u32(R + T2_SOFF + sl * T2_SCH);
+        if (g < T2_NK) {
+          // S[:, half] += Q chunk dc . rows^T
+          const int dc = g >> 1, half = g & 1, qs = dc % T2_QST;
+          if (!mbar_wait(&S.qfull[qs], (dc / T2_QST) & 1) || !mbar_wait(&S.full[sl], (g / T2_SLOTS) & 1)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();                    // the loaders' cp.async writes, for the tensor cores
+          tc_fence_after();
+          const uint64_t ad = smem_desc(smem_u32(R + qs * T2_QCH), 16, 1024, LAYOUT_SW128);
+          const uint64_t bd = smem_desc(sa, 16, 1024, LAYOUT_SW128);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tmem + 256 * half, ad + 2 * kk, bd + 2 * kk, id1, (dc | kk) ? 1u : 0u);
+          mma_commit(&S.empty[sl]);
+          if (half == 1) mma_commit(&S.qempty[qs]);
+          if (g == T2_NK - 1) {
+            mma_commit(&S.s_full);
+            if (!mbar_wait(&S.p_full, 0)) { ok = false; break; }   // P written by the softmax
+            tc_fence_after();
+          }
+        } else {
+          // O_j += P[:, tokens of half] . V[those tokens, dims of block j]
+          const int gv = g - T2_NK, j = gv >> 1, half = gv & 1, ob = j & 3;
+          if (half == 0 && j >= 4) {                   // this buffer's previous block is written out
+            if (!mbar_wait(&S.o_empty[ob], ((j >> 2) - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+          }
+          if (!mbar_wait(&S.full[sl], (g / T2_SLOTS) & 1)) { ok = false; break; }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t d = tmem + 64u + 128u * (uint32_t)ob;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {               // 16 K-steps of 16 tokens
+            const int t0 = 256 * half + 16 * u;
+            const uint64_t bd = smem_desc(sa + (uint32_t)(u * 16 * 128), 8 * 1024, 1024, LAYOUT_SW128);
+            mma_f16_ts(d, tmem + p2_col(t0), bd, id2, (half | u) ? 1u : 0u);
+          }
+          mma_commit(&S.empty[sl]);
+          if (half == 1) mma_commit(&S.o_full[ob]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- softmax --
+    const int half = warp >> 2;                        // region of the 512 entries
+    const int hr = (warp & 3) * 32 + lane;             // head row = TMEM lane
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t tr = trow + 256u * (uint32_t)half;
+    if (!mbar_wait(&S.s_full, 0)) ok = false;
+    tc_fence_after();
     float m = -INFINITY;
-    for (int c0 = cb; c0 < ce; c0 += 64) {       // two TMEM loads per wait
+    for (int c0 = 0; c0 < 256; c0 += 64) {
       uint32_t r[32], r2[32];
       tmem_ld32(tr + c0, r);
       tmem_ld32(tr + c0 + 32, r2);
       tmem_wait_ld();
-      const uint32_t vm = vmask[c0 >> 5], vm2 = vmask[(c0 >> 5) + 1];
+      const uint32_t vm = S.vmask[(half * 256 + c0) >> 5], vm2 = S.vmask[((half * 256 + c0) >> 5) + 1];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]));
-        if ((vm2 >> j) & 1u) m = fmaxf(m, __uint_as_float(r2[j]));
+      for (int q = 0; q < 32; ++q) {
+        if ((vm >> q) & 1u) m = fmaxf(m, __uint_as_float(r[q]));
+        if ((vm2 >> q) & 1u) m = fmaxf(m, __uint_as_float(r2[q]));
       }
     }
     S.mpart[half][hr] = m;
     asm volatile("bar.sync 1, 256;" ::: "memory");
     m = fmaxf(S.mpart[0][hr], S.mpart[1][hr]);
-    const float c2 = scale * 1.4426950408889634f;      // scale * log2(e)
+    const float c2 = scale * 1.4426950408889634f;     // scale * log2(e)
     const float mc = m * c2;
     float l = 0.f;
-    // 32 probabilities -> 16 bf16 pairs -> 16 TMEM columns of this row, over logits
-    // this thread has already read (p_col(c0) < c0 within its half)
     auto write_p = [&](int c0, const uint32_t (&r)[32], uint32_t vm) {
       uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = ((vm >> j) & 1u) ? exp2f(fmaf(__uint_as_float(r[j]), c2, -mc)) : 0.f;
-        const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[j + 1]), c2, -mc)) : 0.f;
+      for (int q = 0; q < 32; q += 2) {
+        const float p0 = ((vm >> q) & 1u) ? exp2f(fmaf(__uint_as_float(r[q]), c2, -mc)) : 0.f;
+        const float p1 = ((vm >> (q + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[q + 1]), c2, -mc)) : 0.f;
         l += p0 + p1;
         __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-        pk[j >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+        pk[q >> 1] = *reinterpret_cast<uint32_t *>(&v2);
       }
-      tmem_st16(tr + p_col(c0), pk);
+      tmem_st16(trow + p2_col(half * 256 + c0), pk);
     };
-    for (int c0 = cb; c0 < ce; c0 += 64) {       // two TMEM loads per wait
+    for (int c0 = 0; c0 < 256; c0 += 64) {
       uint32_t r[32], r2[32];
       tmem_ld32(tr + c0, r);
       tmem_ld32(tr + c0 + 32, r2);
       tmem_wait_ld();
-      write_p(c0, r, vmask[c0 >> 5]);
-      write_p(c0 + 32, r2, vmask[(c0 >> 5) + 1]);
+      write_p(c0, r, S.vmask[(half * 256 + c0) >> 5]);
+      write_p(c0 + 32, r2, S.vmask[((half * 256 + c0) >> 5) + 1]);
     }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&S.p_full);
     S.lpart[half][hr] = l;
     asm volatile("bar.sync 2, 256;" ::: "memory");
-    m_out = m;
-    l_out = S.lpart[0][hr] + S.lpart[1][hr];
-  };
-
-  if (warp < 4) {
-    // ------------------------------------------------ phase 1 loads --
-    const int row_base = tid;                          // 128 threads
-    for (int dc = 0; dc < 9; ++dc) {
-      const int st = dc & 1;
-      if (!mbar_wait(&S.empty[st], ((dc >> 1) & 1) ^ 1)) { ok = false; break; }
-      unsigned char *qb = R + st * TC_STAGE, *kb = qb + TC_QCH;
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&S.qfull[st], TC_QCH);
-        tma_load_2d(qb, &qmap, &S.qfull[st], dc * 64, b * 128);
-      }
-      // 256 rows x 8 chunks: thread handles chunk (tid & 7) of rows (tid >> 3) + 16 i
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int r = (row_base >> 3) + 16 * i, c = row_base & 7;
-        const int32_t g = S.slots[r];
-        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + dc * 64 + c * 8;
-        cp_async_16(kb + sw128(r, c), src, g >= 0 ? 16u : 0u);
-      }
-      cp_async_commit();
-      if (dc > 0) {
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(&S.full[(dc - 1) & 1]);
-      }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(&S.full[8 & 1]);
-
-    // ------------------------------------------------------ softmax --
-    if (!mbar_wait(&S.s_full, 0)) ok = false;
-    tc_fence_after();
-    // V loads of the first stages can start: phase 1 no longer reads smem
-    auto load_v = [&](int vc) {                        // block vc / TC_SPB, tokens (vc % TC_SPB) * 64
-      const int st = vc % TC_VST, j = vc / TC_SPB, r0 = (vc % TC_SPB) * TC_VROWS;
-      unsigned char *vb = V + st * TC_VCH;
-#pragma unroll
-      for (int i = 0; i < TC_VROWS * 8 / 128; ++i) {
-        const int idx = tid + 128 * i;                 // rows x 8 chunks of 16 B (64 dims)
-        const int r = idx >> 3, c = idx & 7;
-        const int32_t g = S.slots[r0 + r];
-        const __nv_bfloat16 *src = kv + (int64_t)(g >= 0 ? g : 0) * KV_W + j * 64 + c * 8;
-        cp_async_16(vb + r * 128 + ((c ^ (r & 7)) << 4), src, g >= 0 ? 16u : 0u);
-      }
-      cp_async_commit();
-    };
-    for (int vc = 0; vc < TC_VST; ++vc) load_v(vc);
-    const int h = tid;                                  // head row = TMEM lane
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float m = 0.f, l = 0.f;
-    softmax_half(0, m, l);
-
-    // ------------------------------------------- phase 2 loads + epilogue --
-    // epilogue of 64-dim block j: O / l from its TMEM buffer to bf16 partials, stored
-    // in groups of 8 dims with heads innermost ([b][s][dim/8][head][8]), so the 32
-    // heads of a warp write one contiguous 512-byte run per store
-    auto epilogue = [&](int j) {
-      if (!mbar_wait(&S.o_full[j & 1], (j >> 1) & 1)) ok = false;
-      tc_fence_after();
+    l = S.lpart[0][hr] + S.lpart[1][hr];
+    if (half == 0) {
+      // ----------------------------------------------------- epilogues --
+      // O / l of block j from its TMEM buffer to bf16 partials, stored in groups of 8
+      // dims with heads innermost ([b][s][dim/8][head][8]): the 32 heads of a warp
+      // write one contiguous 512-byte run per store
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + j * 8) * 128 * 8 + (int64_t)h * 8;
-      uint32_t r[32], r2[32];
-      const uint32_t ob = trow + ((j & 1) ? 192u : 64u);
-      tmem_ld32(ob, r);
-      tmem_ld32(ob + 32, r2);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&S.o_empty[j & 1]);                  // the values are in registers
-      auto store_o = [&](int c0, const uint32_t (&v)[32]) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 32; q += 2) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(v[q]) * inv, __uint_as_float(v[q + 1]) * inv);
-          pk[q >> 1] = *reinterpret_cast<uint32_t *>(&v2);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)                    // dims 64 j + c0 + 8q .. + 7
-          *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      };
-      store_o(0, r);
-      store_o(32, r2);
-    };
-    for (int vc = 0; vc < TC_NV; ++vc) {
-      // stage vc was issued earlier; wait for it (later groups may stay in flight):
-      // groups issued after stage vc so far: vc+1 .. vc+TC_VST-2 (refills lag one iteration)
-      cp_async_wait_upto(max(0, min(TC_VST - 2, TC_NV - 1 - vc)));
-      fence_proxy_async_smem();
-      mbar_arrive(&S.vfull[vc % TC_VST]);
-      // refill the buffer of the stage delivered one iteration ago (likely consumed
-      // by now), not the one just delivered: the other stages stay in flight
-      if (vc >= 1 && vc - 1 + TC_VST < TC_NV) {
-        const int pv = vc - 1;
-        if (!mbar_wait(&S.vempty[pv % TC_VST], (pv / TC_VST) & 1)) { ok = false; }
-        load_v(pv + TC_VST);
-      }
-      // block j = vc / TC_SPB is delivered: write out the block before it
-      if (vc % TC_SPB == TC_SPB - 1 && vc >= TC_SPB) epilogue(vc / TC_SPB - 1);
-    }
-    epilogue(TC_NV / TC_SPB - 1);
-    part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
-    part.ml[(((int64_t)b * nsplit + s) * 128 + h) * 2 + 1] = l;
-  } else if (warp > 4) {
-    // ------------------------------------------- second half of the softmax --
-    if (!mbar_wait(&S.s_full, 0)) ok = false;
-    tc_fence_after();
-    float m = 0.f, l = 0.f;
-    softmax_half(1, m, l);
-  } else if (lane == 0) {
-    // ------------------------------------------------------------- MMA --
-    constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, TC_T);
-    for (int dc = 0; dc < 9 && ok; ++dc) {
-      const int st = dc & 1;
-      if (!mbar_wait(&S.qfull[st], (dc >> 1) & 1) || !mbar_wait(&S.full[st], (dc >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint64_t ad = smem_desc(smem_u32(R + st * TC_STAGE), 16, 1024, LAYOUT_SW128);
-      const uint64_t bd = smem_desc(smem_u32(R + st * TC_STAGE + TC_QCH), 16, 1024, LAYOUT_SW128);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, id1, (dc | kk) ? 1u : 0u);
-      mma_commit(&S.empty[st]);
-    }
-    mma_commit(&S.s_full);
-    if (ok && !mbar_wait(&S.p_full, 0)) ok = false;
-    tc_fence_after();
-    // block j: O_j[128 x 64] = P[128 x 256] . V[256 x 64 dims of block j]; P from TMEM
-    constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 64);
-    for (int j = 0; j < TC_NV / TC_SPB && ok; ++j) {
-      if (j >= 2) {                                    // this buffer's previous block is written out
-        if (!mbar_wait(&S.o_empty[j & 1], ((j >> 1) - 1) & 1)) { ok = false; break; }
+      for (int j = 0; j < 8; ++j) {
+        const int ob = j & 3;
+        if (!mbar_wait(&S.o_full[ob], (j >> 2) & 1)) { ok = false; break; }
         tc_fence_after();
-      }
-      const uint32_t d = tmem + ((j & 1) ? 192u : 64u);
-      for (int s4 = 0; s4 < TC_SPB && ok; ++s4) {
-        const int vc = j * TC_SPB + s4, st = vc % TC_VST;
-        if (!mbar_wait(&S.vfull[st], (vc / TC_VST) & 1)) { ok = false; break; }
-        tc_fence_after();
+        __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + j * 8) * 128 * 8 + (int64_t)hr * 8;
+        uint32_t r[32], r2[32];
+        const uint32_t oc = trow + 64u + 128u * (uint32_t)ob;
+        tmem_ld32(oc, r);
+        tmem_ld32(oc + 32, r2);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&S.o_empty[ob]);                   // the values are in registers
+        auto store_o = [&](int c0, const uint32_t (&v)[32]) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int kk = 0; kk < TC_VROWS / 16; ++kk) {
-          const int t0 = s4 * TC_VROWS + kk * 16;      // tokens of this K-step
-          const uint64_t bd = smem_desc(smem_u32(V + st * TC_VCH + kk * 16 * 128), TC_VCH, 1024, LAYOUT_SW128);
-          mma_f16_ts(d, tmem + p_col(t0), bd, id2, (s4 | kk) ? 1u : 0u);
-        }
-        mma_commit(&S.vempty[st]);
+          for (int q = 0; q < 32; q += 2) {
+            __nv_bfloat162 v2 =
+                __floats2bfloat162_rn(__uint_as_float(v[q]) * inv, __uint_as_float(v[q + 1]) * inv);
+            pk[q >> 1] = *reinterpret_cast<uint32_t *>(&v2);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        };
+        store_o(0, r);
+        store_o(32, r2);
       }
-      mma_commit(&S.o_full[j & 1]);
+      part.ml[(((int64_t)b * nsplit + s) * 128 + hr) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
+      part.ml[(((int64_t)b * nsplit + s) * 128 + hr) * 2 + 1] = l;
     }
   }
   if (!ok) S.fail = 1;                                // a bounded wait gave up
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 256);
+  if (warp == 8) tmem_dealloc(tmem, 512);
   if (S.fail && tid < 128) {
     // this split's partial is not valid: the combine skips a split whose max is -inf
     part.ml[(((int64_t)b * nsplit + s) * 128 + tid) * 2 + 0] = -INFINITY;
@@ -644,16 +602,16 @@ extern "C" echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, i
   } else if (dtype == ECHO_BF16) {
     if (Hq != 128) return ECHO_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return ECHO_ERR_INVALID_ARG;
-    const int ns = (k + TC_T - 1) / TC_T;
+    const int ns = (k + T2_T - 1) / T2_T;
     if (ns > 64) return ECHO_ERR_UNSUPPORTED;
     TcPart tp;
     tp.o = reinterpret_cast<__nv_bfloat16 *>(workspace);
     tp.ml = reinterpret_cast<float *>(tp.o + (size_t)B * ns * 128 * 512);
     CUtensorMap qmap;
     if (!make_q_map(&qmap, q, (uint64_t)B * 128)) return ECHO_ERR_CUDA;
-    ECHO_CUDA_OK(cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM));
-    mla_tc_kernel<<<dim3(ns, B), TC_THREADS, TC_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
-                                                            scale, tp);
+    ECHO_CUDA_OK(cudaFuncSetAttribute(mla_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T2_SMEM));
+    mla_tc2_kernel<<<dim3(ns, B), T2_THREADS, T2_SMEM, st>>>(qmap, (const __nv_bfloat16 *)kv, kv_rows, slot_idx, k,
+                                                             scale, tp);
     ECHO_LAUNCH_OK();
     // the partials' lines are dropped after the merge when they are whole lines
     const int drop = (reinterpret_cast<uintptr_t>(workspace) & 127) == 0;
