@@ -285,7 +285,13 @@ def run_echo(args, ws, rank, local):
     total_steps = base_steps + fill_max
     prefetch = not args.no_prefetch
     scratch = SharedScratch(wl, dev, wl.cap_max)
-    L = [DecodeLayer(wl, l, dev, prefetch=prefetch, scratch=scratch, gen_device=dev) for l in range(layers)]
+    # the model-wide host pool: one pinned buffer with every layer's rows; each request's
+    # context takes one row range, shared by all layers
+    pool = E.HostPool(layers, wl.n_host, torch.float32 if wl.kv_fp32 else torch.bfloat16)
+    host_base = [pool.alloc(c + wl.steps + 8) for c in wl.ctx]
+    assert host_base == wl.host_base
+    L = [DecodeLayer(wl, l, dev, prefetch=prefetch, scratch=scratch, gen_device=dev, host_kv=pool.layer_rows(l),
+                     host_base=host_base) for l in range(layers)]
     inp = StepInputs(wl, layers, total_steps, dev, gen_device=dev)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
@@ -459,17 +465,19 @@ def run_echo(args, ws, rank, local):
             break
     n_free_at_start = [int(dl.cache.read_counters()[E.CTR_N_FREE]) for dl in L]
 
+    # pinned host copies of the e2e leg's inputs, made before the warm-up: pinning new
+    # host memory right before the timed region slowed its first steps
+    e2e_first = s_idx + n_warm + args.steps
+    for l in range(layers):
+        for s in range(e2e_first, e2e_first + args.steps):
+            h_in[(l, s)] = (inp.q_ik[l][s].cpu().pin_memory(), inp.new_ik_ik[l][s].cpu().pin_memory(),
+                            inp.new_kv[l][s].cpu().pin_memory(), inp.q_mla[l][s].cpu().pin_memory())
+
     run_pipelined(s_idx, n_warm, from_host=False)         # every graph, as timed
     s_idx += n_warm
     stream.synchronize()
     for dl in L:
         assert dl.cache.status() == 0, f"device status {dl.cache.status()} after warm-up"
-
-    e2e_first = s_idx + args.steps
-    for l in range(layers):
-        for s in range(e2e_first, e2e_first + args.steps):
-            h_in[(l, s)] = (inp.q_ik[l][s].cpu().pin_memory(), inp.new_ik_ik[l][s].cpu().pin_memory(),
-                            inp.new_kv[l][s].cpu().pin_memory(), inp.q_mla[l][s].cpu().pin_memory())
 
     # ---------------- timed region: inputs resident in HBM ----------------
     seq0 = [dl.seq_len.cpu().double() for dl in L]        # context lengths before the first timed step
@@ -560,6 +568,11 @@ def run_echo(args, ws, rank, local):
             rec["recall_us"] = [round(x, 2) for x in us["recall"]]
             per_step.append(rec)
         stages = {n + "_us": round(statistics.median(v), 2) for n, v in per.items()}
+        # every layer's cache management of a step: write-back and recall ([REV] "Experiments
+        # and results": all-layer management time; the budget is part of the step's write-back
+        # launch, the probe's separate reserve launch is left out)
+        mgmt = [sum(per[n][i] for n in ("writeback", "recall")) * layers for i in range(PROBE_STEPS)]
+        stages["all_layer_management_us"] = round(statistics.median(mgmt), 1)
         stages["how"] = "CUDA events between the stages inside a graph of the step issued through the separate " \
                         "entry points (reserve as its own launch), median of %d steps, mean over layers" % PROBE_STEPS
         mean = lambda v: (sum(v) / len(v)) if v else None
@@ -606,6 +619,7 @@ def run_echo(args, ws, rank, local):
                    "host_slots": wl.n_host, "prefetch": prefetch, "cuda_graph": True,
                    "parallelism": f"replicas x{ws}",
                    "pool_fill_steps": fill, "gpu_free_slots_at_warmup": n_free_at_start,
+                   "host_pool": f"model-wide: {layers} layers x {wl.n_host} rows in one pinned buffer",
                    "l2": "inputs larger than L2 (indexer keys %.0f MB per layer)" % (wl.batch * mean_ctx * 128 / 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": (achieved / peaks["hbm_gbs"]) if achieved else None, "traffic": traffic,
@@ -917,7 +931,9 @@ def run_prefill(args, local) -> int:
 
 
 def run_cap_sweep(args, local) -> int:
-    """Low-locality workload: miss-list size and recall time against the prefetch cap."""
+    """Low-locality workload: miss-list size and recall time against the prefetch cap,
+    for the fixed caps of the sweep and the adaptive cap (last step's transfer grown by
+    the prediction error, plus a slack, at most the sweep's largest cap)."""
     import torch
     from sparse_attention_kv_dsa_gb300 import synth as S
     from sparse_attention_kv_dsa_gb300.runtime import DecodeLayer, SharedScratch, StepInputs
@@ -927,11 +943,16 @@ def run_cap_sweep(args, local) -> int:
     wl.layers = 1
     steps = args.warmup + args.steps
     inp = StepInputs(wl, 1, steps, dev, gen_device=dev)
+    row_bytes = 576 * (4 if wl.kv_fp32 else 2)
+    caps = [(c, None) for c in (wl.cap_sweep or [0, wl.cap_max])]
+    caps.append((max(c for c, _ in caps), ADAPTIVE_SLACK))
     rows = []
-    for cap in (wl.cap_sweep or [0, wl.cap_max]):
+    for cap, slack in caps:
         sc = SharedScratch(wl, dev, max(cap, 1))
-        dl = DecodeLayer(wl, 0, dev, prefetch=cap > 0, cap_max=cap, scratch=sc, gen_device=dev)
-        acc = {"index_prefetch_us": [], "topk_us": [], "recall_us": [], "misses": [], "staged": [], "staged_hits": []}
+        dl = DecodeLayer(wl, 0, dev, prefetch=cap > 0, cap_max=cap, scratch=sc, gen_device=dev,
+                         adaptive_slack=slack)
+        acc = {"index_prefetch_us": [], "topk_us": [], "recall_us": [], "misses": [], "staged": [], "staged_hits": [],
+               "qualified": [], "cap_mean": [], "pred_err_median": []}
         for s in range(steps):
             dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
             st = stage_timing([dl], None, None, torch.cuda.current_stream(), 1, loaded=True)
@@ -940,12 +961,26 @@ def run_cap_sweep(args, local) -> int:
                 for n in ("index_prefetch_us", "topk_us", "recall_us"):
                     acc[n].append(st[n])
                 acc["misses"].append(c[10]); acc["staged"].append(c[12]); acc["staged_hits"].append(c[9])
-        rows.append({"cap": cap, **{n: statistics.median(v) for n, v in acc.items()}})
+                acc["qualified"].append(c[15])
+                acc["cap_mean"].append(float(dl.cap.float().mean()))
+                if slack is not None:
+                    acc["pred_err_median"].append(float(dl.cache.pf_pred_err.median()))
+        row = {"cap": cap if slack is None else f"adaptive (slack {slack}, at most {cap})",
+               **{n: statistics.median(v) for n, v in acc.items() if v}}
+        row["useless_prefetch_bytes"] = (row["staged"] - row["staged_hits"]) * row_bytes
+        row["final_recall_bytes"] = row["misses"] * row_bytes
+        rows.append(row)
         del dl, sc
         torch.cuda.empty_cache()
     print(json.dumps({"mode": "cap-sweep", "workload": wl.name, "steps": args.steps, "warmup": args.warmup,
-                      "per_cap": rows}), flush=True)
+                      "per_cap": rows,
+                      "how": "per step medians of one layer: rows qualified / staged during scoring / staged and "
+                             "selected, rows recalled after the top-k (misses), the mean per-request cap, and stage "
+                             "times from events between the separate entry points"}), flush=True)
     return 0
+
+
+ADAPTIVE_SLACK = 256
 
 
 def main(argv=None):

@@ -483,6 +483,53 @@ echo_status_t echo_translate_slots(const echo_cache_layer_t *layer, const int32_
                                    const int32_t *host_base, int32_t per_row_base, int32_t *out_slot,
                                    echo_stream_t stream);
 
+/*
+ * N1 -- model-wide host pool ([REV] "In-graph per-layer cache management": each
+ * layer's GPU cache is managed inside the graph, the host pool for the whole model).
+ * One pinned buffer (caller-owned, echo_host_pool_bytes long) holds every layer's
+ * host rows: layer l's rows are [l * rows_per_layer, (l + 1) * rows_per_layer) of
+ * ECHO_KV_WIDTH-wide latents.  A request's context takes the same row range in every
+ * layer, so one allocation serves all layers and the request's host_base is shared
+ * by them.  Row ranges are handed out first fit from a sorted, coalesced free list
+ * kept inside the struct (at most ECHO_HOST_POOL_MAX_RANGES free ranges).
+ * Host-side code: no CUDA call except echo_host_pool_layer.  Not thread-safe: one
+ * caller at a time per pool.
+ */
+#define ECHO_HOST_POOL_MAX_RANGES 1024
+
+typedef struct {
+  void *base;                  /* pinned host buffer                            */
+  int32_t n_layers;
+  int32_t kv_dtype;            /* ECHO_F32 or ECHO_BF16                         */
+  int64_t rows_per_layer;
+  int64_t rows_in_use;
+  int32_t n_free;              /* free ranges: ascending, disjoint, coalesced   */
+  int64_t free_first[ECHO_HOST_POOL_MAX_RANGES];
+  int64_t free_rows[ECHO_HOST_POOL_MAX_RANGES];
+} echo_host_pool_t;
+
+/* Bytes of the pinned buffer: n_layers * rows_per_layer rows of 576 elements (0 on bad sizes). */
+size_t echo_host_pool_bytes(int32_t n_layers, int64_t rows_per_layer, int32_t kv_dtype);
+
+/* Describe base as a pool of n_layers x rows_per_layer rows, all free. */
+echo_status_t echo_host_pool_init(echo_host_pool_t *pool, void *base, int32_t n_layers, int64_t rows_per_layer,
+                                  int32_t kv_dtype);
+
+/* Take `rows` consecutive rows (the lowest free range that holds them) in every layer:
+ * *first_row = their first row (a request's host_base).  ECHO_ERR_POOL_EXHAUSTED when
+ * no free range is long enough (nothing changes). */
+echo_status_t echo_host_pool_alloc(echo_host_pool_t *pool, int64_t rows, int64_t *first_row);
+
+/* Give a range back; it is merged with free neighbours.  ECHO_ERR_INVALID_ARG if it is
+ * out of range or overlaps a free range (a double free); ECHO_ERR_UNSUPPORTED if the free
+ * list would need more than ECHO_HOST_POOL_MAX_RANGES entries (nothing changes). */
+echo_status_t echo_host_pool_free(echo_host_pool_t *pool, int64_t first_row, int64_t rows);
+
+/* Layer l's rows: host pointer and device-visible pointer (cudaHostGetDevicePointer of the
+ * pinned buffer), for echo_cache_layer_t.host_kv with n_host = rows_per_layer. */
+echo_status_t echo_host_pool_layer(const echo_host_pool_t *pool, int32_t layer, void **host_rows,
+                                   void **host_rows_dev);
+
 #ifdef __cplusplus
 }
 #endif

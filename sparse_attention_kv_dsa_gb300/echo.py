@@ -61,6 +61,16 @@ class StepArgsT(ctypes.Structure):
                 ("mla_workspace_bytes", ctypes.c_size_t), ("index_events", ctypes.c_void_p * 2)]
 
 
+HOST_POOL_MAX_RANGES = 1024    # ECHO_HOST_POOL_MAX_RANGES
+
+
+class HostPoolT(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("n_layers", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("rows_per_layer", ctypes.c_int64), ("rows_in_use", ctypes.c_int64), ("n_free", ctypes.c_int32),
+                ("free_first", ctypes.c_int64 * HOST_POOL_MAX_RANGES),
+                ("free_rows", ctypes.c_int64 * HOST_POOL_MAX_RANGES)]
+
+
 # Declared signatures: name -> (restype, argtypes).  P = pointer, I = int32.
 _P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
@@ -85,6 +95,11 @@ SIGNATURES = {
     "echo_mark_tokens": (_I, [_P, _I, _I, _P, _I, _P]),
     "echo_token_list": (_I, [_P, _I, _P, _I, _P, _P]),
     "echo_translate_slots": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
+    "echo_host_pool_bytes": (_S, [_I, ctypes.c_int64, _I]),
+    "echo_host_pool_init": (_I, [_P, _P, _I, ctypes.c_int64, _I]),
+    "echo_host_pool_alloc": (_I, [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
+    "echo_host_pool_free": (_I, [_P, ctypes.c_int64, ctypes.c_int64]),
+    "echo_host_pool_layer": (_I, [_P, _I, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)]),
     "echo_cache_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "echo_cache_read_counters": (_I, [_P, ctypes.POINTER(ctypes.c_int32)]),
 }
@@ -315,3 +330,45 @@ def translate_slots(layer: LayerCache, tok, host_base, out_slot, stream=None):
     per_row = int(host_base.numel() == rows)
     check(lib().echo_translate_slots(layer.ref, ptr(tok), rows, k, ptr(host_base), per_row, ptr(out_slot),
                                      stream_handle(stream)), "translate_slots")
+
+
+# ------------------------------------------------------------- host pool --
+class HostPool:
+    """Model-wide host pool: one pinned buffer with every layer's host rows; a request's
+    rows are one range shared by all layers (echo_host_pool_*)."""
+
+    def __init__(self, n_layers: int, rows_per_layer: int, kv_dtype=torch.bfloat16, pinned: bool = True):
+        code = dtype_code(kv_dtype)
+        nbytes = int(lib().echo_host_pool_bytes(n_layers, rows_per_layer, code))
+        if nbytes == 0:
+            raise EchoError(ERR_INVALID_ARG, "host_pool_bytes")
+        self.kv_dtype, self.n_layers, self.rows_per_layer = kv_dtype, int(n_layers), int(rows_per_layer)
+        self.buf = torch.empty(n_layers, rows_per_layer, KV_WIDTH, dtype=kv_dtype, pin_memory=pinned)
+        self.struct = HostPoolT()
+        check(lib().echo_host_pool_init(ctypes.byref(self.struct), self.buf.data_ptr(), n_layers, rows_per_layer,
+                                        code), "host_pool_init")
+
+    def alloc(self, rows: int) -> int:
+        first = ctypes.c_int64()
+        check(lib().echo_host_pool_alloc(ctypes.byref(self.struct), int(rows), ctypes.byref(first)),
+              "host_pool_alloc")
+        return int(first.value)
+
+    def free(self, first_row: int, rows: int) -> None:
+        check(lib().echo_host_pool_free(ctypes.byref(self.struct), int(first_row), int(rows)), "host_pool_free")
+
+    def free_ranges(self) -> list:
+        return [(int(self.struct.free_first[i]), int(self.struct.free_rows[i])) for i in range(self.struct.n_free)]
+
+    @property
+    def rows_in_use(self) -> int:
+        return int(self.struct.rows_in_use)
+
+    def layer_rows(self, layer: int) -> torch.Tensor:
+        """Layer `layer`'s rows [rows_per_layer, 576] (a view of the pinned buffer)."""
+        host = ctypes.c_void_p()
+        check(lib().echo_host_pool_layer(ctypes.byref(self.struct), int(layer), ctypes.byref(host), None),
+              "host_pool_layer")
+        view = self.buf[layer]
+        assert view.data_ptr() == host.value
+        return view

@@ -34,7 +34,8 @@ class DecodeLayer:
     """State and buffers of one layer for a workload."""
 
     def __init__(self, wl: S.Workload, layer: int, device="cuda", *, prefetch=True, cap_max=None,
-                 scratch: SharedScratch | None = None, fill=True, gen_device=None, adaptive_slack=None):
+                 scratch: SharedScratch | None = None, fill=True, gen_device=None, adaptive_slack=None,
+                 host_kv=None, host_base=None):
         dev = torch.device(device)
         self.wl, self.layer, self.device = wl, layer, dev
         B, Lmax = wl.batch, wl.max_ctx
@@ -45,9 +46,12 @@ class DecodeLayer:
         self.prefetch = bool(prefetch) and self.cap_max > 0
         self.scratch = scratch or SharedScratch(wl, dev, max(self.cap_max, 1))
         assert self.scratch.cap_max >= self.cap_max
-        self.cache = E.LayerCache(wl.n_gpu, wl.n_host, kvdt, dev)
+        # host_kv: this layer's rows of a model-wide pool (E.HostPool.layer_rows), with the
+        # requests' host_base from its allocator; default: a pinned buffer of its own
+        self.cache = E.LayerCache(wl.n_gpu, wl.n_host, kvdt, dev, host_kv=host_kv)
         self.idx_k = torch.zeros(B, Lmax, wl.d_idx, dtype=ikdt, device=dev)
-        self.host_base = torch.tensor(wl.host_base, dtype=torch.int32, device=dev)
+        self.host_base = torch.tensor(wl.host_base if host_base is None else host_base, dtype=torch.int32,
+                                      device=dev)
         self.seq_len = torch.tensor(wl.ctx, dtype=torch.int32, device=dev)
         self.theta = torch.full((B,), math.inf, dtype=torch.float32, device=dev)
         self.cap = torch.zeros(B, dtype=torch.int32, device=dev)

@@ -122,6 +122,14 @@ def workloads() -> dict:
         d_idx=128, grid=8, w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=110_000,
         n_host=2_000_000, steps=16, rho=math.sqrt(0.5), cap_max=4096, cap_div=0,
         cap_sweep=[0, 1024, 4096, 16384])
+    # a model-sized stack: 61 layers (the pages' per-model metadata over per-layer size),
+    # 8 requests of ShareGPT-like length, a GPU pool smaller than the context so every
+    # layer evicts at the steady state
+    ctx6 = _ctx_uniform(0xEC40 + 6, 8, 16_000, 24_000)
+    out["model-61layer-b8-ctx20k"] = Workload(
+        name="model-61layer-b8-ctx20k", cfg_id=6, layers=61, batch=8, ctx=ctx6, h_idx=64, d_idx=128, grid=8,
+        w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=65_536, n_host=sum(c + 128 + 8 for c in ctx6),
+        steps=128, rho=0.97, cap_max=4096, cap_div=32)
     out["prefill-chunk2048-ctx100k"] = Workload(
         name="prefill-chunk2048-ctx100k", cfg_id=5, layers=1, batch=1, ctx=[100_000], h_idx=64,
         d_idx=128, grid=8, w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=200_000,
