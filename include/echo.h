@@ -145,6 +145,21 @@ typedef struct {
   int32_t *pf_new_rows; /* [B] or NULL                                              */
   float *pf_pred_err;   /* [B] (with pf_new_rows)                                   */
   int32_t cap_slack;
+  /* Block granularity, optional ([REV] critique: block-sparse / GQA models keep the
+   * metadata per block of tokens).  0 or 1: every host index and slot is one token.
+   * T > 1: one host index / slot holds T consecutive tokens of a request (host_kv
+   * [n_host * T, 576], gpu_kv [n_gpu * T, 576], metadata 4*n_host + 13*n_gpu bytes
+   * over blocks).  The write-back (host_base in tokens, a multiple of T per request)
+   * writes each new token to its host row.  A token that starts a block that is not
+   * resident takes a slot for it like a new token (victims: the LRU-smallest slots
+   * not touched in this step); one in the middle of a block that is not resident
+   * takes none.  After these binds, a token whose block is resident is written to the
+   * block's GPU row and touches the block (priority = this step).  The recall (host_base in blocks: host_base / T) binds and copies
+   * whole blocks; slot_idx holds block slots (echo_expand_block_slots makes the
+   * token slots attention reads).  No fused prefetch: echo_index_prefetch with a cap
+   * and echo_cache_recall with prefetched rows are rejected on such a layer, and so
+   * is echo_decode_layer_step (ECHO_ERR_UNSUPPORTED). */
+  int32_t block_tokens;
 } echo_cache_layer_t;
 
 /* Closed form of the per-layer metadata, 4*N_H + 13*N_G bytes
@@ -529,6 +544,29 @@ echo_status_t echo_host_pool_free(echo_host_pool_t *pool, int64_t first_row, int
  * pinned buffer), for echo_cache_layer_t.host_kv with n_host = rows_per_layer. */
 echo_status_t echo_host_pool_layer(const echo_host_pool_t *pool, int32_t layer, void **host_rows,
                                    void **host_rows_dev);
+
+/*
+ * N4 -- block-sparse selection ([REV] critique: block-sparse / GQA adaptation; reading
+ * R25).  echo_block_scores: for each request b and block j < ceil(seq_len[b] / T),
+ * bscores[b, j] = the largest of scores[b, j*T .. min(seq_len[b], j*T + T)); seq_len_blk[b]
+ * = ceil(seq_len[b] / T).  Then echo_topk over (bscores, seq_len_blk, k/T) selects the
+ * blocks exactly (ties to the lower block) and keeps theta as the EMA of the k/T-th
+ * block score.
+ *   scores [B, Lmax] f32; seq_len [B]; bscores [B, ceil(Lmax / T)] f32 out; seq_len_blk [B] out.
+ */
+echo_status_t echo_block_scores(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t T,
+                                float *bscores, int32_t *seq_len_blk, echo_stream_t stream);
+
+/*
+ * N4 -- token slots of the selected blocks, for echo_sparse_mla_decode over the GPU
+ * pool read as [n_gpu * T, 576]: out[b, j*T + i] = block_slot[b, j] * T + i when
+ * sel_blk[b, j] >= 0, block_slot[b, j] >= 0 and sel_blk[b, j]*T + i < seq_len[b];
+ * else -1.
+ *   sel_blk, block_slot [B, kb] i32 (the block top-k and the recall's slot_idx);
+ *   seq_len [B]; out [B, kb*T] i32.
+ */
+echo_status_t echo_expand_block_slots(const int32_t *sel_blk, const int32_t *block_slot, const int32_t *seq_len,
+                                      int32_t B, int32_t kb, int32_t T, int32_t *out, echo_stream_t stream);
 
 #ifdef __cplusplus
 }

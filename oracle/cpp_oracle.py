@@ -70,6 +70,11 @@ _SIG = {
     "orc_decode_layer_step": (_I32, [_P, _I64, _P, _P, _P, ctypes.c_int, _I64, _I64, _P, _P, _P, _P, _I64, _I64,
                                      _I64, _F, ctypes.c_int, _P, _P, _I64, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
                                      _P, _P, _P, _P, ctypes.c_int, _I64, _P, _P]),
+    "orc_block_scores": (_I64, [_P, _I64, _I64, _P]),
+    "orc_cache_writeback_blocks": (None, [_P, _P, _P, _I64, _I64, _P]),
+    "orc_decode_layer_step_blocks": (_I32, [_P, _I64, _P, _P, _I64, _P, ctypes.c_int, _I64, _I64, _P, _P, _P, _P,
+                                            _I64, _F, _P, _P, _I64, _P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                            _P]),
     "orc_order_key_f32": (None, [_P, _I64, _P]),
     "orc_prefill_buckets": (None, [_P, _I64, _F, _P]),
     "orc_prefill_histogram": (None, [_P, _I64, _F, _P]),
@@ -347,6 +352,19 @@ class LayerCache:
                                         _p(cat), _p(sh), _p(ev), ctypes.byref(nev)))
         return _recall_result(sel, sel_off, cat, sh, ev[:nev.value].copy(), st)
 
+    def writeback_blocks(self, host_base, seq_len, T: int) -> np.ndarray:
+        """Block-mode write-back (R25); seq_len grows in place.  Returns each request's
+        block of its new token."""
+        hb = _c(host_base, np.int64).reshape(-1)
+        own = isinstance(seq_len, np.ndarray) and seq_len.dtype == np.int64 and seq_len.flags.c_contiguous
+        seq = seq_len if own else np.array(seq_len, dtype=np.int64)
+        B = seq.shape[0]
+        out = np.zeros(max(B, 1), dtype=np.int64)
+        lib().orc_cache_writeback_blocks(self.ref, _p(hb), _p(seq), B, int(T), _p(out))
+        if not own:
+            seq_len[:] = seq
+        return out[:B].copy()
+
     def check_invariants(self) -> None:
         code = int(lib().orc_cache_check_invariants(self.ref))
         assert code == 0, {1: "host2gpu[gpu2host[g]] != g", 2: "gpu2host[host2gpu[h]] != h",
@@ -535,3 +553,100 @@ def prefill_block(q_blk, w_blk, keys, pos0: int, kth_pred, k: int):
     sels = [sel[j, :sel_n[j]].copy() for j in range(Q)]
     return {"scores": sc, "hist": hist, "thr": thr.astype(np.int64), "cand": cands,
             "cand_union": token_union(cands), "sel": sels, "kth": kth, "sel_union": token_union(sels)}
+
+
+# --------------------------------------------------------------------------
+# block granularity -- [REV] critique (block-sparse / GQA adaptation); reading R25
+# --------------------------------------------------------------------------
+def block_scores(scores, T: int) -> np.ndarray:
+    """Largest score of each block of T tokens (the last block may be short)."""
+    s = _c(scores, np.float64).reshape(-1)
+    L = s.shape[0]
+    out = np.zeros(max((L + T - 1) // T, 1), dtype=np.float64)
+    n = int(lib().orc_block_scores(_p(s), L, int(T), _p(out)))
+    return out[:n].copy()
+
+
+def block_tokens(sel_blocks, T: int, L: int) -> np.ndarray:
+    """Tokens of the selected blocks, in selection order, below the context length L."""
+    toks = [int(j) * T + i for j in np.asarray(sel_blocks).reshape(-1) for i in range(T) if int(j) * T + i < L]
+    return np.array(toks, dtype=np.int64)
+
+
+@dataclass
+class BlockStepResult:
+    new_block: np.ndarray
+    scores: list          # per request float32 [L_b] (tokens)
+    bscores: list         # per request float64 [ceil(L_b / T)]
+    sel: list             # per request: selected block indices (selection order)
+    kth: np.ndarray       # float32 [B]: the k/T-th block score
+    theta: np.ndarray     # float32 [B]
+    recall: RecallResult  # over blocks
+    out: np.ndarray | None
+    lse: np.ndarray | None
+
+
+def decode_layer_step_blocks(cache: LayerCache, *, host_base, seq_len, T: int, keys_of, q_idx, w_idx, theta,
+                             kb: int, alpha: float = 0.5, q_mla=None, latent_of=None,
+                             scale: float | None = None) -> BlockStepResult:
+    """One decode step in block mode (R25): orc_decode_layer_step_blocks, then attention
+    over every token of the selected blocks below the context length (host rows
+    latent_of(host token rows)).  host_base in tokens, a multiple of T per request."""
+    hb = _c(host_base, np.int64).reshape(-1)
+    assert np.all(hb % T == 0), "each request's host rows must start a block"
+    own = isinstance(seq_len, np.ndarray) and seq_len.dtype == np.int64 and seq_len.flags.c_contiguous
+    seq = seq_len if own else np.array(seq_len, dtype=np.int64)
+    B = seq.shape[0]
+    Ls = [int(x) + 1 for x in seq]
+    keys = [np.asarray(keys_of(b, Ls[b])) for b in range(B)]
+    if all(x.dtype == np.float32 for x in keys):
+        keys, kd = [np.ascontiguousarray(x) for x in keys], 1
+    else:
+        keys, kd = [_c(x, np.float64) for x in keys], 0
+    q = _c(q_idx, np.float64)
+    H, D = q.shape[1], q.shape[2]
+    w = _c(w_idx, np.float64).reshape(B, H)
+    th_in = _c(theta, np.float32).reshape(-1)
+    kptr = (ctypes.c_void_p * max(B, 1))(*[_p(x) for x in keys])
+    Lmax = max(Ls) if B else 1
+    bstride = (Lmax + T - 1) // T
+    new_b = np.zeros(max(B, 1), dtype=np.int64)
+    scores = np.zeros((max(B, 1), Lmax), dtype=np.float32)
+    bsc = np.zeros((max(B, 1), bstride), dtype=np.float64)
+    nblk = np.zeros(max(B, 1), dtype=np.int64)
+    sel = np.zeros((max(B, 1), max(int(kb), 1)), dtype=np.int64)
+    sel_n = np.zeros(max(B, 1), dtype=np.int64)
+    kth = np.zeros(max(B, 1), dtype=np.float32)
+    th_out = np.zeros(max(B, 1), dtype=np.float32)
+    cat = np.zeros((max(B, 1), max(int(kb), 1)), dtype=np.int8)
+    sh = np.zeros((max(B, 1), max(int(kb), 1)), dtype=np.int64)
+    ev = np.zeros(max(cache.n_gpu, 1), dtype=np.int64)
+    nev, bad_b, bad_t = _I64(), _I64(), _I64()
+    st = int(lib().orc_decode_layer_step_blocks(
+        cache.ref, B, _p(hb), _p(seq), int(T), kptr, kd, H, D, _p(q), _p(w), _p(th_in), _p(th_out), int(kb),
+        float(np.float32(alpha)), _p(new_b), _p(scores), Lmax, _p(bsc), bstride, _p(nblk), _p(sel), _p(sel_n),
+        _p(kth), _p(cat), _p(sh), _p(ev), ctypes.byref(nev), ctypes.byref(bad_b), ctypes.byref(bad_t)))
+    if not own:
+        seq_len[:] = seq
+    if st == -1:
+        raise ValueError(f"score not exact in float32 at request {bad_b.value}, t={bad_t.value}")
+    sels = [sel[b, :sel_n[b]].copy() for b in range(B)]
+    sel_off = np.zeros(B + 1, dtype=np.int64)
+    sel_off[1:] = np.cumsum(sel_n[:B])
+    cat_flat = np.concatenate([cat[b, :sel_n[b]] for b in range(B)] + [np.zeros(0, dtype=np.int8)])
+    sh_flat = np.concatenate([sh[b, :sel_n[b]] for b in range(B)] + [np.zeros(0, dtype=np.int64)])
+    rec = _recall_result(sels, sel_off, cat_flat, sh_flat, ev[:nev.value].copy(), st)
+    out = lse = None
+    if q_mla is not None:
+        Hq = q_mla.shape[1]
+        out = np.zeros((B, Hq, V_WIDTH))
+        lse = np.zeros((B, Hq))
+        for b in range(B):
+            toks = block_tokens(sels[b], T, Ls[b])
+            if toks.size == 0:
+                continue
+            o, l_ = sparse_mla_decode(q_mla[b], latent_of(int(hb[b]) + toks), float(scale))
+            out[b], lse[b] = o, l_
+    return BlockStepResult(new_b[:B].copy(), [scores[b, :Ls[b]].copy() for b in range(B)],
+                           [bsc[b, :nblk[b]].copy() for b in range(B)], sels, kth[:B].copy(), th_out[:B].copy(), rec,
+                           out, lse)

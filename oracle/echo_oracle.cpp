@@ -67,6 +67,19 @@
  *       error |theta - kth| / |kth| (float; 0 when either is not finite or kth = 0),
  *       cap_b = min(R7's cap, ceil((1 + e_b) * u_b) + slack); before any
  *       observation (u_b < 0) R7's cap alone.
+ *   R25 block granularity (optional): T consecutive tokens of a request form a block
+ *       (the request's host base a multiple of T), the unit of residency.  A block's
+ *       score is the largest score of its tokens; the selection is the exact top-k/T
+ *       blocks (ties to the lower block), theta the EMA of the k/T-th block score.  The
+ *       write-back writes every new token to the host pool.  First each token that
+ *       starts a block takes a slot for it (evicting the LRU-smallest block not touched
+ *       in this step if none is free), in request order; then the block that receives
+ *       each token, if resident, is touched in this step (so the binds of one step do
+ *       not depend on the order of the requests' rows).  A token in the middle of a
+ *       block that is not resident takes no slot (a later recall copies the whole block
+ *       from the host, the new token included).  Attention runs over every token of the
+ *       selected blocks below the context length.  Metadata is the per-token formula
+ *       over blocks: 4 * N_H / T + 13 * N_G / T bytes.  No fused prefetch.
  */
 
 #include <algorithm>
@@ -578,6 +591,105 @@ int32_t orc_decode_layer_step(orc_cache_t *c, int64_t B, const int64_t *host_bas
     }
     if (adaptive) ad_new_rows[b] = fresh;
   }
+  return st;
+}
+
+/* ------------------------------------------------------- block granularity --
+ * [REV] critique (adapting the design to block-sparse / GQA models: metadata per
+ * block of tokens instead of per token); reading R25. */
+
+/* Block scores: out[j] = max of scores[j*T .. min(L, j*T+T)), j < ceil(L / T). */
+int64_t orc_block_scores(const double *scores, int64_t L, int64_t T, double *out) {
+  const int64_t nb = (L + T - 1) / T;
+  for (int64_t j = 0; j < nb; ++j) {
+    double m = -kInf;
+    for (int64_t t = j * T; t < std::min(L, j * T + T); ++t) m = std::max(m, scores[t]);
+    out[j] = m;
+  }
+  return nb;
+}
+
+/* Write-back in block mode (R25, R16): begins step s.  First every new token that
+ * starts a block that is not resident takes a slot for that block, in request order
+ * (LRU victims among the slots not touched in this step); then the block that
+ * receives each new token (host row host_base[b] + seq_len[b], block that row / T),
+ * if resident now, is touched in this step.  A token in the middle of a block that is
+ * not resident takes no slot.  seq_len grows in place; new_blk gets the blocks. */
+void orc_cache_writeback_blocks(orc_cache_t *c, const int64_t *host_base, int64_t *seq_len, int64_t B, int64_t T,
+                                int64_t *new_blk) {
+  c->step += 1;
+  std::vector<char> ok(B, 0);
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t h = host_base[b] + seq_len[b];
+    const int64_t hb = h / T;
+    new_blk[b] = hb;
+    seq_len[b] += 1;
+    if (h < 0 || hb >= c->n_host) {
+      flag(c, kHostIndex);
+      continue;
+    }
+    ok[b] = 1;
+    if (h % T != 0 || c->host2gpu[hb] >= 0) continue;  /* mid-block, or already resident */
+    if (orc_cache_n_free(c) == 0) {
+      int64_t v;
+      if (orc_cache_lru_victims(c, 1, &v) == 0) {
+        flag(c, kPoolExhausted);
+        continue;
+      }
+      orc_cache_evict(c, &v, 1, nullptr);
+    }
+    bind_from(c, hb, 0);
+  }
+  for (int64_t b = 0; b < B; ++b)                       /* the receiving block is touched */
+    if (ok[b] && c->host2gpu[new_blk[b]] >= 0) c->priority[c->host2gpu[new_blk[b]]] = c->step;
+}
+
+/* One decode step in block mode (R25): write-back, token scores, block scores, exact
+ * top-k/T blocks and the EMA of the k/T-th block score, recall of the missing blocks.
+ * Arguments as orc_decode_layer_step with host_base in tokens (a multiple of T per
+ * request); outputs: scores [B, s_stride] (tokens), bscores [B, b_stride] and their
+ * counts nblk [B], sel [B, kb] (block indices) with counts sel_n, kth (k/T-th block
+ * score), theta_out, per selected block cat and slot_host (host block or -1), and the
+ * evicted host blocks.  Returns the recall's status, -1 on an inexact score. */
+int32_t orc_decode_layer_step_blocks(orc_cache_t *c, int64_t B, const int64_t *host_base, int64_t *seq_len, int64_t T,
+                                     const void *const *keys, int key_dtype, int64_t H, int64_t D,
+                                     const double *q_idx, const double *w_idx, const float *theta_in,
+                                     float *theta_out, int64_t kb, float alpha, int64_t *new_blk, float *scores,
+                                     int64_t s_stride, double *bscores, int64_t b_stride, int64_t *nblk,
+                                     int64_t *sel, int64_t *sel_n, float *kth, int8_t *cat, int64_t *slot_host,
+                                     int64_t *evicted, int64_t *n_evicted, int64_t *bad_req, int64_t *bad_tok) {
+  orc_cache_writeback_blocks(c, host_base, seq_len, B, T, new_blk);
+  std::vector<double> sd;
+  std::vector<int64_t> sel_off(B + 1, 0), sel_flat, base_blk(B);
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t L = seq_len[b];
+    sd.assign(L, 0.0);
+    orc_indexer_scores(q_idx + b * H * D, w_idx + b * H, H, D, keys[b], key_dtype, L, sd.data());
+    const int64_t bad = orc_to_f32_exact(sd.data(), L, scores + b * s_stride);
+    if (bad >= 0) {
+      *bad_req = b;
+      *bad_tok = bad;
+      return -1;
+    }
+    nblk[b] = orc_block_scores(sd.data(), L, T, bscores + b * b_stride);
+    double kv;
+    sel_n[b] = orc_topk_select(bscores + b * b_stride, nblk[b], kb, sel + b * kb, &kv);
+    kth[b] = (float)kv;
+    theta_out[b] = orc_ema_update(theta_in[b], (float)kv, alpha);
+    sel_off[b + 1] = sel_off[b] + sel_n[b];
+    for (int64_t j = 0; j < sel_n[b]; ++j) sel_flat.push_back(sel[b * kb + j]);
+    base_blk[b] = host_base[b] / T;
+  }
+  std::vector<int64_t> st_off(B + 1, 0), st_flat(1, 0);
+  std::vector<int8_t> cat_flat(sel_flat.size() + 1);
+  std::vector<int64_t> sh_flat(sel_flat.size() + 1);
+  const int32_t st = orc_cache_recall(c, B, base_blk.data(), sel_flat.data(), sel_off.data(), st_flat.data(),
+                                      st_off.data(), cat_flat.data(), sh_flat.data(), evicted, n_evicted);
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t j = 0; j < sel_n[b]; ++j) {
+      cat[b * kb + j] = cat_flat[sel_off[b] + j];
+      slot_host[b * kb + j] = sh_flat[sel_off[b] + j];
+    }
   return st;
 }
 

@@ -589,3 +589,44 @@ def prefill_block(q_blk, w_blk, keys, pos0: int, kth_pred, k: int):
         kth[j] = np.float32(kv)
     return {"scores": scores, "hist": hist, "thr": np.array(thr), "cand": cand,
             "cand_union": token_union(cand), "sel": sel, "kth": kth, "sel_union": token_union(sel)}
+
+
+
+# --------------------------------------------------------------------------
+# block granularity -- [REV] critique (block-sparse / GQA adaptation); reading R25
+# --------------------------------------------------------------------------
+def block_scores(scores, T: int) -> np.ndarray:
+    """Largest score of each block of T tokens."""
+    s = np.asarray(scores, dtype=np.float64)
+    return np.array([s[j:j + T].max() for j in range(0, s.shape[0], T)], dtype=np.float64)
+
+
+def writeback_blocks(cache: LayerCache, host_base, seq_len, T: int) -> np.ndarray:
+    """Block-mode write-back (R25) on a numpy LayerCache; seq_len grows in place.
+    New blocks take their slots first, then the receiving blocks are touched."""
+    cache.step += 1
+    out = np.zeros(len(seq_len), dtype=np.int64)
+    ok = np.zeros(len(seq_len), dtype=bool)
+    for b in range(len(seq_len)):
+        h = int(host_base[b]) + int(seq_len[b])
+        hb = h // T
+        out[b] = hb
+        seq_len[b] += 1
+        if h < 0 or hb >= cache.n_host:
+            cache._flag(ST_HOST_INDEX)
+            continue
+        ok[b] = True
+        if h % T or cache.host2gpu[hb] >= 0:
+            continue
+        if cache.n_free() == 0:
+            v = cache.lru_victims(1)
+            if v.size == 0:
+                cache._flag(ST_POOL_EXHAUSTED)
+                continue
+            cache.evict(v)
+        cache.bind(hb)
+    for b in np.nonzero(ok)[0]:
+        g = int(cache.host2gpu[out[b]])
+        if g >= 0:
+            cache.priority[g] = cache.step
+    return out

@@ -295,17 +295,31 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *warp_s
   return v;
 }
 
+// Tokens per host index / slot: 1, or T on a layer with block granularity.
+__device__ __forceinline__ int blk_tokens(const echo_cache_layer_t &L) {
+  return L.block_tokens > 1 ? L.block_tokens : 1;
+}
+
+// Does the new token at host row h need a slot of its own?  Per token: when it is not
+// resident; in blocks: when it starts its block and the block is not resident.
+__device__ __forceinline__ bool wb_needs_slot(const echo_cache_layer_t &L, int64_t h) {
+  const int T = blk_tokens(L);
+  return (h % T) == 0 && ldcg(L.host2gpu + h / T) < 0;
+}
+
 // Write-back of request b's new token by one warp (A1): its host pool row, its GPU slot
 // row if it has a slot (its binding is visible), its indexer key; the prefetch budget
-// of the step when the call carries one; the request's length grows by one.
+// of the step when the call carries one; the request's length grows by one.  In block
+// mode the GPU row is the token's row in its block's slot.
 __device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int lane, int32_t step) {
   const echo_cache_layer_t &L = P.L;
   int32_t *ctr = L.counters;
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
   const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
   const int32_t l = P.seq_len[b];
+  const int T = blk_tokens(L);
   const int64_t h = (int64_t)P.host_base[b] + l;
-  const bool bad_h = h < 0 || h >= L.n_host, bad_l = l >= P.Lmax;
+  const bool bad_h = h < 0 || h >= (int64_t)L.n_host * T, bad_l = l >= P.Lmax;
   if (P.rs_cap && lane == 0) {                           // budget from the length after this write-back
     const int32_t len = (bad_h || bad_l) ? l : l + 1;
     P.rs_cap[b] = budget_cap(L, b, len, P.rs_cap_max, P.rs_cap_div);
@@ -313,17 +327,18 @@ __device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int 
   }
   if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); return; }
   if (bad_l) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); return; }
-  const int32_t g = __ldcg(L.host2gpu + h);
+  const int32_t g = __ldcg(L.host2gpu + h / T);
   const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + (int64_t)b * KV_W * esz);
   uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
-  uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz) : nullptr;
+  uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + ((int64_t)g * T + h % T) * KV_W * esz)
+                       : nullptr;
   for (int c = lane; c < chunks; c += 32) {
     const uint4 v = src[c];
     hdst[c] = v;
     if (gdst) gdst[c] = v;
   }
   if (g >= 0 && lane == 0) L.priority[g] = step;         // refresh an already resident token
-  if (g < 0 && lane == 0) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
+  if (g < 0 && (h % T) == 0 && lane == 0) set_status(ctr, ECHO_ERR_POOL_EXHAUSTED);
   const int kesz = P.ik_dtype == ECHO_F32 ? 4 : 1;
   const char *ks = (const char *)P.new_ik + (int64_t)b * P.D * kesz;
   char *kd = (char *)P.idx_k + ((int64_t)b * P.Lmax + l) * P.D * kesz;
@@ -420,8 +435,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     block_prefix(P.B, [&](int b) {
       const int32_t l = P.seq_len[b];
       const int64_t h = (int64_t)P.host_base[b] + l;
-      const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
-      return (ok && ldcg(L.host2gpu + h) < 0) ? 1 : 0;
+      const bool ok = h >= 0 && h < (int64_t)L.n_host * blk_tokens(L) && l < P.Lmax;
+      return (ok && wb_needs_slot(L, h)) ? 1 : 0;
     }, S.pre_a);
   } else if (P.mode == MODE_RECALL) {
     const int32_t *pfc = P.pf_count;
@@ -430,8 +445,9 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
     block_prefix(P.B, [&](int b) { return (int)ldcg(mcnt + b); }, S.pre_b);
   }
   if (P.mode == MODE_WRITEBACK || P.mode == MODE_RECALL)
-    for (int b = tid; b < P.B; b += MG_THREADS)
-      S.tok0[b] = (int64_t)P.host_base[b] + (P.mode == MODE_WRITEBACK ? P.seq_len[b] : 0);
+    for (int b = tid; b < P.B; b += MG_THREADS)   // write-back: host index of the new token's slot owner
+      S.tok0[b] = P.mode == MODE_WRITEBACK ? ((int64_t)P.host_base[b] + P.seq_len[b]) / blk_tokens(L)
+                                           : (int64_t)P.host_base[b];
   __syncthreads();
   int nA = 0, nB = 0;
   if (P.mode == MODE_WRITEBACK) nA = S.pre_a[P.B];
@@ -700,7 +716,8 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
 
   // ---- data ---------------------------------------------------------------------
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-  const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
+  const int64_t row_bytes = (int64_t)blk_tokens(L) * KV_W * esz;   // one host index / slot
+  const int chunks = (int)(row_bytes / 16);             // 72 (bf16) or 144 (f32) per token
   if (P.mode == MODE_WRITEBACK) {
     // host pool row, GPU slot row and indexer key of each new token; one warp per request
     for (int64_t b = gwarp; b < P.B; b += gwarps) writeback_row(P, (int)b, lane, step);
@@ -724,9 +741,9 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
               my_src = reinterpret_cast<const uint4 *>((const char *)P.stage_kv +
                                                        ((int64_t)b * P.cap_max + ii) * KV_W * esz);
             } else {
-              my_src = reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * KV_W * esz);
+              my_src = reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * row_bytes);
             }
-            my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * KV_W * esz);
+            my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * row_bytes);
           }
         }
       }
@@ -825,8 +842,8 @@ __global__ void __launch_bounds__(WF_THREADS, 1) wb_fast_kernel(const __grid_con
   block_prefix(P.B, [&](int b) {
     const int32_t l = P.seq_len[b];
     const int64_t h = (int64_t)P.host_base[b] + l;
-    const bool ok = h >= 0 && h < L.n_host && l < P.Lmax;
-    return (ok && ldcg(L.host2gpu + h) < 0) ? 1 : 0;
+    const bool ok = h >= 0 && h < (int64_t)L.n_host * blk_tokens(L) && l < P.Lmax;
+    return (ok && wb_needs_slot(L, h)) ? 1 : 0;
   }, pre_a);
   const int n_bind = pre_a[P.B];
   const int m_req = max(0, n_bind - n_free0);
@@ -861,7 +878,7 @@ __global__ void __launch_bounds__(WF_THREADS, 1) wb_fast_kernel(const __grid_con
         if (pre_a[mid] <= r) lo = mid; else hi = mid - 1;
       }
       const int32_t g = g_i;
-      const int64_t h = (int64_t)P.host_base[lo] + P.seq_len[lo];
+      const int64_t h = ((int64_t)P.host_base[lo] + P.seq_len[lo]) / blk_tokens(L);
       L.host2gpu[gh_i] = -1;
       L.free_map[g] = 0;
       L.gpu2host[g] = (int32_t)h;
@@ -1070,6 +1087,7 @@ echo_status_t echo_cache_recall(const echo_cache_layer_t *layer, const int32_t *
   if (!layer_ok(layer) || !sel || !host_base || !miss_list || !n_miss || !slot_idx) return ECHO_ERR_INVALID_ARG;
   if (B <= 0 || B > MAXB || k <= 0) return ECHO_ERR_INVALID_ARG;
   if (pf_count && (!pf_list || !stage_kv || cap_max <= 0)) return ECHO_ERR_INVALID_ARG;
+  if (pf_count && layer->block_tokens > 1) return ECHO_ERR_UNSUPPORTED;   // no fused prefetch over blocks
   ManageParams P = {};
   P.L = *layer;
   P.mode = MODE_RECALL;

@@ -43,7 +43,8 @@ class CacheLayerT(ctypes.Structure):
                 ("host2gpu", ctypes.c_void_p), ("gpu2host", ctypes.c_void_p), ("priority", ctypes.c_void_p),
                 ("index_buf", ctypes.c_void_p), ("free_map", ctypes.c_void_p), ("counters", ctypes.c_void_p),
                 ("gpu_kv", ctypes.c_void_p), ("host_kv", ctypes.c_void_p), ("kv_dtype", ctypes.c_int32),
-                ("pf_new_rows", ctypes.c_void_p), ("pf_pred_err", ctypes.c_void_p), ("cap_slack", ctypes.c_int32)]
+                ("pf_new_rows", ctypes.c_void_p), ("pf_pred_err", ctypes.c_void_p), ("cap_slack", ctypes.c_int32),
+                ("block_tokens", ctypes.c_int32)]
 
 
 class StepArgsT(ctypes.Structure):
@@ -95,6 +96,8 @@ SIGNATURES = {
     "echo_mark_tokens": (_I, [_P, _I, _I, _P, _I, _P]),
     "echo_token_list": (_I, [_P, _I, _P, _I, _P, _P]),
     "echo_translate_slots": (_I, [_P, _P, _I, _I, _P, _I, _P, _P]),
+    "echo_block_scores": (_I, [_P, _P, _I, _I, _I, _P, _P, _P]),
+    "echo_expand_block_slots": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "echo_host_pool_bytes": (_S, [_I, ctypes.c_int64, _I]),
     "echo_host_pool_init": (_I, [_P, _P, _I, ctypes.c_int64, _I]),
     "echo_host_pool_alloc": (_I, [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
@@ -165,9 +168,13 @@ class LayerCache:
     """One layer's GPU cache: device metadata tensors, the GPU KV pool and the
     pinned host pool, described to the library by an echo_cache_layer_t."""
 
-    def __init__(self, n_gpu: int, n_host: int, kv_dtype=torch.bfloat16, device="cuda", host_kv=None):
+    def __init__(self, n_gpu: int, n_host: int, kv_dtype=torch.bfloat16, device="cuda", host_kv=None,
+                 block_tokens: int = 1):
+        """n_gpu / n_host count slots and host indices: tokens, or blocks of block_tokens
+        tokens (then the pools hold n * block_tokens rows of 576)."""
         dev = torch.device(device)
         self.n_gpu, self.n_host, self.kv_dtype = int(n_gpu), int(n_host), kv_dtype
+        self.block_tokens = T = max(int(block_tokens), 1)
         i32 = torch.int32
         self.host2gpu = torch.empty(n_host, dtype=i32, device=dev)
         self.gpu2host = torch.empty(n_gpu, dtype=i32, device=dev)
@@ -175,15 +182,16 @@ class LayerCache:
         self.index_buf = torch.empty(n_gpu, dtype=i32, device=dev)
         self.free_map = torch.empty(n_gpu, dtype=torch.uint8, device=dev)
         self.counters = torch.zeros(NUM_COUNTERS, dtype=i32, device=dev)
-        self.gpu_kv = torch.zeros(n_gpu, KV_WIDTH, dtype=kv_dtype, device=dev)
+        self.gpu_kv = torch.zeros(n_gpu * T, KV_WIDTH, dtype=kv_dtype, device=dev)
         if host_kv is None:
-            host_kv = torch.zeros(n_host, KV_WIDTH, dtype=kv_dtype, pin_memory=True)
-        assert host_kv.is_pinned() and host_kv.shape == (n_host, KV_WIDTH) and host_kv.dtype == kv_dtype
+            host_kv = torch.zeros(n_host * T, KV_WIDTH, dtype=kv_dtype, pin_memory=True)
+        assert host_kv.is_pinned() and host_kv.shape == (n_host * T, KV_WIDTH) and host_kv.dtype == kv_dtype
         self.host_kv = host_kv
         self.host_kv_dev = host_device_pointer(host_kv)
         self.struct = CacheLayerT(self.n_gpu, self.n_host, ptr(self.host2gpu), ptr(self.gpu2host),
                                   ptr(self.priority), ptr(self.index_buf), ptr(self.free_map), ptr(self.counters),
                                   ptr(self.gpu_kv), self.host_kv_dev, dtype_code(kv_dtype))
+        self.struct.block_tokens = T if T > 1 else 0
 
     @property
     def ref(self):
@@ -372,3 +380,16 @@ class HostPool:
         view = self.buf[layer]
         assert view.data_ptr() == host.value
         return view
+
+
+# ------------------------------------------------------ block granularity --
+def block_scores(scores, seq_len, T: int, bscores, seq_len_blk, stream=None):
+    B, Lmax = scores.shape
+    check(lib().echo_block_scores(ptr(scores), ptr(seq_len), B, Lmax, int(T), ptr(bscores), ptr(seq_len_blk),
+                                  stream_handle(stream)), "block_scores")
+
+
+def expand_block_slots(sel_blk, block_slot, seq_len, T: int, out, stream=None):
+    B, kb = sel_blk.shape
+    check(lib().echo_expand_block_slots(ptr(sel_blk), ptr(block_slot), ptr(seq_len), B, kb, int(T), ptr(out),
+                                        stream_handle(stream)), "expand_block_slots")

@@ -180,6 +180,87 @@ class DecodeLayer:
                 "theta": self.theta.cpu().numpy().copy()}
 
 
+class BlockDecodeLayer:
+    """One layer's decode step with block granularity: T consecutive tokens of a
+    request form one host index and one GPU slot (T rows of the pools).  The step is
+    the library's entry points in order: write-back of the new token, indexer scores,
+    block scores (largest token score of each block), exact top-kb blocks with the EMA
+    of the kb-th block score, recall of the missing blocks, the selected blocks' token
+    slots, sparse MLA over those tokens.  No fused prefetch in this mode."""
+
+    def __init__(self, wl: S.Workload, layer: int, T: int, kb: int, device="cuda", *, n_gpu_blocks=None,
+                 fill=True, gen_device=None):
+        dev = torch.device(device)
+        assert T >= 1 and kb >= 1
+        self.wl, self.layer, self.device, self.T, self.kb = wl, layer, dev, int(T), int(kb)
+        B, Lmax = wl.batch, wl.max_ctx
+        kvdt = torch.float32 if wl.kv_fp32 else torch.bfloat16
+        ikdt = torch.float32 if wl.kv_fp32 else torch.float8_e4m3fn
+        self.kvdt, self.ikdt = kvdt, ikdt
+        bases, off = [], 0                                 # block-aligned host rows per request
+        for c in wl.ctx:
+            bases.append(off)
+            off += -(-(c + wl.steps + 8) // T) * T
+        self.n_host_blocks = off // T
+        self.n_gpu_blocks = int(n_gpu_blocks if n_gpu_blocks is not None else max(wl.n_gpu // T, 1))
+        self.cache = E.LayerCache(self.n_gpu_blocks, self.n_host_blocks, kvdt, dev, block_tokens=T)
+        i32 = torch.int32
+        self.host_base = torch.tensor(bases, dtype=i32, device=dev)              # tokens
+        self.host_base_blk = torch.tensor([x // T for x in bases], dtype=i32, device=dev)
+        self.seq_len = torch.tensor(wl.ctx, dtype=i32, device=dev)
+        self.seq_len_blk = torch.zeros(B, dtype=i32, device=dev)
+        self.theta = torch.full((B,), math.inf, dtype=torch.float32, device=dev)
+        self.idx_k = torch.zeros(B, Lmax, wl.d_idx, dtype=ikdt, device=dev)
+        self.scores = torch.empty(B, Lmax, dtype=torch.float32, device=dev)
+        self.nbmax = -(-Lmax // T)
+        self.bscores = torch.empty(B, self.nbmax, dtype=torch.float32, device=dev)
+        self.sel = torch.empty(B, kb, dtype=i32, device=dev)                      # selected blocks
+        self.kth = torch.empty(B, dtype=torch.float32, device=dev)
+        self.miss_list = torch.empty(B, kb, dtype=i32, device=dev)
+        self.n_miss = torch.zeros(B, dtype=i32, device=dev)
+        self.slot_blk = torch.empty(B, kb, dtype=i32, device=dev)
+        self.slot_idx = torch.empty(B, kb * T, dtype=i32, device=dev)              # token rows of gpu_kv
+        self.out = torch.empty(B, wl.h_q, E.V_WIDTH, dtype=kvdt, device=dev)
+        self.lse = torch.empty(B, wl.h_q, dtype=torch.float32, device=dev)
+        ws = E.mla_workspace_bytes(B, wl.h_q, kb * T)
+        self.mla_ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.q_idx = torch.zeros(B, wl.h_idx, wl.d_idx, dtype=ikdt, device=dev)
+        self.w_idx = S.weights_for(wl, layer, "cpu").to(dev)
+        self.new_ik = torch.zeros(B, wl.d_idx, dtype=ikdt, device=dev)
+        self.new_kv = torch.zeros(B, E.KV_WIDTH, dtype=kvdt, device=dev)
+        self.q_mla = torch.zeros(B, wl.h_q, E.KV_WIDTH, dtype=kvdt, device=dev)
+        self.cache.reset()
+        if fill:
+            self.fill_context(gen_device=gen_device)
+
+    def fill_context(self, chunk_rows: int = 1 << 20, gen_device=None):
+        """Seeded context: every past token's indexer key (GPU) and every host row's
+        latent (row r of the pool gets the r-th latent of the stream)."""
+        wl, dev = self.wl, self.device
+        gen_dev = gen_device or (dev if dev.type == "cuda" else "cpu")
+        for b in range(wl.batch):
+            self.idx_k[b, :wl.ctx[b]] = self.to_ik(S.keys_for(wl, self.layer, b, wl.ctx[b], gen_dev))
+        n = self.cache.host_kv.shape[0]
+        for r0 in range(0, n, chunk_rows):
+            r1 = min(n, r0 + chunk_rows)
+            self.cache.host_kv[r0:r1].copy_(S.latents_for(wl, self.layer, r1 - r0, r0, gen_dev).cpu())
+        torch.cuda.synchronize(dev) if dev.type == "cuda" else None
+
+    to_ik = DecodeLayer.to_ik
+    set_step_inputs = DecodeLayer.set_step_inputs
+    load_step_inputs = DecodeLayer.load_step_inputs
+
+    def step(self, stream=None):
+        wl, c, T = self.wl, self.cache, self.T
+        E.cache_writeback(c, self.new_kv, self.new_ik, self.idx_k, self.host_base, self.seq_len, stream)
+        E.index_prefetch(self.q_idx, self.w_idx, self.idx_k, self.seq_len, self.theta, self.scores, stream=stream)
+        E.block_scores(self.scores, self.seq_len, T, self.bscores, self.seq_len_blk, stream)
+        E.topk(self.bscores, self.seq_len_blk, self.kb, self.sel, self.kth, self.theta, wl.alpha, stream)
+        E.cache_recall(c, self.sel, self.host_base_blk, self.miss_list, self.n_miss, self.slot_blk, stream=stream)
+        E.expand_block_slots(self.sel, self.slot_blk, self.seq_len, T, self.slot_idx, stream)
+        E.sparse_mla_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, self.mla_ws, stream)
+
+
 class StepIO:
     """Per-step input and output buffers of one layer beside the layer's own set
     (double buffering: a copy stream fills one set while a step computes on the

@@ -230,3 +230,26 @@ def test_adaptive_cap_steps_agree():
         _same_cache(a, b_)
         th_a, th_b = ra.theta, rb.theta
         qi = S.qidx_next(wl, 0, s, qi)
+
+
+def test_block_writeback_and_scores_agree():
+    rng = np.random.default_rng(42)
+    for trial in range(20):
+        T = int(rng.choice([2, 4, 8]))
+        ng, B = int(rng.integers(2, 12)), int(rng.integers(1, 4))
+        span = 64
+        a, b_ = O.LayerCache(ng, B * span // T), N.LayerCache(ng, B * span // T)
+        base = np.arange(B, dtype=np.int64) * span
+        seq_a = rng.integers(1, 20, B).astype(np.int64)
+        seq_b = seq_a.copy()
+        for s in range(12):
+            assert np.array_equal(a.writeback_blocks(base, seq_a, T), N.writeback_blocks(b_, base, seq_b, T))
+            _same_cache(a, b_)
+            if rng.random() < 0.5:                              # a recall of some blocks
+                sel = [rng.choice(int(seq_a[r] + T - 1) // T, size=1, replace=False) for r in range(B)]
+                ra = a.recall(sel, base // T, [np.zeros(0, dtype=np.int64)] * B)
+                rb = b_.recall(sel, base // T, [np.zeros(0, dtype=np.int64)] * B)
+                assert (ra.hits, ra.misses, ra.status) == (rb.hits, rb.misses, rb.status)
+                _same_cache(a, b_)
+        s = rng.integers(-30, 30, 200) * 0.5
+        assert np.array_equal(O.block_scores(s, T), N.block_scores(s, T))

@@ -43,7 +43,9 @@ MUTATIONS = [
      "if (c->gpu2host[g] >= 0 && c->priority[g] <= c->step) elig.push_back(g);"),
     ("selection not protected", "c->priority[g] = c->step;            /* protect: touched in this step */", ""),
     ("staged rows not bound", "for (int64_t t : staged_sorted[b]) to_bind.push_back(host_base[b] + t);", ""),
-    ("no step increment", "c->step += 1;", ""),
+    ("no step increment", "c->step += 1;\n  for (int64_t b = 0; b < B; ++b) {\n    const int64_t h = host_base[b] + seq_len[b];\n    new_h[b] = h;",
+     "for (int64_t b = 0; b < B; ++b) {\n    const int64_t h = host_base[b] + seq_len[b];\n    new_h[b] = h;"),
+    ("no step increment in block mode", "c->step += 1;\n  std::vector<char> ok(B, 0);", "std::vector<char> ok(B, 0);"),
     ("12 bytes per slot", "return 4 * n_host + 13 * n_gpu;", "return 4 * n_host + 12 * n_gpu;"),
     ("value width off by one", "out[h * v_width + v] += p * c[j * D + v];", "out[h * v_width + v] += p * c[j * D + v + 1];"),
     ("no softmax scale", "logit[j] = scale * dot;\n      if (logit[j] > m) m = logit[j];",
@@ -60,6 +62,12 @@ MUTATIONS = [
      "return std::max<int64_t>(c, 0);"),
     ("prediction error relative to theta", "return d / std::fabs(kth);", "return d / std::fabs(theta);"),
     ("transfer counts the hits", "fresh += cat[b * k + j] != 0 ? 1 : 0;", "fresh += 1;"),
+    ("block score from the first token", "for (int64_t t = j * T; t < std::min(L, j * T + T); ++t) m = std::max(m, scores[t]);",
+     "m = scores[j * T];"),
+    ("block slot taken in the middle of a block", "if (h % T != 0 || c->host2gpu[hb] >= 0) continue;",
+     "if (c->host2gpu[hb] >= 0) continue;"),
+    ("receiving block not touched", "if (ok[b] && c->host2gpu[new_blk[b]] >= 0) c->priority[c->host2gpu[new_blk[b]]] = c->step;",
+     ";"),
 ]
 
 

@@ -584,3 +584,90 @@ def test_adaptive_state_follows_the_steps():
             assert r.cap == [O.prefetch_cap(int(L), wl.cap_max, wl.cap_div) for L in seq]
         theta = r.theta
         qi = S.qidx_next(wl, 0, s, qi)
+
+
+# -------------------------------------------------- block granularity (R25) --
+def test_block_scores_are_block_maxima():
+    assert O.block_scores([1.0, 5.0, 2.0, 7.0, 3.0], 2).tolist() == [5.0, 7.0, 3.0]   # short last block
+    rng = np.random.default_rng(41)
+    for _ in range(50):
+        L, T = int(rng.integers(1, 300)), int(rng.choice([1, 4, 16, 64]))
+        s = rng.integers(-50, 50, L) * 0.25
+        assert O.block_scores(s, T).tolist() == [max(s[j:j + T]) for j in range(0, L, T)]
+
+
+def test_block_writeback_hand_sequence():
+    # T = 4, two GPU slots (blocks), one request whose host rows start at 0, 3 tokens so far:
+    #   s1: token 3, middle of block 0, not resident      -> no slot
+    #   s2: token 4 starts block 1                         -> free slot, priority 2
+    #       recall selects blocks {0, 1}: 1 protected (2), 0 missing -> the other slot (2)
+    #   s3..s5: tokens 5, 6, 7 in resident block 1        -> its priority 3, 4, 5
+    #   s6: token 8 starts block 2, no free slot           -> evict block 0 (priority 2), bind 2 (6)
+    c = O.LayerCache(2, 8)
+    seq = np.array([3], dtype=np.int64)
+    assert c.writeback_blocks([0], seq, 4).tolist() == [0] and c.resident_priority() == {}
+    assert c.writeback_blocks([0], seq, 4).tolist() == [1] and c.resident_priority() == {1: 2}
+    r = c.recall([np.array([0, 1])], [0], [np.zeros(0, dtype=np.int64)])
+    assert r.misses == [[0]] and r.hits == [[1]] and c.resident_priority() == {0: 2, 1: 2}
+    for s in (3, 4, 5):
+        c.writeback_blocks([0], seq, 4)
+        assert c.resident_priority() == {0: 2, 1: s}
+    assert c.writeback_blocks([0], seq, 4).tolist() == [2]
+    assert c.resident_priority() == {1: 5, 2: 6} and seq.tolist() == [9]
+    c.check_invariants()
+
+
+def test_block_writeback_binds_before_touching():
+    # T = 2, one GPU slot, two requests (host rows from 0 and from 100):
+    #   s1: request 0's row 0 starts block 0 -> the free slot; request 1's row 101 is mid-block 50
+    #   s2: request 1's row 102 starts block 51 and evicts block 0 (stamp 1 < 2), although
+    #       request 0's row 1 lands in block 0 in the same step: binds come before touches
+    c = O.LayerCache(1, 64)
+    seq = np.array([0, 1], dtype=np.int64)
+    assert c.writeback_blocks([0, 100], seq, 2).tolist() == [0, 50] and c.resident_priority() == {0: 1}
+    assert c.writeback_blocks([0, 100], seq, 2).tolist() == [0, 51] and c.resident_priority() == {51: 2}
+    assert c.status == 0 and seq.tolist() == [2, 3]
+    c.check_invariants()
+
+
+def test_block_metadata_closed_form():
+    # the per-token formula over blocks: 2M host rows and 200K GPU rows in blocks of 64
+    assert O.metadata_bytes(2_000_000 // 64, 200_000 // 64) == 4 * 31250 + 13 * 3125
+
+
+def test_block_decode_step_properties():
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    T, kb = 16, 6
+    wl = S.small_workload(ctx=(300, 520, 129), topk=kb * T, n_gpu=40, cap_max=0, steps=4)
+    B = wl.batch
+    base = [(hb + T - 1) // T * T for hb in wl.host_base]            # block-aligned host rows
+    n_host_blk = (base[-1] + wl.ctx[-1] + wl.steps + 8 + T) // T + 1
+    keys = [S.grid_to_float(S.keys_for(wl, 0, b, wl.max_ctx)).numpy() for b in range(B)]
+    lat = S.latents_for(wl, 0, n_host_blk * T).float().numpy()
+    c = O.LayerCache(wl.n_gpu, n_host_blk)
+    seq = np.array(wl.ctx, dtype=np.int64)
+    theta = np.full(B, np.inf, dtype=np.float32)
+    qi = S.qidx_initial(wl, 0)
+    w = S.weights_for(wl, 0).numpy()
+    for s in range(wl.steps):
+        q = S.grid_to_float(qi).numpy()
+        qm = S.qmla_for(wl, 0, s).float().numpy()
+        r = O.decode_layer_step_blocks(c, host_base=base, seq_len=seq, T=T, keys_of=lambda b, L: keys[b][:L],
+                                       q_idx=q, w_idx=w, theta=theta, kb=kb, q_mla=qm,
+                                       latent_of=lambda h: lat[h], scale=wl.scale)
+        c.check_invariants()
+        for b in range(B):
+            L = int(seq[b])
+            bs = np.array([r.scores[b][j:j + T].max() for j in range(0, L, T)], dtype=np.float64)
+            assert np.array_equal(r.bscores[b], bs)
+            order = sorted(range(bs.shape[0]), key=lambda j: (-bs[j], j))[:kb]
+            assert r.sel[b].tolist() == order
+            assert r.kth[b] == np.float32(bs[order[-1]])
+            for j in r.sel[b]:                                 # every selected block resident
+                assert c.host2gpu[base[b] // T + int(j)] >= 0
+            toks = [j * T + i for j in order for i in range(T) if j * T + i < L]
+            o, _ = O.sparse_mla_decode(qm[b], lat[base[b] + np.array(toks)], wl.scale)
+            assert np.array_equal(o, r.out[b])
+            assert r.theta[b] == O.ema_update(theta[b], r.kth[b], 0.5)
+        theta = r.theta
+        qi = S.qidx_next(wl, 0, s, qi)
