@@ -983,6 +983,88 @@ def run_cap_sweep(args, local) -> int:
 ADAPTIVE_SLACK = 256
 
 
+def run_blocks(args, local) -> int:
+    """Decode with block granularity (T tokens per host index and GPU slot, the top-k/T
+    blocks selected): every layer's step (write-back, indexer, block scores and block
+    top-k, recall of whole blocks, sparse MLA over the selected blocks' tokens)
+    captured in one CUDA Graph per step; per-replay CUDA events; per-stage times from
+    a second graph with events between the stages."""
+    import torch
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    from sparse_attention_kv_dsa_gb300.runtime import BlockDecodeLayer, StepInputs
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = S.workloads()[args.workload]
+    if args.layers:
+        wl.layers = args.layers
+    T = args.blocks
+    kb = wl.topk // T
+    steps = args.warmup + args.steps + 2
+    inp = StepInputs(wl, wl.layers, steps, dev, gen_device=dev)
+    L = [BlockDecodeLayer(wl, l, T, kb, dev, gen_device=dev) for l in range(wl.layers)]
+    st = torch.cuda.Stream(dev)
+    names = BlockDecodeLayer.STAGES
+    sev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+           for _ in range(wl.layers)]
+
+    def whole(stream, probe=False):
+        with torch.cuda.stream(stream):
+            for l, dl in enumerate(L):
+                if probe:
+                    sev[l][0].record(stream)
+                dl.step(stream, mark=(lambda i, l=l: sev[l][i + 1].record(stream)) if probe else None)
+
+    def load(s):
+        for l, dl in enumerate(L):
+            dl.load_step_inputs(inp.q_ik[l][s], inp.new_ik_ik[l][s], inp.new_kv[l][s], inp.q_mla[l][s])
+
+    load(0)
+    whole(st)                                            # first step eagerly (cold cache)
+    st.synchronize()
+    g, gp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        whole(st)
+    with torch.cuda.graph(gp, stream=st):
+        whole(st, probe=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_step, misses, hits, stage = [], [], [], {n: [] for n in names}
+    for s in range(1, steps):
+        load(s)
+        with torch.cuda.stream(st):
+            probe = s == steps - 1 or s >= args.warmup + args.steps
+            e0.record(st)
+            (gp if probe else g).replay()
+            e1.record(st)
+        st.synchronize()
+        if s < args.warmup:
+            continue
+        ctr = [dl.cache.read_counters() for dl in L]
+        if probe:
+            for l in range(wl.layers):
+                for i, n in enumerate(names):
+                    stage[n].append(sev[l][i].elapsed_time(sev[l][i + 1]) * 1e3)
+        else:
+            t_step.append(e0.elapsed_time(e1))
+            misses.append(sum(c[10] for c in ctr))
+            hits.append(sum(c[8] for c in ctr))
+    status = [dl.cache.status() for dl in L]
+    ms = statistics.median(t_step)
+    row_bytes = T * 576 * (4 if wl.kv_fp32 else 2)
+    print(json.dumps({
+        "mode": "blocks", "workload": wl.name, "layers": wl.layers, "batch": wl.batch,
+        "block_tokens": T, "blocks_selected": kb, "gpu_blocks": L[0].n_gpu_blocks, "host_blocks": L[0].n_host_blocks,
+        "steps": len(t_step), "warmup": args.warmup, "ms_per_step": ms, "step_ms": [round(x, 3) for x in t_step],
+        "tokens_per_s": wl.batch / (ms * 1e-3),
+        "stages_us_per_layer": {n + "_us": round(statistics.median(v), 2) for n, v in stage.items() if v},
+        "block_hit_rate": sum(hits) / max(sum(hits) + sum(misses), 1),
+        "recalled_blocks_per_step": statistics.median(misses),
+        "recall_bytes_per_step": statistics.median(misses) * row_bytes,
+        "device_status": status,
+        "how": "one CUDA Graph per step over every layer, CUDA events around each replay (inputs loaded "
+               "before the start event); stage times from a graph with events between the stages"}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1002,6 +1084,8 @@ def main(argv=None):
     ap.add_argument("--prefill", action="store_true",
                     help="prefill chunk indexing: serial / overlapped / candidate-prefetch pipelines "
                          "(default workload: prefill-chunk2048-ctx100k)")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="decode with block granularity: T tokens per host index and GPU slot")
     ap.add_argument("--fill-max", type=int, default=96,
                     help="untimed steps, at most, that bring the GPU pool to its steady (full) state")
     args = ap.parse_args(argv)
@@ -1016,6 +1100,9 @@ def main(argv=None):
     if args.prefill:
         args.workload = args.workload or "prefill-chunk2048-ctx100k"
         return run_prefill(args, local)
+    if args.blocks:
+        args.workload = args.workload or DEFAULT_WL
+        return run_blocks(args, local)
     args.workload = args.workload or DEFAULT_WL
     if args.impl == "reference":
         return run_reference(args, ws, rank)

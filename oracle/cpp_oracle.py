@@ -58,6 +58,7 @@ _SIG = {
     "orc_prediction_error": (_F, [_F, _F]),
     "orc_adaptive_cap": (_I64, [_I64, _I64, _I64, _I64, _F, _I64]),
     "orc_sparse_mla_decode": (None, [_P, _I64, _P, _I64, _I64, _D, _I64, _P, _P]),
+    "orc_sparse_gqa_decode": (None, [_P, _I64, _P, _I64, _I64, _D, _P, _P]),
     "orc_dense_masked_attention": (None, [_P, _I64, _P, _I64, _I64, _P, _D, _I64, _P]),
     "orc_cache_reset": (None, [_P]),
     "orc_cache_n_free": (_I64, [_P]),
@@ -219,6 +220,19 @@ def sparse_mla_decode(q, latents, scale: float, v_width: int = V_WIDTH):
     out = np.zeros((Hq, v_width), dtype=np.float64)
     lse = np.zeros(Hq, dtype=np.float64)
     lib().orc_sparse_mla_decode(_p(q), Hq, _p(c), n, D, float(scale), int(v_width), _p(out), _p(lse))
+    return out, lse
+
+
+def sparse_gqa_decode(q, rows, scale: float):
+    """Attention of one KV head's G query heads over its selected tokens (R26):
+    q [G, d], rows [n, 2d] (key then value).  Returns out [G, d], lse [G]."""
+    q = _c(q, np.float64)
+    c = _c(rows, np.float64)
+    G, d = q.shape
+    assert c.ndim == 2 and c.shape[1] == 2 * d and c.shape[0] >= 1
+    out = np.zeros((G, d), dtype=np.float64)
+    lse = np.zeros(G, dtype=np.float64)
+    lib().orc_sparse_gqa_decode(_p(q), G, _p(c), c.shape[0], d, float(scale), _p(out), _p(lse))
     return out, lse
 
 

@@ -80,6 +80,13 @@
  *       from the host, the new token included).  Attention runs over every token of the
  *       selected blocks below the context length.  Metadata is the per-token formula
  *       over blocks: 4 * N_H / T + 13 * N_G / T bytes.  No fused prefetch.
+ *   R26 several KV heads (optional): a GQA layer with n_kv KV heads of dimension d and
+ *       G query heads per KV head adds a KV-head dimension to the cache: each (request,
+ *       KV head) pair is a unit of its own (own host rows of 2d values per token: key
+ *       then value, own indexer scores and top-k, own residency), so the metadata grows
+ *       by n_kv and its per-unit rules (R1-R25) are unchanged.  Query head i of a
+ *       request attends with KV head i / G over that head's selected tokens, logits
+ *       scaled by 1/sqrt(d).
  */
 
 #include <algorithm>
@@ -276,6 +283,36 @@ void orc_sparse_mla_decode(const double *q, int64_t Hq, const double *c, int64_t
       for (int64_t v = 0; v < v_width; ++v) out[h * v_width + v] += p * c[j * D + v];
     }
     lse[h] = m + std::log(l);
+  }
+}
+
+/* Sparse attention of one KV head with several query heads (N4, reading R26: a GQA
+ * layer's KV head is its own unit of selection; its G query heads attend over the
+ * tokens selected for it).  q [G, d]; rows [n, 2d] hold each selected token's key
+ * (dims 0..d-1) and value (dims d..2d-1), n >= 1; in double:
+ *   logit_j = scale * sum_e q[e] key_j[e]
+ *   out     = sum_j softmax(logit)_j value_j,   lse = m + log(sum_j exp(logit_j - m))
+ * out [G, d], lse [G]. */
+void orc_sparse_gqa_decode(const double *q, int64_t G, const double *rows, int64_t n, int64_t d, double scale,
+                           double *out, double *lse) {
+  const int64_t w = 2 * d;
+  std::vector<double> logit(n);
+  for (int64_t g = 0; g < G; ++g) {
+    double m = -kInf;
+    for (int64_t j = 0; j < n; ++j) {
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e) dot += q[g * d + e] * rows[j * w + e];
+      logit[j] = scale * dot;
+      m = std::max(m, logit[j]);
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < n; ++j) z += std::exp(logit[j] - m);
+    for (int64_t e = 0; e < d; ++e) out[g * d + e] = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      const double p = std::exp(logit[j] - m) / z;
+      for (int64_t e = 0; e < d; ++e) out[g * d + e] += p * rows[j * w + d + e];
+    }
+    lse[g] = m + std::log(z);
   }
 }
 

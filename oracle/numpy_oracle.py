@@ -238,6 +238,19 @@ def sparse_mla_decode(q: np.ndarray, latents: np.ndarray, scale: float, v_width:
     return out, lse
 
 
+def sparse_gqa_decode(q: np.ndarray, rows: np.ndarray, scale: float):
+    """One KV head's G query heads over its selected tokens (R26), float64.
+    q [G, d]; rows [n, 2d]: key in the first d values, value in the last d."""
+    q = np.asarray(q, dtype=np.float64)
+    c = np.asarray(rows, dtype=np.float64)
+    d = q.shape[1]
+    logits = float(scale) * (q @ c[:, :d].T)           # [G, n]
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    z = e.sum(axis=1, keepdims=True)
+    return (e / z) @ c[:, d:], m[:, 0] + np.log(z[:, 0])
+
+
 def dense_masked_attention(q: np.ndarray, cache: np.ndarray, mask: np.ndarray, scale: float,
                            v_width: int = V_WIDTH):
     """Textbook dense attention over a whole cache with a boolean mask: a second,

@@ -250,15 +250,24 @@ class BlockDecodeLayer:
     set_step_inputs = DecodeLayer.set_step_inputs
     load_step_inputs = DecodeLayer.load_step_inputs
 
-    def step(self, stream=None):
+    STAGES = ("writeback", "index", "block_topk", "recall", "mla")
+
+    def step(self, stream=None, mark=None):
+        """Enqueue one step; mark(i), if given, is called after stage i of STAGES."""
         wl, c, T = self.wl, self.cache, self.T
+        mark = mark or (lambda i: None)
         E.cache_writeback(c, self.new_kv, self.new_ik, self.idx_k, self.host_base, self.seq_len, stream)
+        mark(0)
         E.index_prefetch(self.q_idx, self.w_idx, self.idx_k, self.seq_len, self.theta, self.scores, stream=stream)
+        mark(1)
         E.block_scores(self.scores, self.seq_len, T, self.bscores, self.seq_len_blk, stream)
         E.topk(self.bscores, self.seq_len_blk, self.kb, self.sel, self.kth, self.theta, wl.alpha, stream)
+        mark(2)
         E.cache_recall(c, self.sel, self.host_base_blk, self.miss_list, self.n_miss, self.slot_blk, stream=stream)
+        mark(3)
         E.expand_block_slots(self.sel, self.slot_blk, self.seq_len, T, self.slot_idx, stream)
         E.sparse_mla_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, self.mla_ws, stream)
+        mark(4)
 
 
 class StepIO:

@@ -253,3 +253,12 @@ def test_block_writeback_and_scores_agree():
                 _same_cache(a, b_)
         s = rng.integers(-30, 30, 200) * 0.5
         assert np.array_equal(O.block_scores(s, T), N.block_scores(s, T))
+
+
+def test_gqa_attention_cpp_vs_numpy():
+    rng = np.random.default_rng(64)
+    for G, d, n in ((1, 8, 1), (8, 128, 300), (16, 64, 77)):
+        q, rows = rng.standard_normal((G, d)), rng.standard_normal((n, 2 * d))
+        oc, lc = O.sparse_gqa_decode(q, rows, d ** -0.5)
+        on, ln = N.sparse_gqa_decode(q, rows, d ** -0.5)
+        assert np.allclose(oc, on, rtol=0, atol=1e-12) and np.allclose(lc, ln, rtol=0, atol=1e-12)

@@ -68,6 +68,11 @@ MUTATIONS = [
      "if (c->host2gpu[hb] >= 0) continue;"),
     ("receiving block not touched", "if (ok[b] && c->host2gpu[new_blk[b]] >= 0) c->priority[c->host2gpu[new_blk[b]]] = c->step;",
      ";"),
+    ("GQA value read from the key half", "out[g * d + e] += p * rows[j * w + d + e];",
+     "out[g * d + e] += p * rows[j * w + e];"),
+    ("GQA logits from the value half", "dot += q[g * d + e] * rows[j * w + e];",
+     "dot += q[g * d + e] * rows[j * w + d + e];"),
+    ("GQA scale dropped", "rows[j * w + e];\n      logit[j] = scale * dot;", "rows[j * w + e];\n      logit[j] = dot;"),
 ]
 
 

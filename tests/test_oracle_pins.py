@@ -671,3 +671,51 @@ def test_block_decode_step_properties():
             assert r.theta[b] == O.ema_update(theta[b], r.kth[b], 0.5)
         theta = r.theta
         qi = S.qidx_next(wl, 0, s, qi)
+
+
+# ------------------------------------------------ several KV heads (R26) --
+def test_gqa_single_token_is_its_value():
+    rng = np.random.default_rng(61)
+    q, row = rng.standard_normal((4, 16)), rng.standard_normal((1, 32))
+    out, lse = O.sparse_gqa_decode(q, row, 0.25)
+    assert np.array_equal(out, np.repeat(row[:, 16:], 4, axis=0))
+    assert np.allclose(lse, 0.25 * (q @ row[0, :16]), rtol=0, atol=1e-14)
+
+
+def test_gqa_zero_keys_average_the_values():
+    rng = np.random.default_rng(62)
+    rows = rng.standard_normal((5, 16))
+    rows[:, :8] = 0.0
+    out, lse = O.sparse_gqa_decode(rng.standard_normal((3, 8)), rows, 0.5)
+    assert np.allclose(out, np.repeat(rows[:, 8:].mean(axis=0, keepdims=True), 3, axis=0), rtol=0, atol=1e-15)
+    assert np.allclose(lse, np.log(5.0), rtol=0, atol=1e-15)
+
+
+def test_gqa_two_token_closed_form():
+    # keys e1 and 0, one head q = 3 e1, scale 0.5: logits 1.5 and 0, weights 1/(1+e^-1.5) and the rest
+    rows = np.zeros((2, 8))
+    rows[0, 0] = 1.0
+    rows[0, 4:] = [1.0, 2.0, 3.0, 4.0]
+    rows[1, 4:] = [-1.0, 0.0, 5.0, 2.0]
+    q = np.array([[3.0, 0.0, 0.0, 0.0]])
+    out, lse = O.sparse_gqa_decode(q, rows, 0.5)
+    p = 1.0 / (1.0 + math.exp(-1.5))
+    assert np.allclose(out[0], p * rows[0, 4:] + (1 - p) * rows[1, 4:], rtol=0, atol=1e-15)
+    assert abs(lse[0] - (1.5 + math.log(1.0 + math.exp(-1.5)))) < 1e-15
+
+
+def test_gqa_is_mla_with_the_key_in_the_rope_dims():
+    # an MLA row [value | zeros | key | zeros] with the query on the key's dims gives the
+    # same logits and the same weighted values (d = 64 fits into dims 512..575)
+    rng = np.random.default_rng(63)
+    d, n, G = 64, 37, 6
+    rows = rng.standard_normal((n, 2 * d))
+    q = rng.standard_normal((G, d))
+    lat = np.zeros((n, 576))
+    lat[:, :d] = rows[:, d:]
+    lat[:, 512:512 + d] = rows[:, :d]
+    q576 = np.zeros((G, 576))
+    q576[:, 512:512 + d] = q
+    o1, l1 = O.sparse_gqa_decode(q, rows, 0.125)
+    o2, l2 = O.sparse_mla_decode(q576, lat, 0.125)
+    assert np.allclose(o1, o2[:, :d], rtol=0, atol=1e-13) and np.allclose(l1, l2, rtol=0, atol=1e-13)
