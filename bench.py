@@ -1049,12 +1049,14 @@ def run_blocks(args, local) -> int:
             hits.append(sum(c[8] for c in ctr))
     status = [dl.cache.status() for dl in L]
     ms = statistics.median(t_step)
-    row_bytes = T * 576 * (4 if wl.kv_fp32 else 2)
+    row_bytes = T * wl.kv_width * (4 if wl.kv_fp32 else 2)
+    n_req = wl.batch // max(wl.kv_heads, 1)
     print(json.dumps({
-        "mode": "blocks", "workload": wl.name, "layers": wl.layers, "batch": wl.batch,
+        "mode": "blocks", "workload": wl.name, "layers": wl.layers, "batch": n_req,
+        "kv_heads": wl.kv_heads or None, "attention": "gqa" if wl.kv_heads else "mla",
         "block_tokens": T, "blocks_selected": kb, "gpu_blocks": L[0].n_gpu_blocks, "host_blocks": L[0].n_host_blocks,
         "steps": len(t_step), "warmup": args.warmup, "ms_per_step": ms, "step_ms": [round(x, 3) for x in t_step],
-        "tokens_per_s": wl.batch / (ms * 1e-3),
+        "tokens_per_s": n_req / (ms * 1e-3),
         "stages_us_per_layer": {n + "_us": round(statistics.median(v), 2) for n, v in stage.items() if v},
         "block_hit_rate": sum(hits) / max(sum(hits) + sum(misses), 1),
         "recalled_blocks_per_step": statistics.median(misses),

@@ -160,7 +160,20 @@ typedef struct {
    * and echo_cache_recall with prefetched rows are rejected on such a layer, and so
    * is echo_decode_layer_step (ECHO_ERR_UNSUPPORTED). */
   int32_t block_tokens;
+  /* Values per token row of host_kv and gpu_kv (and of the write-back's new_kv):
+   * 0 means ECHO_KV_WIDTH (576, the MLA latent).  Otherwise a positive width whose
+   * bytes are a multiple of 16, e.g. 2*d for one KV head's key and value of a GQA
+   * layer (several KV heads, [REV] critique: a KV-head dimension; reading R26: each
+   * (request, KV head) pair is a request of its own to the cache).  Layers with a
+   * width other than 576 take no fused prefetch and no echo_decode_layer_step
+   * (ECHO_ERR_UNSUPPORTED). */
+  int32_t row_elems;
 } echo_cache_layer_t;
+
+/* sizeof of the structs this header declares (echo_cache_layer_t, echo_step_args_t,
+ * echo_host_pool_t), in that order, written to out[0..2]: lets a binding check its
+ * own copy of the layouts.  Pure host function. */
+void echo_abi_struct_sizes(size_t out[3]);
 
 /* Closed form of the per-layer metadata, 4*N_H + 13*N_G bytes
  * ([REV] "In-graph per-layer cache management": 2M host / 200K GPU slots give
@@ -183,11 +196,11 @@ echo_status_t echo_cache_reset(const echo_cache_layer_t *layer, echo_stream_t st
  * management": KV is backed up to the host when generated, so eviction needs no
  * copy back; "Trade-offs": every new token is written back).
  * Begins step s = counters[STEP] + 1.  For b = 0..B-1: h = host_base[b] + seq_len[b];
- * new_kv[b] (576 values, kv_dtype) is stored to host_kv[h] and to a GPU slot (a free
+ * new_kv[b] (one row: 576 values, or the layer's row_elems; kv_dtype) is stored to host_kv[h] and to a GPU slot (a free
  * one, else the resident token with the smallest (priority, host index) among those
  * with priority < s is evicted); the slot's priority becomes s; new_ik[b] (D values,
  * ik_dtype) is appended to idx_k[b, seq_len[b]]; seq_len[b] += 1.
- *   new_kv [B,576] device; new_ik [B,D] device; idx_k [B,Lmax,D] device (in/out);
+ *   new_kv [B,row] device; new_ik [B,D] device; idx_k [B,Lmax,D] device (in/out);
  *   host_base [B], seq_len [B] device int32 (seq_len in/out).
  * Device errors: HOST_INDEX if h >= n_host; POOL_EXHAUSTED if no slot can be freed;
  * a token whose seq_len has reached Lmax is not appended (INVALID_ARG status).
@@ -346,6 +359,26 @@ echo_status_t echo_cache_recall(const echo_cache_layer_t *layer, const int32_t *
 size_t echo_sparse_mla_workspace_bytes(int32_t B, int32_t Hq, int32_t k);
 echo_status_t echo_sparse_mla_decode(const void *q, const void *kv, int32_t kv_rows, int32_t dtype,
                                      const int32_t *slot_idx, int32_t B, int32_t Hq, int32_t k,
+                                     float scale, void *out, float *lse, void *workspace,
+                                     size_t workspace_bytes, echo_stream_t stream);
+
+/*
+ * N4 -- sparse attention of a GQA layer with several KV heads ([REV] critique: a
+ * KV-head dimension; reading R26).  A group n is one (request, KV head) pair; its G
+ * query heads attend over the rows selected for it:
+ *   logit_j = scale * q[n,g,:] . kv[slot_idx[n,j], 0:d]          (-1 entries skipped)
+ *   out[n,g,:] = softmax_j(logit) . kv[slot_idx[n,j], d:2d];  lse[n,g] = log sum_j exp(logit_j)
+ *   q [NG,G,d] dtype (a request's [Hq,d] queries with query head i = h*G + g belong to
+ *   KV head h); kv [kv_rows, 2d] dtype (key then value per row, a layer's gpu_kv with
+ *   row_elems = 2d); slot_idx [NG,k]; out [NG,G,d] dtype; lse [NG,G] float32.
+ *   d = 64 or 128; 1 <= G <= 16; dtype ECHO_BF16 (tensor cores) or ECHO_F32.
+ *   workspace: echo_sparse_gqa_workspace_bytes(NG, G, d, k) bytes of device memory
+ *   (0 when the call needs none).
+ * A group with no valid entry gives out = 0 and lse = -inf.
+ */
+size_t echo_sparse_gqa_workspace_bytes(int32_t NG, int32_t G, int32_t d, int32_t k);
+echo_status_t echo_sparse_gqa_decode(const void *q, const void *kv, int32_t kv_rows, int32_t dtype,
+                                     const int32_t *slot_idx, int32_t NG, int32_t G, int32_t d, int32_t k,
                                      float scale, void *out, float *lse, void *workspace,
                                      size_t workspace_bytes, echo_stream_t stream);
 

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libecho.so")
-SOURCES = ["cache.cu", "indexer.cu", "topk.cu", "mla.cu", "step.cu", "prefill.cu", "blocks.cu", "hostpool.cpp"]
+SOURCES = ["cache.cu", "indexer.cu", "topk.cu", "mla.cu", "step.cu", "prefill.cu", "blocks.cu", "gqa.cu", "hostpool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -13,10 +13,11 @@
 
 namespace echo {
 
-// One warp per (request, block): the largest score of the block's tokens below the
-// request's length.  Block counts per request come from the first warp of each row.
-__global__ void block_scores_kernel(const float *scores, const int32_t *seq_len, int B, int Lmax, int T, int nbmax,
-                                    float *bscores, int32_t *seq_len_blk) {
+// Blocks of T >= 32 tokens: one warp per (request, block), the largest score of the
+// block's tokens below the request's length.  The first warp of each row writes the
+// request's block count.
+__global__ void block_scores_warp_kernel(const float *scores, const int32_t *seq_len, int B, int Lmax, int T,
+                                         int nbmax, float *bscores, int32_t *seq_len_blk) {
   const int lane = threadIdx.x & 31;
   const int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   if (w >= (int64_t)B * nbmax) return;
@@ -31,6 +32,23 @@ __global__ void block_scores_kernel(const float *scores, const int32_t *seq_len,
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) bscores[(int64_t)b * nbmax + j] = m;
+}
+
+// Blocks of T < 32 tokens: one thread per (request, block), grid-strided.
+__global__ void block_scores_thread_kernel(const float *scores, const int32_t *seq_len, int B, int Lmax, int T,
+                                           int nbmax, float *bscores, int32_t *seq_len_blk) {
+  const int64_t n = (int64_t)B * nbmax;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int b = (int)(i / nbmax), j = (int)(i % nbmax);
+    const int L = min(max(seq_len[b], 0), Lmax);
+    const int nb = (L + T - 1) / T;
+    if (j == 0) seq_len_blk[b] = nb;
+    if (j >= nb) continue;
+    const float *row = scores + (int64_t)b * Lmax;
+    float m = -INFINITY;
+    for (int t = j * T; t < min(L, j * T + T); ++t) m = fmaxf(m, row[t]);
+    bscores[i] = m;
+  }
 }
 
 // One thread per token position of the selected blocks.
@@ -53,9 +71,16 @@ extern "C" echo_status_t echo_block_scores(const float *scores, const int32_t *s
                                            int32_t T, float *bscores, int32_t *seq_len_blk, echo_stream_t stream) {
   if (!scores || !seq_len || !bscores || !seq_len_blk || B <= 0 || Lmax <= 0 || T <= 0) return ECHO_ERR_INVALID_ARG;
   const int nbmax = (Lmax + T - 1) / T;
-  const int64_t threads = (int64_t)B * nbmax * 32;
-  block_scores_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
-      scores, seq_len, B, Lmax, T, nbmax, bscores, seq_len_blk);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (T >= 32) {
+    const int64_t threads = (int64_t)B * nbmax * 32;
+    block_scores_warp_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(scores, seq_len, B, Lmax, T, nbmax,
+                                                                                bscores, seq_len_blk);
+  } else {
+    const int64_t n = (int64_t)B * nbmax;
+    const int grid = (int)std::min<int64_t>((n + 255) / 256, (int64_t)sm_count() * 8);
+    block_scores_thread_kernel<<<grid, 256, 0, st>>>(scores, seq_len, B, Lmax, T, nbmax, bscores, seq_len_blk);
+  }
   ECHO_LAUNCH_OK();
   return ECHO_OK;
 }

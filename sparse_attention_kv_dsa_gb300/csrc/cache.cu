@@ -315,7 +315,8 @@ __device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int 
   const echo_cache_layer_t &L = P.L;
   int32_t *ctr = L.counters;
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-  const int chunks = KV_W * esz / 16;                   // 72 (bf16) or 144 (f32)
+  const int64_t rb = (int64_t)kv_row_elems(L) * esz;   // bytes of one token row
+  const int chunks = (int)(rb / 16);                    // 72 (bf16 latent) or 144 (f32)
   const int32_t l = P.seq_len[b];
   const int T = blk_tokens(L);
   const int64_t h = (int64_t)P.host_base[b] + l;
@@ -328,10 +329,9 @@ __device__ __forceinline__ void writeback_row(const ManageParams &P, int b, int 
   if (bad_h) { if (lane == 0) set_status(ctr, ECHO_ERR_HOST_INDEX); return; }
   if (bad_l) { if (lane == 0) set_status(ctr, ECHO_ERR_INVALID_ARG); return; }
   const int32_t g = __ldcg(L.host2gpu + h / T);
-  const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + (int64_t)b * KV_W * esz);
-  uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * KV_W * esz);
-  uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + ((int64_t)g * T + h % T) * KV_W * esz)
-                       : nullptr;
+  const uint4 *src = reinterpret_cast<const uint4 *>((const char *)P.new_kv + (int64_t)b * rb);
+  uint4 *hdst = reinterpret_cast<uint4 *>((char *)L.host_kv + h * rb);
+  uint4 *gdst = g >= 0 ? reinterpret_cast<uint4 *>((char *)L.gpu_kv + ((int64_t)g * T + h % T) * rb) : nullptr;
   for (int c = lane; c < chunks; c += 32) {
     const uint4 v = src[c];
     hdst[c] = v;
@@ -716,45 +716,61 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgr_kernel(const __grid_constan
 
   // ---- data ---------------------------------------------------------------------
   const int esz = L.kv_dtype == ECHO_F32 ? 4 : 2;
-  const int64_t row_bytes = (int64_t)blk_tokens(L) * KV_W * esz;   // one host index / slot
-  const int chunks = (int)(row_bytes / 16);             // 72 (bf16) or 144 (f32) per token
+  const int64_t row_bytes = (int64_t)blk_tokens(L) * kv_row_elems(L) * esz;   // one host index / slot
+  const int chunks = (int)(row_bytes / 16);             // 72 (bf16) or 144 (f32) per latent token
   if (P.mode == MODE_WRITEBACK) {
     // host pool row, GPU slot row and indexer key of each new token; one warp per request
     for (int64_t b = gwarp; b < P.B; b += gwarps) writeback_row(P, (int)b, lane, step);
   } else if (P.mode == MODE_RECALL) {
     // rows: rank r < nA from staging, else from the host pool (zero-copy reads).
-    // Lane j < 4 resolves row r0 + j (list entry, host index, slot) so the four
-    // lookups run in parallel; then the warp moves the four rows together.
     const int n = nA + nB;
-    for (int64_t r0 = gwarp * 4; r0 < n; r0 += gwarps * 4) {
-      const uint4 *my_src = nullptr;
-      uint4 *my_dst = nullptr;
-      const int64_t r = r0 + lane;
-      if (lane < 4 && r < n) {
-        int b = 0;
-        const int64_t h = token_of((uint32_t)r, &b);
-        if (h >= 0 && h < L.n_host) {
-          const int32_t g = ldcg(L.host2gpu + h);
-          if (g >= 0) {                                     // not bound: pool exhausted
-            if (r < nA) {
-              const int ii = (int)r - S.pre_a[b];
-              my_src = reinterpret_cast<const uint4 *>((const char *)P.stage_kv +
-                                                       ((int64_t)b * P.cap_max + ii) * KV_W * esz);
-            } else {
-              my_src = reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * row_bytes);
-            }
-            my_dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * row_bytes);
-          }
-        }
+    auto resolve = [&](int64_t r, const uint4 **src, uint4 **dst) {
+      *src = nullptr;
+      *dst = nullptr;
+      int b = 0;
+      const int64_t h = token_of((uint32_t)r, &b);
+      if (h < 0 || h >= L.n_host) return;
+      const int32_t g = ldcg(L.host2gpu + h);
+      if (g < 0) return;                                  // not bound: pool exhausted
+      if (r < nA) {
+        const int ii = (int)r - S.pre_a[b];
+        *src = reinterpret_cast<const uint4 *>((const char *)P.stage_kv + ((int64_t)b * P.cap_max + ii) * KV_W * esz);
+      } else {
+        *src = reinterpret_cast<const uint4 *>((const char *)L.host_kv + h * row_bytes);
       }
-      const uint4 *src[4];
-      uint4 *dst[4];
+      *dst = reinterpret_cast<uint4 *>((char *)L.gpu_kv + (int64_t)g * row_bytes);
+    };
+    if (chunks <= 144) {
+      // token rows: lane j < 4 resolves row r0 + j (list entry, host index, slot) so
+      // the four lookups run in parallel; then the warp moves the four rows together
+      for (int64_t r0 = gwarp * 4; r0 < n; r0 += gwarps * 4) {
+        const uint4 *my_src = nullptr;
+        uint4 *my_dst = nullptr;
+        if (lane < 4 && r0 + lane < n) resolve(r0 + lane, &my_src, &my_dst);
+        const uint4 *src[4];
+        uint4 *dst[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        src[j] = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), j));
-        dst[j] = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), j));
+        for (int j = 0; j < 4; ++j) {
+          src[j] = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), j));
+          dst[j] = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), j));
+        }
+        warp_copy_rows4(src, dst, chunks);
       }
-      warp_copy_rows4(src, dst, chunks);
+    } else {
+      // rows of several KB (blocks of tokens, wide rows): one warp per 6 KB segment of
+      // a row, so that a few large rows still spread over the whole grid
+      constexpr int SEG = 384;
+      const int segs = (chunks + SEG - 1) / SEG;
+      for (int64_t u = gwarp; u < (int64_t)n * segs; u += gwarps) {
+        const int64_t r = u / segs;
+        const int c0 = (int)(u % segs) * SEG, c1 = min(chunks, c0 + SEG);
+        const uint4 *my_src = nullptr;
+        uint4 *my_dst = nullptr;
+        if (lane == 0) resolve(r, &my_src, &my_dst);
+        const uint4 *src = reinterpret_cast<const uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), 0));
+        uint4 *dst = reinterpret_cast<uint4 *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_dst), 0));
+        if (src) warp_copy_span(src, dst, c0, c1);
+      }
     }
     // slot translation for every selected entry (A10)
     for (int64_t i = gtid; i < (int64_t)P.B * P.k; i += gthreads) {
@@ -967,8 +983,11 @@ static cudaError_t run_manage(ManageParams P, cudaStream_t st) {
 }
 
 static bool layer_ok(const echo_cache_layer_t *L) {
-  return L && L->n_gpu > 0 && L->n_host > 0 && L->host2gpu && L->gpu2host && L->priority && L->index_buf &&
-         L->free_map && L->counters && L->gpu_kv && L->host_kv &&
+  if (!L || L->row_elems < 0 || L->row_elems > (1 << 16) || L->block_tokens < 0 || L->block_tokens > 4096)
+    return false;
+  const int esz = L->kv_dtype == ECHO_F32 ? 4 : 2;
+  return L->n_gpu > 0 && L->n_host > 0 && L->host2gpu && L->gpu2host && L->priority && L->index_buf &&
+         L->free_map && L->counters && L->gpu_kv && L->host_kv && (kv_row_elems(*L) * esz) % 16 == 0 &&
          (L->kv_dtype == ECHO_F32 || L->kv_dtype == ECHO_BF16) &&
          ((reinterpret_cast<uintptr_t>(L->gpu2host) | reinterpret_cast<uintptr_t>(L->priority) |
            reinterpret_cast<uintptr_t>(L->counters)) & 15) == 0;
@@ -982,6 +1001,12 @@ extern "C" {
 
 size_t echo_cache_metadata_bytes(int64_t n_host, int64_t n_gpu) {
   return (size_t)(4 * n_host + 13 * n_gpu);
+}
+
+void echo_abi_struct_sizes(size_t out[3]) {
+  out[0] = sizeof(echo_cache_layer_t);
+  out[1] = sizeof(echo_step_args_t);
+  out[2] = sizeof(echo_host_pool_t);
 }
 
 echo_status_t echo_host_device_pointer(void *host_ptr, void **dev_ptr) {
@@ -1087,7 +1112,7 @@ echo_status_t echo_cache_recall(const echo_cache_layer_t *layer, const int32_t *
   if (!layer_ok(layer) || !sel || !host_base || !miss_list || !n_miss || !slot_idx) return ECHO_ERR_INVALID_ARG;
   if (B <= 0 || B > MAXB || k <= 0) return ECHO_ERR_INVALID_ARG;
   if (pf_count && (!pf_list || !stage_kv || cap_max <= 0)) return ECHO_ERR_INVALID_ARG;
-  if (pf_count && layer->block_tokens > 1) return ECHO_ERR_UNSUPPORTED;   // no fused prefetch over blocks
+  if (pf_count && !layer_takes_prefetch(layer)) return ECHO_ERR_UNSUPPORTED;
   ManageParams P = {};
   P.L = *layer;
   P.mode = MODE_RECALL;

@@ -27,6 +27,17 @@ namespace echo {
 constexpr int KV_W = ECHO_KV_WIDTH;   // 576
 constexpr int V_W = ECHO_V_WIDTH;     // 512
 
+// Values per token row of a layer's pools: 576 unless the layer sets row_elems.
+__host__ __device__ __forceinline__ int kv_row_elems(const echo_cache_layer_t &L) {
+  return L.row_elems > 0 ? L.row_elems : KV_W;
+}
+
+// The fused prefetch stages 576-wide token rows: layers with block granularity or
+// another row width take none.
+inline bool layer_takes_prefetch(const echo_cache_layer_t *L) {
+  return L->block_tokens <= 1 && kv_row_elems(*L) == KV_W;
+}
+
 // ---------------------------------------------------------------- status --
 __device__ __forceinline__ void set_status(int32_t *counters, int32_t code) {
   if (counters) atomicCAS(counters + ECHO_CTR_STATUS, 0, code);
@@ -277,6 +288,24 @@ namespace echo {
 // Warp-cooperative copy of up to 4 rows of `chunks` 16-byte chunks each (src may be
 // host-mapped memory).  All loads of a batch are issued before any store so that
 // several rows are in flight on the host link.  Rows with a null src are skipped.
+// Chunks [c0, c1) of one row by a warp, four 16-byte loads per lane in flight.
+__device__ __forceinline__ void warp_copy_span(const uint4 *src, uint4 *dst, int c0, int c1) {
+  const int lane = threadIdx.x & 31;
+  for (int base = c0; base < c1; base += 128) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = base + lane + 32 * u;
+      if (c < c1) v[u] = __ldg(src + c);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = base + lane + 32 * u;
+      if (c < c1) dst[c] = v[u];
+    }
+  }
+}
+
 __device__ __forceinline__ void warp_copy_rows4(const uint4 *const (&src)[4], uint4 *const (&dst)[4],
                                                 int chunks) {
   const int lane = threadIdx.x & 31;

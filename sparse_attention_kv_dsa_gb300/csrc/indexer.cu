@@ -521,7 +521,7 @@ extern "C" echo_status_t echo_index_prefetch(const void *q, const float *w, cons
   if (cap) {
     if (!layer || !host_base || !pf_list || !pf_count || !stage_kv || cap_max <= 0) return ECHO_ERR_INVALID_ARG;
     if (!layer->host2gpu || !layer->host_kv || !layer->counters) return ECHO_ERR_INVALID_ARG;
-    if (layer->block_tokens > 1) return ECHO_ERR_UNSUPPORTED;     // no fused prefetch over blocks
+    if (!layer_takes_prefetch(layer)) return ECHO_ERR_UNSUPPORTED;
   }
   IxParams P = {};
   P.w = w;

@@ -14,7 +14,8 @@
 extern "C" echo_status_t echo_decode_layer_step(const echo_cache_layer_t *layer, const echo_step_args_t *a,
                                                 echo_stream_t stream) {
   if (!layer || !a) return ECHO_ERR_INVALID_ARG;
-  if (layer->block_tokens > 1) return ECHO_ERR_UNSUPPORTED;   // block layers: the entry points in order
+  // block granularity or another row width: the entry points in order
+  if (layer->block_tokens > 1 || echo::kv_row_elems(*layer) != echo::KV_W) return ECHO_ERR_UNSUPPORTED;
   const bool pf = a->prefetch != 0 && a->cap_max > 0;
   // write-back, and in the same launch the step's prefetch budget
   echo_status_t st = echo::cache_writeback_reserve(layer, a->new_kv, a->new_ik, a->idx_k, a->D, a->Lmax, a->idx_dtype,

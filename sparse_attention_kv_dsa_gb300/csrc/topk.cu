@@ -518,6 +518,7 @@ extern "C" echo_status_t echo_topk_prefetch(const float *scores, const int32_t *
                                             void *stage_kv, echo_stream_t stream) {
   if (!cap || cap_max <= 0 || !host_base || !layer || !pf_list || !pf_count || !stage_kv) return ECHO_ERR_INVALID_ARG;
   if (!layer->host2gpu || !layer->host_kv) return ECHO_ERR_INVALID_ARG;
+  if (!layer_takes_prefetch(layer)) return ECHO_ERR_UNSUPPORTED;
   const PfFix F = {seq_len, Lmax, cap, cap_max, host_base, *layer, scores, pf_list, pf_count, stage_kv};
   return launch_topk(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, F, stream);
 }

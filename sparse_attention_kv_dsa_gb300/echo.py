@@ -44,7 +44,7 @@ class CacheLayerT(ctypes.Structure):
                 ("index_buf", ctypes.c_void_p), ("free_map", ctypes.c_void_p), ("counters", ctypes.c_void_p),
                 ("gpu_kv", ctypes.c_void_p), ("host_kv", ctypes.c_void_p), ("kv_dtype", ctypes.c_int32),
                 ("pf_new_rows", ctypes.c_void_p), ("pf_pred_err", ctypes.c_void_p), ("cap_slack", ctypes.c_int32),
-                ("block_tokens", ctypes.c_int32)]
+                ("block_tokens", ctypes.c_int32), ("row_elems", ctypes.c_int32)]
 
 
 class StepArgsT(ctypes.Structure):
@@ -89,6 +89,9 @@ SIGNATURES = {
     "echo_cache_recall": (_I, [_P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "echo_sparse_mla_workspace_bytes": (_S, [_I, _I, _I]),
     "echo_sparse_mla_decode": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
+    "echo_abi_struct_sizes": (None, [_P]),
+    "echo_sparse_gqa_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "echo_sparse_gqa_decode": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "echo_sparse_mla_decode_noalloc": (_I, [_P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _P]),
     "echo_decode_layer_step": (_I, [_P, _P, _P]),
     "echo_prefill_index": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -169,12 +172,14 @@ class LayerCache:
     pinned host pool, described to the library by an echo_cache_layer_t."""
 
     def __init__(self, n_gpu: int, n_host: int, kv_dtype=torch.bfloat16, device="cuda", host_kv=None,
-                 block_tokens: int = 1):
+                 block_tokens: int = 1, row_elems: int = KV_WIDTH):
         """n_gpu / n_host count slots and host indices: tokens, or blocks of block_tokens
-        tokens (then the pools hold n * block_tokens rows of 576)."""
+        tokens (then the pools hold n * block_tokens token rows).  A token row has
+        row_elems values: the 576-wide MLA latent, or e.g. one KV head's key and value."""
         dev = torch.device(device)
         self.n_gpu, self.n_host, self.kv_dtype = int(n_gpu), int(n_host), kv_dtype
         self.block_tokens = T = max(int(block_tokens), 1)
+        self.row_elems = W = int(row_elems)
         i32 = torch.int32
         self.host2gpu = torch.empty(n_host, dtype=i32, device=dev)
         self.gpu2host = torch.empty(n_gpu, dtype=i32, device=dev)
@@ -182,16 +187,17 @@ class LayerCache:
         self.index_buf = torch.empty(n_gpu, dtype=i32, device=dev)
         self.free_map = torch.empty(n_gpu, dtype=torch.uint8, device=dev)
         self.counters = torch.zeros(NUM_COUNTERS, dtype=i32, device=dev)
-        self.gpu_kv = torch.zeros(n_gpu * T, KV_WIDTH, dtype=kv_dtype, device=dev)
+        self.gpu_kv = torch.zeros(n_gpu * T, W, dtype=kv_dtype, device=dev)
         if host_kv is None:
-            host_kv = torch.zeros(n_host * T, KV_WIDTH, dtype=kv_dtype, pin_memory=True)
-        assert host_kv.is_pinned() and host_kv.shape == (n_host * T, KV_WIDTH) and host_kv.dtype == kv_dtype
+            host_kv = torch.zeros(n_host * T, W, dtype=kv_dtype, pin_memory=True)
+        assert host_kv.is_pinned() and host_kv.shape == (n_host * T, W) and host_kv.dtype == kv_dtype
         self.host_kv = host_kv
         self.host_kv_dev = host_device_pointer(host_kv)
         self.struct = CacheLayerT(self.n_gpu, self.n_host, ptr(self.host2gpu), ptr(self.gpu2host),
                                   ptr(self.priority), ptr(self.index_buf), ptr(self.free_map), ptr(self.counters),
                                   ptr(self.gpu_kv), self.host_kv_dev, dtype_code(kv_dtype))
         self.struct.block_tokens = T if T > 1 else 0
+        self.struct.row_elems = W if W != KV_WIDTH else 0
 
     @property
     def ref(self):
@@ -291,6 +297,21 @@ def sparse_mla_decode(q, kv, slot_idx, scale: float, out, lse, workspace, stream
                                        scale, ptr(out), ptr(lse), ptr(workspace),
                                        workspace.numel() * workspace.element_size(), stream_handle(stream)),
           "sparse_mla_decode")
+
+
+def gqa_workspace_bytes(NG: int, G: int, d: int, k: int) -> int:
+    return int(lib().echo_sparse_gqa_workspace_bytes(NG, G, d, k))
+
+
+def sparse_gqa_decode(q, kv, slot_idx, scale: float, out, lse, workspace=None, stream=None):
+    """q [NG,G,d] (one group = one request's KV head), kv [rows,2d], slot_idx [NG,k]."""
+    NG, G, d = q.shape
+    k = slot_idx.shape[1]
+    ws = ptr(workspace) if workspace is not None else None
+    nb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().echo_sparse_gqa_decode(ptr(q), ptr(kv), kv.shape[0], dtype_code(q.dtype), ptr(slot_idx), NG, G, d,
+                                       k, scale, ptr(out), ptr(lse), ws, nb, stream_handle(stream)),
+          "sparse_gqa_decode")
 
 
 def decode_layer_step(layer: LayerCache, args: StepArgsT, stream=None):

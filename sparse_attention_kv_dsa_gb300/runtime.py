@@ -186,7 +186,11 @@ class BlockDecodeLayer:
     the library's entry points in order: write-back of the new token, indexer scores,
     block scores (largest token score of each block), exact top-kb blocks with the EMA
     of the kb-th block score, recall of the missing blocks, the selected blocks' token
-    slots, sparse MLA over those tokens.  No fused prefetch in this mode."""
+    slots, sparse attention over those tokens.  No fused prefetch in this mode.
+
+    With a GQA workload (wl.kv_heads > 0) every "request" of this layer is one
+    (request, KV head) group with rows of that head's key and value, and attention is
+    each group's query heads over its own selection; otherwise sparse MLA."""
 
     def __init__(self, wl: S.Workload, layer: int, T: int, kb: int, device="cuda", *, n_gpu_blocks=None,
                  fill=True, gen_device=None):
@@ -203,7 +207,8 @@ class BlockDecodeLayer:
             off += -(-(c + wl.steps + 8) // T) * T
         self.n_host_blocks = off // T
         self.n_gpu_blocks = int(n_gpu_blocks if n_gpu_blocks is not None else max(wl.n_gpu // T, 1))
-        self.cache = E.LayerCache(self.n_gpu_blocks, self.n_host_blocks, kvdt, dev, block_tokens=T)
+        self.cache = E.LayerCache(self.n_gpu_blocks, self.n_host_blocks, kvdt, dev, block_tokens=T,
+                                  row_elems=wl.kv_width)
         i32 = torch.int32
         self.host_base = torch.tensor(bases, dtype=i32, device=dev)              # tokens
         self.host_base_blk = torch.tensor([x // T for x in bases], dtype=i32, device=dev)
@@ -220,15 +225,19 @@ class BlockDecodeLayer:
         self.n_miss = torch.zeros(B, dtype=i32, device=dev)
         self.slot_blk = torch.empty(B, kb, dtype=i32, device=dev)
         self.slot_idx = torch.empty(B, kb * T, dtype=i32, device=dev)              # token rows of gpu_kv
-        self.out = torch.empty(B, wl.h_q, E.V_WIDTH, dtype=kvdt, device=dev)
+        # attention: sparse MLA, or (several KV heads) each group's query heads over its rows
+        self.gqa = wl.kv_heads > 0
+        vw = wl.q_width if self.gqa else E.V_WIDTH
+        self.out = torch.empty(B, wl.h_q, vw, dtype=kvdt, device=dev)
         self.lse = torch.empty(B, wl.h_q, dtype=torch.float32, device=dev)
-        ws = E.mla_workspace_bytes(B, wl.h_q, kb * T)
+        ws = (E.gqa_workspace_bytes(B, wl.h_q, wl.q_width, kb * T) if self.gqa
+              else E.mla_workspace_bytes(B, wl.h_q, kb * T))
         self.mla_ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self.q_idx = torch.zeros(B, wl.h_idx, wl.d_idx, dtype=ikdt, device=dev)
         self.w_idx = S.weights_for(wl, layer, "cpu").to(dev)
         self.new_ik = torch.zeros(B, wl.d_idx, dtype=ikdt, device=dev)
-        self.new_kv = torch.zeros(B, E.KV_WIDTH, dtype=kvdt, device=dev)
-        self.q_mla = torch.zeros(B, wl.h_q, E.KV_WIDTH, dtype=kvdt, device=dev)
+        self.new_kv = torch.zeros(B, wl.kv_width, dtype=kvdt, device=dev)
+        self.q_mla = torch.zeros(B, wl.h_q, wl.q_width, dtype=kvdt, device=dev)
         self.cache.reset()
         if fill:
             self.fill_context(gen_device=gen_device)
@@ -266,7 +275,12 @@ class BlockDecodeLayer:
         E.cache_recall(c, self.sel, self.host_base_blk, self.miss_list, self.n_miss, self.slot_blk, stream=stream)
         mark(3)
         E.expand_block_slots(self.sel, self.slot_blk, self.seq_len, T, self.slot_idx, stream)
-        E.sparse_mla_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, self.mla_ws, stream)
+        if self.gqa:
+            E.sparse_gqa_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, self.mla_ws,
+                                stream)
+        else:
+            E.sparse_mla_decode(self.q_mla, c.gpu_kv, self.slot_idx, wl.scale, self.out, self.lse, self.mla_ws,
+                                stream)
         mark(4)
 
 

@@ -72,6 +72,8 @@ class Workload:
     cap_sweep: list = field(default_factory=list)
     prefill_chunk: int = 0
     prefill_blocks: list = field(default_factory=list)
+    kv_width: int = 576          # values per cached token row (576: MLA latent; 2d: a KV head's key, value)
+    kv_heads: int = 0            # 0: MLA; n: GQA, every request split into n (request, KV head) groups
 
     @property
     def seed(self) -> int:
@@ -91,8 +93,13 @@ class Workload:
         return out
 
     @property
+    def q_width(self) -> int:
+        """Values per attention query head: 576 (MLA) or the KV head's dimension d."""
+        return self.kv_width // 2 if self.kv_heads else self.kv_width
+
+    @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(576.0)
+        return 1.0 / math.sqrt(float(self.q_width))
 
 
 def _ctx_uniform(seed: int, n: int, lo: int, hi: int) -> list:
@@ -101,7 +108,7 @@ def _ctx_uniform(seed: int, n: int, lo: int, hi: int) -> list:
 
 
 def workloads() -> dict:
-    """The five synthetic workloads, keyed by name."""
+    """The synthetic workloads, keyed by name."""
     w16 = [i / 16.0 for i in range(1, 17)]
     out = {}
     out["tiny-fp32-b1-ctx4k"] = Workload(
@@ -130,6 +137,13 @@ def workloads() -> dict:
         name="model-61layer-b8-ctx20k", cfg_id=6, layers=61, batch=8, ctx=ctx6, h_idx=64, d_idx=128, grid=8,
         w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=65_536, n_host=sum(c + 128 + 8 for c in ctx6),
         steps=128, rho=0.97, cap_max=4096, cap_div=32)
+    # a GQA layer with several KV heads: 16 requests x 8 KV heads (128 groups of 8 query
+    # heads, d = 128), each group selecting its own top-2048 tokens
+    ctx7 = _ctx_uniform(0xEC40 + 7, 16, 32_000, 48_000)
+    g7 = gqa_workload("gqa-b16x8kv-ctx32k-48k-2layer", ctx=ctx7, kv_heads=8, group=8, head_dim=128, h_idx=64,
+                      topk=2048, steps=64, rho=0.97, cfg_id=7)
+    g7.layers, g7.n_gpu = 2, 128 * 2048 * 3
+    out[g7.name] = g7
     out["prefill-chunk2048-ctx100k"] = Workload(
         name="prefill-chunk2048-ctx100k", cfg_id=5, layers=1, batch=1, ctx=[100_000], h_idx=64,
         d_idx=128, grid=8, w_values=w16, topk=2048, h_q=128, kv_fp32=False, n_gpu=200_000,
@@ -150,6 +164,20 @@ def small_workload(name="small-b3", *, batch=None, ctx=(700, 1500, 333), h_idx=6
                     d_idx=d_idx, grid=grid, w_values=w_values or [i / 16.0 for i in range(1, 17)],
                     topk=topk, h_q=h_q, kv_fp32=kv_fp32, n_gpu=n_gpu, n_host=n_host, steps=steps,
                     rho=rho, cap_max=cap_max, cap_div=cap_div)
+
+
+def gqa_workload(name="gqa-small", *, ctx=(700, 1500, 333), kv_heads=4, group=8, head_dim=128, h_idx=64,
+                 d_idx=128, grid=8, topk=256, kv_fp32=False, n_gpu=4096, steps=4, rho=0.9, cfg_id=101) -> Workload:
+    """A GQA layer with several KV heads: each request of context ctx[r] becomes kv_heads
+    groups (request r, KV head h) = row r * kv_heads + h of every per-group tensor, each
+    with its own indexer queries and keys, host rows of 2 * head_dim values and top-k;
+    group's queries are the request's query heads h * group .. h * group + group - 1."""
+    gctx = [c for c in ctx for _ in range(kv_heads)]
+    n_host = sum(c + steps + 8 for c in gctx) + 64
+    return Workload(name=name, cfg_id=cfg_id, layers=1, batch=len(gctx), ctx=gctx, h_idx=h_idx, d_idx=d_idx,
+                    grid=grid, w_values=[i / 16.0 for i in range(1, 17)], topk=topk, h_q=group, kv_fp32=kv_fp32,
+                    n_gpu=n_gpu, n_host=n_host, steps=steps, rho=rho, cap_max=0, cap_div=0,
+                    kv_width=2 * head_dim, kv_heads=kv_heads)
 
 
 # ---------------------------------------------------------------- draws ----
@@ -211,17 +239,17 @@ def weights_for(wl: Workload, layer: int, device="cpu") -> torch.Tensor:
 
 def latents_for(wl: Workload, layer: int, rows: int, row0: int = 0, device="cpu") -> torch.Tensor:
     dt = torch.float32 if wl.kv_fp32 else torch.bfloat16
-    return normal(mix_seed(wl.seed, P_LAT, layer, row0), (rows, 576), dt, device)
+    return normal(mix_seed(wl.seed, P_LAT, layer, row0), (rows, wl.kv_width), dt, device)
 
 
 def qmla_for(wl: Workload, layer: int, step: int, device="cpu") -> torch.Tensor:
     dt = torch.float32 if wl.kv_fp32 else torch.bfloat16
-    return normal(mix_seed(wl.seed, P_QMLA, layer, step), (wl.batch, wl.h_q, 576), dt, device)
+    return normal(mix_seed(wl.seed, P_QMLA, layer, step), (wl.batch, wl.h_q, wl.q_width), dt, device)
 
 
 def new_kv_for(wl: Workload, layer: int, step: int, device="cpu") -> torch.Tensor:
     dt = torch.float32 if wl.kv_fp32 else torch.bfloat16
-    return normal(mix_seed(wl.seed, P_NEWKV, layer, step), (wl.batch, 576), dt, device)
+    return normal(mix_seed(wl.seed, P_NEWKV, layer, step), (wl.batch, wl.kv_width), dt, device)
 
 
 def new_ik_for(wl: Workload, layer: int, step: int, device="cpu") -> torch.Tensor:

@@ -42,11 +42,18 @@ def _run(wl, T, kb, n_gpu_blocks, steps):
         for b in range(B):
             keys[b] = np.concatenate([keys[b], new_ik[b:b + 1]])
             lat[bases[b] + seq[b]] = new_kv[b]
+        q_att = inp.q_mla[0][s].float().cpu().numpy()
+        gqa = wl.kv_heads > 0
         r = O.decode_layer_step_blocks(oc, host_base=bases, seq_len=seq, T=T, keys_of=lambda b, L: keys[b][:L],
                                        q_idx=S.grid_to_float(inp.q_int[0][s].cpu()).numpy(), w_idx=w,
-                                       theta=theta, kb=kb, alpha=wl.alpha,
-                                       q_mla=inp.q_mla[0][s].float().cpu().numpy(),
+                                       theta=theta, kb=kb, alpha=wl.alpha, q_mla=None if gqa else q_att,
                                        latent_of=lambda rows: lat[rows], scale=wl.scale)
+        if gqa:                                   # each group's query heads over its own selection
+            r.out = np.zeros((B, wl.h_q, wl.q_width))
+            r.lse = np.zeros((B, wl.h_q))
+            for b in range(B):
+                toks = O.block_tokens(r.sel[b], T, int(seq[b]))
+                r.out[b], r.lse[b] = O.sparse_gqa_decode(q_att[b], lat[bases[b] + toks], wl.scale)
         theta = r.theta
         assert dl.cache.status() == r.recall.status == 0
         assert np.array_equal(dl.seq_len.cpu().numpy(), seq)
@@ -119,3 +126,15 @@ def test_single_token_blocks_match_the_token_step():
     # T = 1 is the token-granular cache without prefetch
     wl = S.small_workload(ctx=(700, 1500, 333), topk=256, n_gpu=1024, cap_max=0, steps=4)
     _run(wl, 1, 256, 1024, wl.steps)
+
+
+# ------------------------------------------------ several KV heads (R26) --
+def test_gqa_groups_in_blocks_of_16_bf16():
+    # 3 requests x 4 KV heads = 12 groups, 8 query heads each, d = 128
+    wl = S.gqa_workload(ctx=(300, 520, 129), kv_heads=4, group=8, head_dim=128, topk=96, steps=6)
+    assert _run(wl, 16, 6, 90, wl.steps) > 0
+
+
+def test_gqa_token_granular_fp32_d64():
+    wl = S.gqa_workload(ctx=(700, 333), kv_heads=2, group=16, head_dim=64, topk=300, kv_fp32=True, steps=4)
+    _run(wl, 1, 300, 2048, wl.steps)

@@ -13,7 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "echo.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:echo_status_t|size_t|int32_t)\s+(echo_\w+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:echo_status_t|size_t|int32_t|void)\s+(echo_\w+)\s*\(", src, flags=re.M)))
 
 
 def test_header_declares_the_hot_path_calls():
@@ -35,6 +35,14 @@ def test_library_builds_and_exports_every_declared_symbol():
 def test_binding_signatures_cover_the_header():
     import sparse_attention_kv_dsa_gb300.echo as E
     assert set(E.SIGNATURES) == set(declared_functions())
+
+
+def test_binding_struct_layouts_match_the_library():
+    import ctypes as C
+    import sparse_attention_kv_dsa_gb300.echo as E
+    out = (C.c_size_t * 3)()
+    E.lib().echo_abi_struct_sizes(out)
+    assert list(out) == [C.sizeof(E.CacheLayerT), C.sizeof(E.StepArgsT), C.sizeof(E.HostPoolT)]
 
 
 def test_metadata_closed_form_through_the_abi():
