@@ -7,7 +7,9 @@
 //   "Key observations", Obs. 2 (Fig 7-8) -- the k-th score is tracked by an EMA with
 //   smoothing 0.5, which is the next step's prefetch threshold.
 //
-// One thread-block cluster (8 CTAs x 512 threads, two CTAs per SM) per request.  Each CTA holds the
+// One thread-block cluster (8 CTAs x 512 threads, two CTAs per SM) per request; when the
+// rows' clusters of 8 would not fit in one wave, the smallest cluster (1, 2 or 4 CTAs)
+// whose slices still fit in shared memory.  Each CTA holds the
 // order-preserving uint32 keys of a contiguous slice of the request's scores in
 // shared memory.  A first pass histograms a window of keys around the key of the EMA
 // threshold (the predicted k-th score) and lists, per warp and in token order, every
@@ -73,19 +75,20 @@ __device__ __forceinline__ void tk_coarse(const uint32_t *h, uint32_t *coarse) {
 // every CTA, then the 32 bins of the chosen group.  Needs 1 <= need <= the keys in the
 // histograms.  Every thread calls it after the cluster barrier that follows tk_coarse;
 // ends with a barrier.
+template <int CL>
 __device__ __forceinline__ void tk_find(const uint32_t *h, const uint32_t *coarse, uint32_t need, uint32_t *res) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     // lane L holds groups 63 - 2L (the higher) and 62 - 2L
-    uint32_t a[TK_CL], c[TK_CL];
+    uint32_t a[CL], c[CL];
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) {
+    for (uint32_t r = 0; r < CL; ++r) {
       a[r] = ld_dsmem_u32(map_dsmem(coarse + 63 - 2 * lane, r));
       c[r] = ld_dsmem_u32(map_dsmem(coarse + 62 - 2 * lane, r));
     }
     uint32_t hi = 0, lo = 0;
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) { hi += a[r]; lo += c[r]; }
+    for (uint32_t r = 0; r < CL; ++r) { hi += a[r]; lo += c[r]; }
     uint32_t incl = hi + lo;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -102,12 +105,12 @@ __device__ __forceinline__ void tk_find(const uint32_t *h, const uint32_t *coars
     g = max(__shfl_sync(0xffffffffu, g, src), 0);
     gab = __shfl_sync(0xffffffffu, gab, src);
     // lane i: bin 32 g + i
-    uint32_t fv[TK_CL];
+    uint32_t fv[CL];
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) fv[r] = ld_dsmem_u32(map_dsmem(h + 32 * g + lane, r));
+    for (uint32_t r = 0; r < CL; ++r) fv[r] = ld_dsmem_u32(map_dsmem(h + 32 * g + lane, r));
     uint32_t f = 0;
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) f += fv[r];
+    for (uint32_t r = 0; r < CL; ++r) f += fv[r];
     uint32_t sfx = f;                                      // bins 32 g + lane .. 32 g + 31
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -136,7 +139,8 @@ __device__ __forceinline__ void record_pred_err(const PfFix &F, int b, float the
   F.L.pf_pred_err[b] = ok ? __fdiv_rn(fabsf(__fsub_rn(theta, kth)), fabsf(kth)) : 0.f;
 }
 
-__global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     topk_kernel(const float *scores, const int32_t *seq_len, int Lmax, int k, int32_t *out_idx, float *kth_out,
                 float *theta, float alpha, int lcap, const __grid_constant__ PfFix F) {
   namespace cg = cooperative_groups;
@@ -146,15 +150,15 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   uint32_t *keys = reinterpret_cast<uint32_t *>(dsm + ((sizeof(TkShared) + 15) & ~size_t(15)));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
-  const int b = blockIdx.x / TK_CL;
+  const int b = blockIdx.x / CL;
   const int L = min(max(seq_len[b], 0), Lmax);
   const float *sc = scores + (int64_t)b * Lmax;
   int32_t *out = out_idx + (int64_t)b * k;
-  const int per = ((L + TK_CL - 1) / TK_CL + 3) & ~3;        // slice length, multiple of 4
+  const int per = ((L + CL - 1) / CL + 3) & ~3;        // slice length, multiple of 4
   const int t0 = min(L, (int)rank * per), t1 = min(L, t0 + per);
   const int n = t1 - t0;
   // keys live in shared memory when the slice for Lmax fits (that is what was allocated)
-  const int per_max = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
+  const int per_max = ((Lmax + CL - 1) / CL + 3) & ~3;
   const bool cached = per_max <= TK_KEYCAP;
   // per-warp candidate lists (token, key) after the keys: lcap entries per warp
   int32_t *list_t = reinterpret_cast<int32_t *>(keys + (cached ? per_max : 0));
@@ -169,7 +173,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       out[t0 + i] = t0 + i;
       mn = min(mn, f32_key(sc[t0 + i]));
     }
-    for (int i = L + (int)rank * TK_THREADS + tid; i < k; i += TK_CL * TK_THREADS) out[i] = -1;
+    for (int i = L + (int)rank * TK_THREADS + tid; i < k; i += CL * TK_THREADS) out[i] = -1;
     mn = __reduce_min_sync(0xffffffffu, mn);
     if (tid == 0) S.minkey = 0xffffffffu;
     __syncthreads();
@@ -178,7 +182,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     cluster_sync();
     if (rank == 0 && tid == 0) {
       uint32_t m = 0xffffffffu;
-      for (uint32_t r = 0; r < TK_CL; ++r) m = min(m, *cluster.map_shared_rank(&S.minkey, r));
+      for (uint32_t r = 0; r < CL; ++r) m = min(m, *cluster.map_shared_rank(&S.minkey, r));
       const float kv = L > 0 ? key_f32(m) : -INFINITY;
       kth_out[b] = kv;
       record_pred_err(F, b, theta[b], kv);
@@ -268,8 +272,8 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     cluster_sync();
     // cluster totals: keys above the window, keys in it, any list overflow
     if (tid < 32) {
-      const uint32_t ab = lane < TK_CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], lane)) : 0u;
-      const uint32_t wn = lane < TK_CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], lane)) : 0u;
+      const uint32_t ab = lane < CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], lane)) : 0u;
+      const uint32_t wn = lane < CL ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], lane)) : 0u;
       const uint32_t tab_l = __reduce_add_sync(0xffffffffu, ab & 0x7fffffffu);
       const uint32_t tot_l = __reduce_add_sync(0xffffffffu, wn);
       const uint32_t ovf_l = __reduce_or_sync(0xffffffffu, ab >> 31);
@@ -278,7 +282,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     __syncthreads();
     const uint32_t tab = S.tot_s[0], tot = S.tot_s[1], ovf = S.tot_s[2];
     if (tab < (uint32_t)k && (uint32_t)k <= tab + tot) {   // the k-th key is in the window
-      tk_find(h, S.coarse[0], (uint32_t)k - tab, S.res);
+      tk_find<CL>(h, S.coarse[0], (uint32_t)k - tab, S.res);
       prefix = wlo + (S.res[0] << 11);
       above = tab + S.res[1];
       left = 11;
@@ -303,7 +307,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     __syncthreads();
     tk_coarse(h, S.coarse[buf]);
     cluster_sync();
-    tk_find(h, S.coarse[buf], (uint32_t)k - above, S.res);
+    tk_find<CL>(h, S.coarse[buf], (uint32_t)k - above, S.res);
     prefix |= S.res[0];
     above += S.res[1];
     const uint32_t kstar = prefix;
@@ -334,14 +338,14 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     cluster_sync();
     uint32_t gt_base = 0, eq_base = 0;
     {
-      uint32_t g[TK_CL], e[TK_CL];
+      uint32_t g[CL], e[CL];
 #pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) {
+      for (uint32_t r = 0; r < CL; ++r) {
         g[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r)) : 0u;
         e[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r)) : 0u;
       }
 #pragma unroll
-      for (uint32_t r = 0; r < TK_CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
+      for (uint32_t r = 0; r < CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
     }
     uint32_t gpos = gt_base + S.warp_gt[warp];
     uint32_t epos = eq_base + S.warp_eq[warp];
@@ -385,7 +389,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     __syncthreads();
     tk_coarse(h, S.coarse[buf]);
     cluster_sync();
-    tk_find(h, S.coarse[buf], (uint32_t)k - above, S.res);
+    tk_find<CL>(h, S.coarse[buf], (uint32_t)k - above, S.res);
     prefix |= S.res[0] << shift;
     above += S.res[1];
     left = shift;
@@ -423,14 +427,14 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   cluster_sync();
   uint32_t gt_base = 0, eq_base = 0;
   {
-    uint32_t g[TK_CL], e[TK_CL];
+    uint32_t g[CL], e[CL];
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) {
+    for (uint32_t r = 0; r < CL; ++r) {
       g[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[0], r)) : 0u;
       e[r] = r < rank ? ld_dsmem_u32(map_dsmem(&S.cta_cnt[1], r)) : 0u;
     }
 #pragma unroll
-    for (uint32_t r = 0; r < TK_CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
+    for (uint32_t r = 0; r < CL; ++r) { gt_base += g[r]; eq_base += e[r]; }
   }
   uint32_t gpos = gt_base + S.warp_gt[warp];
   uint32_t epos = eq_base + S.warp_eq[warp];
@@ -461,7 +465,7 @@ __global__ void __cluster_dims__(TK_CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
 
 // Entries per warp of the candidate lists: as many as fit (up to 256) while two CTAs
 // still share an SM; 0 (no lists) when fewer than 64 fit.
-static int topk_lcap(int Lmax) {
+static int topk_lcap(int Lmax, int cl) {
   static int per_sm = 0, reserved = 0;
   if (!per_sm) {
     int dev = 0;
@@ -470,7 +474,7 @@ static int topk_lcap(int Lmax) {
     cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (per_sm <= 0) per_sm = 1;
   }
-  const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
+  const int per = ((Lmax + cl - 1) / cl + 3) & ~3;
   const long base = (long)((sizeof(TkShared) + 15) & ~size_t(15)) + (per <= TK_KEYCAP ? (long)per * 4 : 0);
   const long room = (long)per_sm / 2 - reserved - base;
   if (room <= 0) return 0;
@@ -478,8 +482,8 @@ static int topk_lcap(int Lmax) {
   return lc >= 64 ? lc : 0;
 }
 
-static size_t topk_smem(int Lmax, int lcap, bool fix) {
-  const int per = ((Lmax + TK_CL - 1) / TK_CL + 3) & ~3;
+static size_t topk_smem(int Lmax, int cl, int lcap, bool fix) {
+  const int per = ((Lmax + cl - 1) / cl + 3) & ~3;
   size_t s = (sizeof(TkShared) + 15) & ~size_t(15);
   if (per <= TK_KEYCAP) s += (size_t)per * 4;
   s += (size_t)TK_WARPS * lcap * 8;
@@ -487,18 +491,37 @@ static size_t topk_smem(int Lmax, int lcap, bool fix) {
   return s;
 }
 
+template <int CL>
+static echo_status_t run_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t k,
+                              int32_t *out_idx, float *kth, float *theta, float alpha, int lcap, size_t smem,
+                              const PfFix &F, cudaStream_t st) {
+  ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  topk_kernel<CL><<<B * CL, TK_THREADS, smem, st>>>(scores, seq_len, Lmax, k, out_idx, kth, theta, alpha, lcap, F);
+  ECHO_LAUNCH_OK();
+  return ECHO_OK;
+}
+
 static echo_status_t launch_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax, int32_t k,
                                  int32_t *out_idx, float *kth, float *theta, float alpha, const PfFix &F,
                                  echo_stream_t stream) {
   if (!scores || !seq_len || !out_idx || !kth || !theta || B <= 0 || Lmax <= 0 || k <= 0) return ECHO_ERR_INVALID_ARG;
   if (!(alpha >= 0.f && alpha <= 1.f)) return ECHO_ERR_INVALID_ARG;
-  const int lcap = topk_lcap(Lmax);
-  const size_t smem = topk_smem(Lmax, lcap, F.cap != nullptr);
-  ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  topk_kernel<<<B * TK_CL, TK_THREADS, smem, (cudaStream_t)stream>>>(scores, seq_len, Lmax, k, out_idx, kth, theta,
-                                                                     alpha, lcap, F);
-  ECHO_LAUNCH_OK();
-  return ECHO_OK;
+  // A cluster of TK_CL CTAs per row while every row's cluster fits in one wave (two CTAs
+  // per SM); with more rows, the smallest cluster whose slices still fit in shared
+  // memory, so that short rows (blocks, many groups, prefill queries) take fewer CTAs.
+  int cl = TK_CL;
+  if ((int64_t)B * TK_CL > 2 * (int64_t)sm_count())
+    for (cl = 1; cl < TK_CL && ((Lmax + cl - 1) / cl + 3) / 4 * 4 > TK_KEYCAP; cl *= 2) {
+    }
+  const int lcap = topk_lcap(Lmax, cl);
+  const size_t smem = topk_smem(Lmax, cl, lcap, F.cap != nullptr);
+  cudaStream_t st = (cudaStream_t)stream;
+  switch (cl) {
+    case 1: return run_topk<1>(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, lcap, smem, F, st);
+    case 2: return run_topk<2>(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, lcap, smem, F, st);
+    case 4: return run_topk<4>(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, lcap, smem, F, st);
+    default: return run_topk<TK_CL>(scores, seq_len, B, Lmax, k, out_idx, kth, theta, alpha, lcap, smem, F, st);
+  }
 }
 
 }  // namespace echo

@@ -143,6 +143,19 @@ def test_topk_many_rows():
     check_topk(lists, k, thetas)
 
 
+def test_topk_many_long_rows_take_smaller_clusters():
+    # more rows than clusters of eight fit in one wave, each too long for one CTA's
+    # shared memory: clusters of two; predictions inside, above and below the window
+    rng = np.random.default_rng(8)
+    n_rows = E.lib().echo_device_sm_count() // 4 + 3
+    lists = [(rng.integers(0, 2 ** 14, int(rng.integers(30_000, 46_000))) / 1024.0).astype(np.float32)
+             for _ in range(n_rows)]
+    check_topk(lists, 2048, [[math.inf, 15.6, 60.0, 1.0][r % 4] for r in range(n_rows)])
+    lists = [(rng.integers(0, 2 ** 14, int(rng.integers(70_000, 90_000))) / 1024.0).astype(np.float32)
+             for _ in range(n_rows)]                                    # clusters of four
+    check_topk(lists, 2048, [[15.6, math.inf][r % 2] for r in range(n_rows)])
+
+
 def test_topk_candidate_lists_and_their_fallbacks():
     # a prediction near the k-th score: the last pass and the output read the per-warp
     # candidate lists; ties at the k-th key spread over every warp and CTA; a window
