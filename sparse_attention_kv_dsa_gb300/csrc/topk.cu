@@ -239,8 +239,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       if (i < s1) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
       const bool ab = i < s1 && (uint64_t)kk >= whi;
       const bool inw = i < s1 && kk >= wlo && (uint64_t)kk < whi;
-      nab += __popc(__ballot_sync(0xffffffffu, ab));
-      nwin += __popc(__ballot_sync(0xffffffffu, inw));
+      nab += ab ? 1u : 0u;                                 // per lane; summed over the warp below
+      nwin += inw ? 1u : 0u;
       if (inw) atomicAdd(&h[(kk - wlo) >> 11], 1u);
       const uint32_t bal = __ballot_sync(0xffffffffu, ab || inw);
       if (ab || inw) {
@@ -252,6 +252,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       }
       nl += __popc(bal);
     }
+    nab = __reduce_add_sync(0xffffffffu, nab);
+    nwin = __reduce_add_sync(0xffffffffu, nwin);
     if (lane == 0) {
       S.warp_gt[warp] = nab;
       S.warp_eq[warp] = nwin;
@@ -314,12 +316,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     const uint32_t need_eq = (uint32_t)k - above;
     // ---- ordered output from the lists (every key >= K* is listed) ----
     uint32_t gt = 0, eq = 0;
-    for (uint32_t j0 = 0; j0 < nl; j0 += 32) {
-      const uint32_t j = j0 + lane;
-      const uint32_t kk = j < nl ? lk[j] : 0u;
-      gt += __popc(__ballot_sync(0xffffffffu, j < nl && kk > kstar));
-      eq += __popc(__ballot_sync(0xffffffffu, j < nl && kk == kstar));
+    for (uint32_t j = lane; j < nl; j += 32) {
+      const uint32_t kk = lk[j];
+      gt += kk > kstar ? 1u : 0u;
+      eq += kk == kstar ? 1u : 0u;
     }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
     if (lane == 0) { S.warp_gt[warp] = gt; S.warp_eq[warp] = eq; }
     __syncthreads();
     if (tid == 0) {
@@ -402,13 +405,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   // ---- ordered output ---------------------------------------------------
   // warp w of this CTA owns the contiguous sub-range [s0, s1) of the slice
   uint32_t gt = 0, eq = 0;
-  for (int i0 = s0; i0 < s1; i0 += 32) {
-    const int i = i0 + lane;
-    uint32_t kk = 0;
-    if (i < s1) kk = cached ? keys[i] : f32_key(sc[t0 + i]);
-    gt += __popc(__ballot_sync(0xffffffffu, i < s1 && kk > kstar));
-    eq += __popc(__ballot_sync(0xffffffffu, i < s1 && kk == kstar));
+  for (int i = s0 + lane; i < s1; i += 32) {
+    const uint32_t kk = cached ? keys[i] : f32_key(sc[t0 + i]);
+    gt += kk > kstar ? 1u : 0u;
+    eq += kk == kstar ? 1u : 0u;
   }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
   if (lane == 0) { S.warp_gt[warp] = gt; S.warp_eq[warp] = eq; }
   __syncthreads();
   if (tid == 0) {
