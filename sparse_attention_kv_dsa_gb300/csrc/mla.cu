@@ -191,17 +191,18 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 //   softmax  over all 512 entries at once: warps 0-3 read region 0, warps 4-7 region
 //            1 (one head row per thread), the row max and sum are exchanged through
 //            shared memory, and bf16 P goes back into TMEM over logits already read
-//            (tokens 128 r + c of a region to column 64 r + c / 2 of its 0-63 or
-//            128-191 band).
-//   phase 2  O = P . V in eight 64-dim blocks, each over the two token halves; A = P
-//            from TMEM, B = 64-token x 64-dim pieces (MN-major) of a stage; four O
-//            buffers (columns 64-127, 192-255, 320-383, 448-511) so the epilogue of
-//            block j overlaps the MMAs of blocks j+1 .. j+3.  The epilogue writes O / l
-//            as bf16 partials plus (m, l) per head, in the layout the combine reads.
-// Every load stage is 256 rows x 64 dims (32 KB; row r at 128 r, its 16-byte chunk c
-// at (c ^ (r & 7)) * 16): a K stage of phase 1 and a V stage of phase 2 differ only in
-// the dims and in how the MMA reads it, so both go through one ring of five slots
-// (160 KB in flight), and the V rows start loading as soon as phase 1 frees slots.
+//            (token t of region r to column 256 r + (t mod 256) / 2, so P fills the first
+//            128 columns of each region).
+//   phase 2  O = P . V in four 128-dim blocks, each over four 128-token quarters; A = P
+//            from TMEM, B = 16-token x 128-dim pieces (MN-major, two 64-dim atoms) of a
+//            stage; two O buffers (columns 128-255 and 384-511) so the epilogue of block
+//            j overlaps the MMAs of block j+1.  The epilogue writes O / l as bf16
+//            partials plus (m, l) per head, in the layout the combine reads.
+// Every load stage is 32 KB in 128-byte rows (row r at 128 r, its 16-byte chunk c at
+// (c ^ (r & 7)) * 16): a K stage of phase 1 is 256 rows x 64 dims, a V stage of phase 2
+// is two atoms of 128 rows x 64 dims (the block's two dim halves, 16 KB apart); both go
+// through one ring of five slots (160 KB in flight), and the V rows start loading as
+// soon as phase 1 frees slots.
 // Roles: warps 0-3 softmax of region 0 and the epilogues, warps 4-7 softmax of
 // region 1, warp 8 issues the MMAs from lane 0 and the Q chunks' TMA from lane 1
 // (three chunks ahead, apart from the row loads), warps 9-16 only load rows.  Each
@@ -215,13 +216,13 @@ constexpr int T2_QST = 3, T2_SLOTS = 5;
 constexpr int T2_QCH = 128 * 128;             // Q chunk bytes
 constexpr int T2_SCH = 256 * 128;             // stage: 256 rows x 64 dims
 constexpr int T2_NK = 18;                     // phase-1 stages: 9 chunks x 2 halves
-constexpr int T2_NS = T2_NK + 16;             // + phase-2 stages: 8 blocks x 2 halves
+constexpr int T2_NS = T2_NK + 16;             // + phase-2 stages: 4 blocks x 4 quarters
 constexpr int T2_SOFF = T2_QST * T2_QCH;
 constexpr int T2_REGION = T2_SOFF + T2_SLOTS * T2_SCH;     // 192 KB
 
 struct T2Shared {
   uint64_t qfull[T2_QST], qempty[T2_QST], full[T2_SLOTS], empty[T2_SLOTS];
-  uint64_t s_full, p_full, o_full[4], o_empty[4];
+  uint64_t s_full, p_full, o_full[2], o_empty[2];
   uint32_t tmem_base;
   int fail;
   int32_t slots[T2_T];
@@ -237,8 +238,7 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
 
 // TMEM column of the bf16 pair holding tokens t, t+1 (t even) of the 512 entries
 __device__ __forceinline__ uint32_t p2_col(int t) {
-  const int c = t & 255;
-  return (uint32_t)(256 * (t >> 8) + (c >> 1) + (c >= 128 ? 64 : 0));
+  return (uint32_t)(256 * (t >> 8) + ((t & 255) >> 1));
 }
 
 __global__ void __launch_bounds__(T2_THREADS, 1)
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     for (int i = 0; i < T2_SLOTS; ++i) { mbar_init(&S.full[i], T2_LOADERS); mbar_init(&S.empty[i], 1); }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, 256);
-    for (int i = 0; i < 4; ++i) { mbar_init(&S.o_full[i], 1); mbar_init(&S.o_empty[i], 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&S.o_full[i], 1); mbar_init(&S.o_empty[i], 128); }
     S.fail = 0;
     fence_mbar_init();
   }
@@ -293,17 +293,29 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < RPT; ++i) rows[h][i] = S.slots[h * 256 + r0 + 32 * i];
     for (int g = 0; g < T2_NS && ok; ++g) {
-      const int gg = g < T2_NK ? g : g - T2_NK;
-      const int dc = gg >> 1, half = gg & 1;           // dims 64 dc .., tokens 256 half ..
       const int sl = g % T2_SLOTS;
       if (!mbar_wait(&S.empty[sl], ((g / T2_SLOTS) & 1) ^ 1)) { ok = false; break; }
       unsigned char *sb = R + T2_SOFF + sl * T2_SCH;
+      if (g < T2_NK) {
+        const int dc = g >> 1, half = g & 1;           // dims 64 dc .., tokens 256 half ..
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        const int r = r0 + 32 * i;
-        const int32_t row = half ? rows[1][i] : rows[0][i];
-        const __nv_bfloat16 *src = kv + (int64_t)(row >= 0 ? row : 0) * KV_W + dc * 64 + c * 8;
-        cp_async_16(sb + r * 128 + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16u : 0u);
+        for (int i = 0; i < RPT; ++i) {
+          const int r = r0 + 32 * i;
+          const int32_t row = half ? rows[1][i] : rows[0][i];
+          const __nv_bfloat16 *src = kv + (int64_t)(row >= 0 ? row : 0) * KV_W + dc * 64 + c * 8;
+          cp_async_16(sb + r * 128 + ((c ^ (r & 7)) << 4), src, row >= 0 ? 16u : 0u);
+        }
+      } else {
+        // value stage: tokens 128 q .. of dims 128 j .., two 64-dim atoms of 128 rows
+        const int gv = g - T2_NK, j = gv >> 2, q = gv & 3;
+        const int cc = lt & 15, atom = cc >> 3, c2 = cc & 7, rr0 = lt >> 4;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const int r = rr0 + 16 * i;
+          const int32_t row = S.slots[128 * q + r];
+          const __nv_bfloat16 *src = kv + (int64_t)(row >= 0 ? row : 0) * KV_W + j * 128 + atom * 64 + c2 * 8;
+          cp_async_16(sb + atom * (128 * 128) + r * 128 + ((c2 ^ (r & 7)) << 4), src, row >= 0 ? 16u : 0u);
+        }
       }
       cp_async_arrive(&S.full[sl]);
     }
@@ -326,7 +338,7 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
     if (lane == 0) {
       // --------------------------------------------------------------- MMA --
       constexpr uint32_t id1 = instr_desc(FMT_BF16, FMT_BF16, 0, 0, 128, 256);
-      constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 64);
+      constexpr uint32_t id2 = instr_desc(FMT_BF16, FMT_BF16, 0, 1, 128, 128);
       for (int g = 0; g < T2_NS && ok; ++g) {
         const int sl = g % T2_SLOTS;
         const uint32_t sa = smem_u32(R + T2_SOFF + sl * T2_SCH);
@@ -352,24 +364,24 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             tc_fence_after();
           }
         } else {
-          // O_j += P[:, tokens of half] . V[those tokens, dims of block j]
-          const int gv = g - T2_NK, j = gv >> 1, half = gv & 1, ob = j & 3;
-          if (half == 0 && j >= 4) {                   // this buffer's previous block is written out
-            if (!mbar_wait(&S.o_empty[ob], ((j >> 2) - 1) & 1)) { ok = false; break; }
+          // O_j += P[:, tokens of quarter q] . V[those tokens, dims of block j]
+          const int gv = g - T2_NK, j = gv >> 2, q = gv & 3, ob = j & 1;
+          if (q == 0 && j >= 2) {                      // this buffer's previous block is written out
+            if (!mbar_wait(&S.o_empty[ob], ((j >> 1) - 1) & 1)) { ok = false; break; }
             tc_fence_after();
           }
           if (!mbar_wait(&S.full[sl], (g / T2_SLOTS) & 1)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t d = tmem + 64u + 128u * (uint32_t)ob;
+          const uint32_t d = tmem + 128u + 256u * (uint32_t)ob;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {               // 16 K-steps of 16 tokens
-            const int t0 = 256 * half + 16 * u;
-            const uint64_t bd = smem_desc(sa + (uint32_t)(u * 16 * 128), 8 * 1024, 1024, LAYOUT_SW128);
-            mma_f16_ts(d, tmem + p2_col(t0), bd, id2, (half | u) ? 1u : 0u);
+          for (int u = 0; u < 8; ++u) {                // 8 K-steps of 16 tokens; N = 128 dims in two atoms
+            const int t0 = 128 * q + 16 * u;
+            const uint64_t bd = smem_desc(sa + (uint32_t)(u * 16 * 128), 128 * 128, 1024, LAYOUT_SW128);
+            mma_f16_ts(d, tmem + p2_col(t0), bd, id2, (q | u) ? 1u : 0u);
           }
           mma_commit(&S.empty[sl]);
-          if (half == 1) mma_commit(&S.o_full[ob]);
+          if (q == 3) mma_commit(&S.o_full[ob]);
         }
       }
     }
@@ -432,18 +444,12 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
       // dims with heads innermost ([b][s][dim/8][head][8]): the 32 heads of a warp
       // write one contiguous 512-byte run per store
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      for (int j = 0; j < 8; ++j) {
-        const int ob = j & 3;
-        if (!mbar_wait(&S.o_full[ob], (j >> 2) & 1)) { ok = false; break; }
+      for (int j = 0; j < 4; ++j) {
+        const int ob = j & 1;
+        if (!mbar_wait(&S.o_full[ob], (j >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + j * 8) * 128 * 8 + (int64_t)hr * 8;
-        uint32_t r[32], r2[32];
-        const uint32_t oc = trow + 64u + 128u * (uint32_t)ob;
-        tmem_ld32(oc, r);
-        tmem_ld32(oc + 32, r2);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&S.o_empty[ob]);                   // the values are in registers
+        __nv_bfloat16 *dst = part.o + (((int64_t)b * nsplit + s) * 64 + j * 16) * 128 * 8 + (int64_t)hr * 8;
+        const uint32_t oc = trow + 128u + 256u * (uint32_t)ob;
         auto store_o = [&](int c0, const uint32_t (&v)[32]) {
           uint32_t pk[16];
 #pragma unroll
@@ -457,8 +463,18 @@ __global__ void __launch_bounds__(T2_THREADS, 1)
             *reinterpret_cast<uint4 *>(dst + (int64_t)((c0 >> 3) + q) * 128 * 8) =
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         };
-        store_o(0, r);
-        store_o(32, r2);
+        for (int hc = 0; hc < 2; ++hc) {               // the block's 128 columns in two halves
+          uint32_t r[32], r2[32];
+          tmem_ld32(oc + 64u * hc, r);
+          tmem_ld32(oc + 64u * hc + 32, r2);
+          tmem_wait_ld();
+          if (hc == 1) {
+            tc_fence_before();
+            mbar_arrive(&S.o_empty[ob]);               // the values are in registers
+          }
+          store_o(64 * hc, r);
+          store_o(64 * hc + 32, r2);
+        }
       }
       part.ml[(((int64_t)b * nsplit + s) * 128 + hr) * 2 + 0] = m == -INFINITY ? -INFINITY : m * scale;
       part.ml[(((int64_t)b * nsplit + s) * 128 + hr) * 2 + 1] = l;
