@@ -157,15 +157,17 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def kernel_traffic(kernel_src: str, workload: str):
+def kernel_traffic(kernel_src, workload: str):
     """DRAM bytes per launch of the indexer from the committed ncu summary, if it was
-    taken on the current source of the kernel (else None)."""
+    taken on the current source of the kernel (its file and the shared device header;
+    else None)."""
     p = os.path.join(ROOT, "profiles", "indexer_traffic.json")
     if not os.path.exists(p):
         return None, None
     with open(p) as f:
         d = json.load(f)
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    srcs = [kernel_src] if isinstance(kernel_src, str) else list(kernel_src)
+    h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
     if d.get("source_sha") != h:
         return None, "kernel changed since the ncu capture"
     per = d.get("per_workload", {}).get(workload)
@@ -599,8 +601,8 @@ def run_echo(args, ws, rank, local):
     ix_flat = [x for row in ix_samples for x in row]
     ix_avg_ms = statistics.median(ix_flat) if ix_flat else stages.get("index_prefetch_us", 0.0) / 1e3
     achieved = ix_bytes / (ix_avg_ms / 1e3) / 1e9 if ix_avg_ms else None
-    traffic, tnote = kernel_traffic(os.path.join(ROOT, "sparse_attention_kv_dsa_gb300", "csrc", "indexer.cu"),
-                                    wl.name)
+    csrc = os.path.join(ROOT, "sparse_attention_kv_dsa_gb300", "csrc")
+    traffic, tnote = kernel_traffic([os.path.join(csrc, "indexer.cu"), os.path.join(csrc, "common.cuh")], wl.name)
     sel_total = ctr_tot["hits"] + ctr_tot["staged_hits"] + ctr_tot["misses"]
     clocks = clk.summary()
     link = None if args.skip_host_link else host_link(dev)

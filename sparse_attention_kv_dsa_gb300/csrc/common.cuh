@@ -348,6 +348,21 @@ __device__ __forceinline__ void block_prefix(int n, F f, int32_t *pre) {
   __shared__ int32_t bp_warp[32];
   __shared__ int32_t bp_carry;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if (n <= 32) {                                   // a batch of requests: one warp, one barrier
+    if (wid == 0) {
+      const int v = lane < n ? f(lane) : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane < n) pre[lane] = x - v;
+      if (lane == 31) pre[n] = x;
+    }
+    __syncthreads();
+    return;
+  }
   if (threadIdx.x == 0) bp_carry = 0;
   __syncthreads();
   for (int base = 0; base < n; base += blockDim.x) {

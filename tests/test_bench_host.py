@@ -7,7 +7,7 @@ import os
 import bench
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-IX = os.path.join(ROOT, "sparse_attention_kv_dsa_gb300", "csrc", "indexer.cu")
+IX = [os.path.join(ROOT, "sparse_attention_kv_dsa_gb300", "csrc", f) for f in ("indexer.cu", "common.cuh")]
 
 
 def test_launches_per_step_follow_the_step_executor():
