@@ -36,3 +36,18 @@ def test_indexer_traffic_record_matches_the_current_source(monkeypatch):
     monkeypatch.setattr(bench.hashlib, "sha256", Other)
     traffic2, note2 = bench.kernel_traffic(IX, "saturated-b32-ctx80k-100k-4layer")
     assert traffic2 is None and "changed" in note2
+
+
+def test_step_roofline_sums_the_stage_ceilings():
+    from sparse_attention_kv_dsa_gb300 import synth as S
+    wl = S.workloads()["saturated-b32-ctx80k-100k-4layer"]
+    peaks = {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0, "source": "test"}
+    r = bench.step_roofline(wl, 90_000.0, 32 * 90_000.0 * 132, {"prefetched_rows": 0.0, "final_recall_rows": 0.0},
+                            None, peaks, 4, 1.0)
+    us = r["ceiling_us_per_layer"]
+    assert abs(us["indexer"] - 32 * 90_000 * 132 / 8e12 * 1e6) < 0.01          # 47.5 us
+    assert abs(us["topk"] - (4 * 32 * 90_000 + 8 * 32 * 2048) / 8e12 * 1e6) < 0.01
+    # sparse MLA: 18.3 GFLOP at 2 PFLOP/s (9.1 us) is below its 80 MB at 8 TB/s (10.0 us)
+    assert abs(us["sparse_mla"] - (32 * 2048 * 1152 + 32 * 128 * (576 + 512) * 2) / 8e12 * 1e6) < 0.01
+    assert abs(r["ceiling_ms_per_step"] - sum(us.values()) * 4 / 1e3) < 1e-3
+    assert r["frac"] == round(r["ceiling_ms_per_step"] / 1.0, 3)
