@@ -7,7 +7,12 @@ priorities, EMA thresholds, context lengths) and recomputes the whole step
   every step evicts: two steps, every attention head of one request per step and eight
   heads of two others.
 * the GQA workload (16 requests x 8 KV heads = 128 groups of 8 query heads, contexts
-  32K-48K), blocks of 16 tokens: one step, attention of eight groups.
+  32K-48K), blocks of 16 tokens: one step, attention of eight groups; the same with one
+  token per host index and slot, attention of six groups.
+* the saturated workload (32 requests at 80K-100K) with blocks of 64 tokens and the
+  bench's pool of 3125 blocks: one step, eight heads of three requests.
+The rows attention reads are checked against rows built from the inputs alone (the host
+pool as filled before any step, and the step inputs for the tokens written back since).
 """
 
 import numpy as np
@@ -22,12 +27,20 @@ from harness import check_gpu_maps, gpu_residency
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def build(wl, T, kb, n_gpu_blocks, steps_before, steps_total):
+def build(wl, T, kb, n_gpu_blocks, steps_before, steps_total, latents_on_gpu=False):
+    """latents_on_gpu: draw the host pool's latents with the GPU generator (fast at the
+    largest sizes; the oracle reads them back from the pool), then overwrite the context
+    keys with the CPU generator's, which the oracle regenerates."""
     from sparse_attention_kv_dsa_gb300.runtime import BlockDecodeLayer, StepInputs
     wl.layers = 1
     dev = torch.device("cuda")
-    dl = BlockDecodeLayer(wl, 0, T, kb, dev, n_gpu_blocks=n_gpu_blocks, gen_device="cpu")
-    inp = StepInputs(wl, 1, steps_total, dev, gen_device="cpu")
+    dl = BlockDecodeLayer(wl, 0, T, kb, dev, n_gpu_blocks=n_gpu_blocks,
+                          gen_device="cuda" if latents_on_gpu else "cpu")
+    if latents_on_gpu:
+        for b in range(wl.batch):
+            dl.idx_k[b, :wl.ctx[b]] = dl.to_ik(S.keys_for(wl, 0, b, wl.ctx[b], "cpu"))
+        torch.cuda.synchronize()
+    inp = StepInputs(wl, 1, steps_total, dev, gen_device="cpu")   # CPU streams: the oracle regenerates them
     for s in range(steps_before):
         dl.load_step_inputs(inp.q_ik[0][s], inp.new_ik_ik[0][s], inp.new_kv[0][s], inp.q_mla[0][s])
         dl.step()
@@ -38,6 +51,19 @@ def build(wl, T, kb, n_gpu_blocks, steps_before, steps_total):
         for b in range(wl.batch):
             keys[b] = np.concatenate([keys[b], nik[b:b + 1]])
     return dl, inp, keys
+
+
+def expected_rows(wl, dl, inp, b, toks, base):
+    """Latent rows of group b's tokens from the inputs alone: context tokens from the
+    host pool as filled before any step, later tokens from the step input that wrote
+    them back."""
+    toks = np.asarray(toks, dtype=np.int64)
+    ctx = wl.ctx[b]
+    out = dl.cache.host_kv[torch.from_numpy(base + np.minimum(toks, ctx - 1))].float().numpy()
+    for i, t in enumerate(toks):
+        if t >= ctx:
+            out[i] = inp.new_kv[0][int(t - ctx)][b].float().cpu().numpy()
+    return out
 
 
 def handoff_step(wl, dl, inp, s, keys, attn_groups, rng):
@@ -82,7 +108,6 @@ def handoff_step(wl, dl, inp, s, keys, attn_groups, rng):
     assert (ctr[8], ctr[10]) == (hits, ms), "hit / miss counters"
     # attention (and the rows it read) against the oracle over the host rows of the
     # oracle's selection; the host pool holds every token written so far
-    host = dl.cache.host_kv
     kv = dl.cache.gpu_kv
     slot = dl.slot_idx.cpu().numpy()
     qa = inp.q_mla[0][s].float().cpu().numpy()
@@ -91,12 +116,12 @@ def handoff_step(wl, dl, inp, s, keys, attn_groups, rng):
     for b, heads in attn_groups:
         L = int(seq[b])
         toks = O.block_tokens(r.sel[b], T, L)
-        rows = host[torch.from_numpy(bases[b] + toks)].float().numpy()
+        rows = expected_rows(wl, dl, inp, b, toks, bases[b])
         valid = slot[b] >= 0
         got = kv[torch.from_numpy(slot[b][valid]).long().cuda()].float().cpu().numpy()
         assert valid.sum() == toks.size
         gpu_toks = np.array([int(sel[b, j // T]) * T + j % T for j in np.nonzero(valid)[0]])
-        assert np.array_equal(got, host[torch.from_numpy(bases[b] + gpu_toks)].float().numpy()), "rows read"
+        assert np.array_equal(got, expected_rows(wl, dl, inp, b, gpu_toks, bases[b])), "rows read"
         if wl.kv_heads:
             o, l_ = O.sparse_gqa_decode(qa[b, heads], rows, wl.scale)
         else:
@@ -123,4 +148,23 @@ def test_gqa_groups_at_full_size_by_state_handoff():
     dl, inp, keys = build(wl, 16, 128, wl.n_gpu // 16, steps_before=2, steps_total=3)
     rng = np.random.default_rng(17)
     groups = [(int(n), np.arange(wl.h_q)) for n in rng.choice(wl.batch, 8, replace=False)]
+    assert handoff_step(wl, dl, inp, 2, keys, groups, rng) > 0
+
+
+def test_blocks_of_64_at_the_saturated_size():
+    # the launch configuration of bench.py --blocks 64: 32 requests at 80K-100K, 32 blocks
+    # of 64 tokens selected, a pool of 3125 blocks
+    wl = S.workloads()["saturated-b32-ctx80k-100k-4layer"]
+    dl, inp, keys = build(wl, 64, 32, wl.n_gpu // 64, steps_before=2, steps_total=3, latents_on_gpu=True)
+    rng = np.random.default_rng(64)
+    groups = [(int(b), rng.choice(wl.h_q, 8, replace=False)) for b in rng.choice(wl.batch, 3, replace=False)]
+    handoff_step(wl, dl, inp, 2, keys, groups, rng)
+
+
+def test_gqa_token_granular_at_full_size():
+    # the GQA workload with one token per host index and slot (bench.py --blocks 1)
+    wl = S.workloads()["gqa-b16x8kv-ctx32k-48k-2layer"]
+    dl, inp, keys = build(wl, 1, wl.topk, wl.n_gpu, steps_before=2, steps_total=3, latents_on_gpu=True)
+    rng = np.random.default_rng(65)
+    groups = [(int(n), np.arange(wl.h_q)) for n in rng.choice(wl.batch, 6, replace=False)]
     assert handoff_step(wl, dl, inp, 2, keys, groups, rng) > 0
