@@ -406,10 +406,12 @@ def mla(q, kv, idx, scale):
     return out, lse
 
 
-# bf16 k = 2048 / 600 / 300 / 2600: 8 / 3 / 2 / 11 splits of 256 entries (the combine
-# takes its register path up to 8 splits and its loop beyond)
+# bf16 k = 2048 / 300 / 600 / 1300 / 2600 / 4096 / 4700: 4 / 1 / 2 / 3 / 6 / 8 / 10 splits
+# of 512 entries (the combine takes its register path up to 8 splits and its loop beyond)
 @pytest.mark.parametrize("dtype,Hq,k", [(torch.bfloat16, 128, 2048), (torch.bfloat16, 128, 300),
-                                        (torch.bfloat16, 128, 600), (torch.bfloat16, 128, 2600),
+                                        (torch.bfloat16, 128, 600), (torch.bfloat16, 128, 1300),
+                                        (torch.bfloat16, 128, 2600), (torch.bfloat16, 128, 4096),
+                                        (torch.bfloat16, 128, 4700),
                                         (torch.float32, 16, 256), (torch.float32, 16, 77)])
 def test_mla_vs_oracle(dtype, Hq, k):
     B, N = 3, 5000
