@@ -606,6 +606,7 @@ def run_echo(args, ws, rank, local):
     sel_total = ctr_tot["hits"] + ctr_tot["staged_hits"] + ctr_tot["misses"]
     clocks = clk.summary()
     link = None if args.skip_host_link else host_link(dev)
+    alloc = None if args.skip_host_link else allocator_bench(dev)
     if rank != 0:
         return 0
     step_roof = step_roofline(wl, mean_ctx, ix_bytes, telemetry, link, peaks, layers, t_ms_max / args.steps)
@@ -654,6 +655,7 @@ def run_echo(args, ws, rank, local):
                           "that layer's recall time in the same step; median",
         "host_link": link,
         "recall_kernel_frac_of_host_link": (link["zero_copy_recall_gbs"] / link["memcpy_h2d_gbs"]) if link else None,
+        "allocator": alloc,
         "hit_rate": (ctr_tot["hits"] / sel_total) if sel_total else None,
         "hit_rate_after_prefetch": ((ctr_tot["hits"] + ctr_tot["staged_hits"]) / sel_total) if sel_total else None,
         "device_status": statuses,
@@ -818,6 +820,51 @@ def host_link(dev) -> dict:
     return {"memcpy_h2d_gbs": best, "zero_copy_recall_gbs": zc, "peak_gbs": max(best, zc), "recall_miss_sweep": sweep,
             "how": "1 GiB pinned cudaMemcpyAsync; echo_cache_recall of 256 .. 65536 missed 1152-B rows into an "
                    "empty pool (best of 3 each); the largest gives zero_copy_recall_gbs"}
+
+
+def allocator_bench(dev) -> dict:
+    """The cache's allocator alone, the analog of the pages' alloc + free microbenchmark:
+    on a full pool of 200,000 slots whose tokens were all last touched in an earlier step,
+    echo_cache_evict frees the n least recently used slots and echo_cache_alloc binds n new
+    host indices to free slots (each a cooperative launch; best of 5 per n)."""
+    import torch
+    import sparse_attention_kv_dsa_gb300.echo as E
+    i32 = torch.int32
+    n_gpu, n_host = 200_000, 260_000
+    layer = E.LayerCache(n_gpu, n_host, torch.bfloat16, dev)
+    layer.reset()
+    out = torch.empty(n_gpu, dtype=i32, device=dev)
+    E.cache_alloc(layer, torch.arange(n_gpu, dtype=i32, device=dev), torch.tensor([n_gpu], dtype=i32, device=dev), out)
+    torch.cuda.synchronize()
+    layer.counters[E.CTR_STEP] = 1            # the step after the fill: every slot may be evicted
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    nxt = n_gpu
+    rows = []
+    for n in (32, 512, 2048, 8192):
+        need = torch.tensor([n], dtype=i32, device=dev)
+        best = None
+        for _ in range(5):
+            hosts = torch.arange(nxt, nxt + n, dtype=i32, device=dev)
+            nxt += n
+            torch.cuda.synchronize()
+            e[0].record()
+            E.cache_evict(layer, need)
+            e[1].record()
+            E.cache_alloc(layer, hosts, need, out)
+            e[2].record()
+            torch.cuda.synchronize()
+            t = (e[0].elapsed_time(e[1]) * 1e3, e[1].elapsed_time(e[2]) * 1e3)
+            best = t if best is None or sum(t) < sum(best) else best
+        rows.append({"n": n, "evict_us": round(best[0], 1), "alloc_us": round(best[1], 1),
+                     "evict_alloc_us": round(sum(best), 1)})
+    status = layer.status()
+    del layer
+    torch.cuda.empty_cache()
+    return {"pool_slots": n_gpu, "sweep": rows, "status": status,
+            "how": "full pool of 200,000 slots; echo_cache_evict of the n least recently used, then "
+                   "echo_cache_alloc of n new host indices; best of 5 per n (the pages: alloc + free "
+                   "6-8 us on H20, context only)"}
 
 
 def run_compare_prefetch(args, local) -> int:
