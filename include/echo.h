@@ -272,6 +272,8 @@ echo_status_t echo_index_prefetch(const void *q, const float *w, const void *idx
  * theta[b] <- kth[b] if theta[b] == +inf, else alpha*kth[b] + (1-alpha)*theta[b]
  * (float32, each operation rounded, no fused multiply-add).
  *   scores [B,Lmax] float32; seq_len [B]; out_idx [B,k] int32; kth [B]; theta [B] in/out.
+ * kth's contents on entry (the previous step's k-th scores when the caller keeps the
+ * buffer) only size the search around theta: any value gives the same results.
  */
 echo_status_t echo_topk(const float *scores, const int32_t *seq_len, int32_t B, int32_t Lmax,
                         int32_t k, int32_t *out_idx, float *kth, float *theta, float alpha,

@@ -12,10 +12,11 @@
 // whose slices still fit in shared memory.  Each CTA holds the
 // order-preserving uint32 keys of a contiguous slice of the request's scores in
 // shared memory.  A first pass histograms a window of keys around the key of the EMA
-// threshold (the predicted k-th score) and lists, per warp and in token order, every
-// key from the window up; when the k-th key falls inside, one more 11-bit pass over
-// those lists finds the k-th largest key K* and the output is written from them,
-// otherwise an MSB-first radix select over every key (11 + 11 + 10 bit digits) does.
+// threshold (the predicted k-th score; the window's width follows the last call's
+// prediction error) and lists, per warp and in token order, every key from the window
+// up; when the k-th key falls inside, one more pass over those lists finds the k-th
+// largest key K* and the output is written from them, otherwise an MSB-first radix
+// select over every key (11 + 11 + 10 bit digits) does.
 // Each CTA histograms its slice and publishes the sums of its 32-bin groups; every CTA
 // finds a digit from the group sums of all eight, then from the 32 bins of the chosen
 // group, read through distributed shared memory, so every CTA derives the same digit
@@ -163,8 +164,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   // per-warp candidate lists (token, key) after the keys: lcap entries per warp
   int32_t *list_t = reinterpret_cast<int32_t *>(keys + (cached ? per_max : 0));
   uint32_t *list_k = reinterpret_cast<uint32_t *>(list_t + TK_WARPS * lcap);
-  // the threshold the indexer scored against, read before rank 0 updates it
+  // the threshold the indexer scored against, read before rank 0 updates it, and the
+  // previous call's k-th score, read before rank 0 replaces it (it sizes the window)
   const float theta_scored = (F.cap != nullptr && rank == 0) ? theta[b] : 0.f;
+  const float kth_hint = kth_out[b];
 
   if (L <= k) {
     // every token is selected; kth = smallest score
@@ -210,12 +213,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
 
   // ---- window pass around the predicted k-th key ----------------------------
   // The EMA threshold theta[b] predicts this step's k-th score.  One pass counts the
-  // keys above a window of 2^22 key values around it, histograms the window's keys in
-  // 2048 bins of 2048 values, and lists every key from the window up (token, key) per
-  // warp, in token order (warp w owns a contiguous part of the slice).  When the k-th
-  // key falls in the window and no list overflowed, the last 11-bit pass and the
-  // output read only the lists; otherwise the passes read every key.  Either way the
-  // result is the exact k-th key.
+  // keys above a window of key values around it, histograms the window's keys in 2048
+  // bins of 2^sb values, and lists every key from the window up (token, key) per warp,
+  // in token order (warp w owns a contiguous part of the slice).  The window's half
+  // width is 8x the distance between the prediction and the k-th key of the previous
+  // call (left in kth_out, read before this call replaces it), a power of two from
+  // 2^17 to 2^21 key values (2^21 without a finite previous key).  When the k-th key
+  // falls in the window and no list overflowed, the last sb-bit pass and the output
+  // read only the lists; otherwise the passes read every key.  Either way the result
+  // is the exact k-th key: the width only decides how much work the lists save.
   const int wspan = (n + TK_WARPS - 1) / TK_WARPS;
   const int s0 = min(n, warp * wspan), s1 = min(n, s0 + wspan);
   uint32_t prefix = 0, above = 0;
@@ -223,10 +229,18 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   bool use_list = false;
   uint32_t nl = 0;                                         // this warp's list length
   const float th_pred = theta[b];
+  int sb = 11;                                             // window bin width 2^sb
   if (isfinite(th_pred)) {                                // uniform across the cluster
     const uint32_t kt = f32_key(th_pred);
-    const uint32_t wlo = (kt > (1u << 21) ? kt - (1u << 21) : 0u) & ~((1u << 11) - 1u);
-    const uint64_t whi = (uint64_t)wlo + (1ull << 22);
+    if (isfinite(kth_hint)) {
+      const uint32_t kp = f32_key(kth_hint);
+      const uint64_t d8 = 8ull * (kt > kp ? kt - kp : kp - kt);
+      sb = 7;
+      while (sb < 11 && (1ull << (sb + 10)) < d8) ++sb;
+    }
+    const uint32_t half = 1u << (sb + 10);
+    const uint32_t wlo = (kt > half ? kt - half : 0u) & ~((1u << sb) - 1u);
+    const uint64_t whi = (uint64_t)wlo + 2ull * half;
     uint32_t *h = S.hist[0];
     for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
     __syncthreads();
@@ -241,7 +255,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
       const bool inw = i < s1 && kk >= wlo && (uint64_t)kk < whi;
       nab += ab ? 1u : 0u;                                 // per lane; summed over the warp below
       nwin += inw ? 1u : 0u;
-      if (inw) atomicAdd(&h[(kk - wlo) >> 11], 1u);
+      if (inw) atomicAdd(&h[(kk - wlo) >> sb], 1u);
       const uint32_t bal = __ballot_sync(0xffffffffu, ab || inw);
       if (ab || inw) {
         const uint32_t pos = nl + __popc(bal & lanemask_lt());
@@ -285,9 +299,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     const uint32_t tab = S.tot_s[0], tot = S.tot_s[1], ovf = S.tot_s[2];
     if (tab < (uint32_t)k && (uint32_t)k <= tab + tot) {   // the k-th key is in the window
       tk_find<CL>(h, S.coarse[0], (uint32_t)k - tab, S.res);
-      prefix = wlo + (S.res[0] << 11);
+      prefix = wlo + (S.res[0] << sb);
       above = tab + S.res[1];
-      left = 11;
+      left = sb;
       use_list = lcap > 0 && ovf == 0;                     // uniform: every CTA read every flag
     }
     buf = 1;                        // other CTAs may still read hist[0]
@@ -295,7 +309,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
   }
 
   if (use_list) {
-    // ---- last 11-bit pass over the lists: the keys of the chosen window bin ----
+    // ---- last sb-bit pass over the lists: the keys of the chosen window bin ----
     uint32_t *h = S.hist[buf];
     for (int i = tid; i < TK_BINS; i += TK_THREADS) h[i] = 0;
     __syncthreads();
@@ -304,7 +318,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(TK_THREADS, 2)
     for (uint32_t j0 = 0; j0 < nl; j0 += 32) {              // warp-uniform trip count
       const uint32_t j = j0 + lane;
       const uint32_t kk = j < nl ? lk[j] : 0u;
-      hist_add_warp(h, j < nl && (kk >> 11) == (prefix >> 11), kk & 2047u);   // one bin's keys: ties are common
+      hist_add_warp(h, j < nl && (kk >> sb) == (prefix >> sb), kk & ((1u << sb) - 1u));   // one bin's keys: ties are common
     }
     __syncthreads();
     tk_coarse(h, S.coarse[buf]);

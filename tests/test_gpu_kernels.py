@@ -80,7 +80,7 @@ def test_indexer_fp8_extreme_grid_values():
 
 
 # -------------------------------------------------------------------- top-k --
-def run_topk(scores_list, k, theta0, alpha=0.5):
+def run_topk(scores_list, k, theta0, alpha=0.5, kth0=None):
     B = len(scores_list)
     Lmax = max(max(len(s) for s in scores_list), 1)
     sc = torch.full((B, Lmax), -123.0)
@@ -89,15 +89,15 @@ def run_topk(scores_list, k, theta0, alpha=0.5):
     sc = sc.to(dev)
     seq = torch.tensor([len(s) for s in scores_list], dtype=torch.int32, device=dev)
     out = torch.full((B, k), -5, dtype=torch.int32, device=dev)
-    kth = torch.empty(B, device=dev)
+    kth = torch.empty(B, device=dev) if kth0 is None else torch.tensor(kth0, dtype=torch.float32, device=dev)
     theta = torch.tensor(theta0, dtype=torch.float32, device=dev)
     E.topk(sc, seq, k, out, kth, theta, alpha)
     torch.cuda.synchronize()
     return out.cpu().numpy(), kth.cpu().numpy(), theta.cpu().numpy()
 
 
-def check_topk(scores_list, k, theta0, alpha=0.5):
-    out, kth, theta = run_topk(scores_list, k, theta0, alpha)
+def check_topk(scores_list, k, theta0, alpha=0.5, kth0=None):
+    out, kth, theta = run_topk(scores_list, k, theta0, alpha, kth0)
     for b, s in enumerate(scores_list):
         s = np.asarray(s, dtype=np.float32)
         sel, kv = O.topk_select(s, k)
@@ -167,6 +167,18 @@ def test_topk_candidate_lists_and_their_fallbacks():
     c = (2.5 + rng.integers(-8, 8, L) / 4096.0).astype(np.float32)         # all in the window
     # windows above and below the k-th key: full passes
     check_topk([a, b, c, a, a], 2048, [15.6, 2.0, 2.5, 60.0, 1.0])
+
+
+def test_topk_window_width_from_the_previous_kth():
+    # the k-th score left in kth by the previous call sizes the window around theta:
+    # no hint (NaN, -inf), a hint at theta (the narrowest window, 2^17 keys each side;
+    # the k-th key just inside it), a hint at theta whose window misses the k-th key (full
+    # passes), and a far hint (the widest window) all give the exact selection
+    rng = np.random.default_rng(9)
+    a = (rng.integers(0, 2 ** 14, 100_000) / 1024.0).astype(np.float32)  # k-th near 15.7
+    rows = [a] * 6
+    check_topk(rows, 2048, [15.6, 15.6, 15.6, 15.0, 15.6, 16.2],
+               kth0=[math.nan, -math.inf, 15.6, 15.0, 1.0, 16.2])
 
 
 def test_topk_large_context_k2048():
