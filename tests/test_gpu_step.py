@@ -58,6 +58,16 @@ def test_fp8_cap_binds_through_separate_entry_points(defer_cap):
     assert ctr[15] > ctr[12], "qualifying tokens did not exceed the cap"
 
 
+# a pool of at least ECHO_PENDING_LIST_MIN_SLOTS slots under eviction pressure: the recall's
+# victim selection finishes on the candidate list of its first radix pass
+@pytest.mark.parametrize("prefetch", [True, False])
+def test_fp8_large_pool_evictions(prefetch):
+    wl = S.small_workload("fp8-bigpool", ctx=(9000, 7000, 8100), topk=2048, n_gpu=14336, steps=7, cap_max=256,
+                          rho=0.6)
+    ls, st = run(wl, prefetch=prefetch)
+    assert ls.dl.cache.read_counters()[11] > 0, "the recall never evicted"
+
+
 @pytest.mark.parametrize("slack", [4, 300])
 def test_fp8_adaptive_cap(slack):
     # the cap follows the last step's transfer and prediction error (small slack: it
